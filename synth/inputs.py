@@ -1,0 +1,200 @@
+"""Seeded synthetic inputs for the attention workloads.
+
+Draws come from numpy's Philox counter-based generator, keyed by
+``(seed, stream_id)`` so that every tensor of a workload has its own
+independent, reproducible stream. Normal draws are fp64; they are rounded
+to the dtype the kernel reads (fp32, or bf16 by round-to-nearest-even via
+fp32) *before* either side sees them, and the oracle receives the rounded
+values widened back to fp64.
+
+Nothing here computes attention: no dot product, softmax or normalisation.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+# Stream ids: one independent substream per tensor of a workload.
+STREAM_Q, STREAM_K, STREAM_V = 0, 1, 2
+STREAM_XQ, STREAM_XKV = 3, 4
+STREAM_WQ, STREAM_WK, STREAM_WV, STREAM_WO = 5, 6, 7, 8
+STREAM_KEYLEN = 9
+
+MASK_NONE = 0
+MASK_CAUSAL = 1
+MASK_KEY_PADDING = 2
+
+
+def _rng(seed: int, stream: int) -> np.random.Generator:
+    return np.random.Generator(np.random.Philox(np.random.SeedSequence([int(seed), int(stream)])))
+
+
+def draw_normal(seed: int, stream: int, shape, std: float = 1.0) -> np.ndarray:
+    """i.i.d. N(0, std^2) draws in fp64."""
+    x = _rng(seed, stream).standard_normal(size=shape, dtype=np.float64)
+    if std != 1.0:
+        x *= std
+    return x
+
+
+def draw_key_lens(seed: int, stream: int, batch: int, lo: int, hi: int) -> np.ndarray:
+    """One integer key length per batch element, uniform on [lo, hi] inclusive."""
+    return _rng(seed, stream).integers(lo, hi + 1, size=batch, dtype=np.int64).astype(np.int32)
+
+
+def round_to_f32(x: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(x, dtype=np.float64).astype(np.float32)
+
+
+def round_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """fp64 -> fp32 (RNE) -> bf16 (RNE); returns the bf16 bit patterns as uint16."""
+    u = round_to_f32(x).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    rounded = (u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)
+    return rounded.astype(np.uint16)
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns exactly to fp64."""
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One synthetic attention (or MHA sublayer) problem.
+
+    Layout of every activation is [B, n, h, d] (heads concatenated along the
+    feature axis), which is also the row-major [B*n, h*d] matrix X.W gives.
+    """
+
+    name: str
+    dtype: str  # "f32" or "bf16"
+    B: int
+    h: int
+    n_q: int
+    n_k: int
+    d_k: int
+    d_v: int
+    mask_kind: int
+    seed: int
+    key_len_range: tuple | None = None  # inclusive (lo, hi) when KEY_PADDING
+    d_model: int = 0  # > 0 for the MHA sublayer
+    description: str = ""
+
+    @property
+    def scale(self) -> float:
+        """1/sqrt(d_k), as the fp32 value passed to the kernels."""
+        return float(np.float32(1.0 / math.sqrt(self.d_k)))
+
+    @property
+    def is_mha(self) -> bool:
+        return self.d_model > 0
+
+    def attn_flops(self) -> float:
+        """4*B*h*n_q*n_k*d, halved for causal (the defined metric's FLOP count)."""
+        f = 4.0 * self.B * self.h * self.n_q * self.n_k * self.d_k
+        return f * 0.5 if self.mask_kind & MASK_CAUSAL else f
+
+    def proj_flops(self) -> float:
+        if not self.is_mha:
+            return 0.0
+        hd = self.h * self.d_k
+        return 2.0 * self.B * (self.n_q * self.d_model * hd + 2 * self.n_k * self.d_model * hd
+                               + self.n_q * self.h * self.d_v * self.d_model)
+
+    def tokens(self) -> int:
+        return self.B * self.n_q
+
+    def with_(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+WORKLOADS = {
+    "enc_self_f32": Workload(
+        "enc_self_f32", "f32", B=2, h=8, n_q=64, n_k=64, d_k=64, d_v=64,
+        mask_kind=MASK_NONE, seed=0,
+        description="encoder self-attention, fp32, B=2 h=8 n=64 d=64, unmasked"),
+    "dec_causal_bf16": Workload(
+        "dec_causal_bf16", "bf16", B=32, h=8, n_q=100, n_k=100, d_k=64, d_v=64,
+        mask_kind=MASK_CAUSAL, seed=1,
+        description="decoder masked self-attention, bf16, B=32 h=8 n=100 d=64, causal"),
+    "cross_bf16": Workload(
+        "cross_bf16", "bf16", B=64, h=8, n_q=128, n_k=256, d_k=64, d_v=64,
+        mask_kind=MASK_KEY_PADDING, seed=2, key_len_range=(64, 256),
+        description="cross-attention, bf16, B=64 h=8 n_q=128 n_k=256 d=64, key lengths U[64,256]"),
+    "mha_bf16": Workload(
+        "mha_bf16", "bf16", B=16, h=8, n_q=512, n_k=512, d_k=64, d_v=64,
+        mask_kind=MASK_NONE, seed=3, d_model=512,
+        description="post-norm MHA sublayer, bf16, B=16 n=512 d_model=512 h=8 d=64"),
+    "long_causal_d128": Workload(
+        "long_causal_d128", "bf16", B=4, h=16, n_q=8192, n_k=8192, d_k=128, d_v=128,
+        mask_kind=MASK_CAUSAL, seed=4,
+        description="long-sequence causal self-attention, bf16, B=4 h=16 n=8192 d=128"),
+    "long_causal_d64": Workload(
+        "long_causal_d64", "bf16", B=4, h=32, n_q=8192, n_k=8192, d_k=64, d_v=64,
+        mask_kind=MASK_CAUSAL, seed=5,
+        description="long-sequence causal self-attention, bf16, B=4 h=32 n=8192 d=64"),
+}
+
+
+def workload(name: str) -> Workload:
+    return WORKLOADS[name]
+
+
+def _to_kernel_dtype(x: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "f32":
+        return round_to_f32(x)
+    if dtype == "bf16":
+        return round_to_bf16_bits(x)
+    raise ValueError(dtype)
+
+
+def widen(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Kernel-dtype array (fp32, or bf16 bits) -> exact fp64 copy for the oracle."""
+    if dtype == "f32":
+        return x.astype(np.float64)
+    return bf16_bits_to_f64(x)
+
+
+def attn_inputs(w: Workload) -> dict:
+    """Q, K, V in [B, n, h, d] at the kernel dtype (fp32 arrays or bf16 bits), plus key lengths."""
+    out = {
+        "q": _to_kernel_dtype(draw_normal(w.seed, STREAM_Q, (w.B, w.n_q, w.h, w.d_k)), w.dtype),
+        "k": _to_kernel_dtype(draw_normal(w.seed, STREAM_K, (w.B, w.n_k, w.h, w.d_k)), w.dtype),
+        "v": _to_kernel_dtype(draw_normal(w.seed, STREAM_V, (w.B, w.n_k, w.h, w.d_v)), w.dtype),
+        "key_lens": None,
+    }
+    if w.mask_kind & MASK_KEY_PADDING:
+        lo, hi = w.key_len_range if w.key_len_range else (1, w.n_k)
+        out["key_lens"] = draw_key_lens(w.seed, STREAM_KEYLEN, w.B, lo, hi)
+    return out
+
+
+def mha_inputs(w: Workload, self_attention: bool = True) -> dict:
+    """X (and X_kv), the four projection matrices ~ N(0, 1/d_model), gamma=1, beta=0."""
+    dm, hdk, hdv = w.d_model, w.h * w.d_k, w.h * w.d_v
+    wstd = 1.0 / math.sqrt(dm)
+    x_q = _to_kernel_dtype(draw_normal(w.seed, STREAM_XQ, (w.B, w.n_q, dm)), w.dtype)
+    if self_attention:
+        x_kv = x_q
+    else:
+        x_kv = _to_kernel_dtype(draw_normal(w.seed, STREAM_XKV, (w.B, w.n_k, dm)), w.dtype)
+    out = {
+        "x_q": x_q,
+        "x_kv": x_kv,
+        "wq": _to_kernel_dtype(draw_normal(w.seed, STREAM_WQ, (dm, hdk), wstd), w.dtype),
+        "wk": _to_kernel_dtype(draw_normal(w.seed, STREAM_WK, (dm, hdk), wstd), w.dtype),
+        "wv": _to_kernel_dtype(draw_normal(w.seed, STREAM_WV, (dm, hdv), wstd), w.dtype),
+        "wo": _to_kernel_dtype(draw_normal(w.seed, STREAM_WO, (hdv, dm), wstd), w.dtype),
+        "gamma": np.ones(dm, dtype=np.float32),
+        "beta": np.zeros(dm, dtype=np.float32),
+        "eps": 1e-6,
+        "key_lens": None,
+    }
+    if w.mask_kind & MASK_KEY_PADDING:
+        lo, hi = w.key_len_range if w.key_len_range else (1, w.n_k)
+        out["key_lens"] = draw_key_lens(w.seed, STREAM_KEYLEN, w.B, lo, hi)
+    return out
