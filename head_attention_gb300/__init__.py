@@ -1,0 +1,25 @@
+"""hattn: multi-head scaled dot-product attention for NVIDIA GB300 (sm_103a).
+
+The compute path is libhattn.so (hand-written tcgen05/TMA CUDA kernels behind
+a C ABI declared in include/hattn.h); this package only builds it and binds it.
+"""
+
+from ._binding import (  # noqa: F401
+    EXPORTED,
+    HATTN_BF16,
+    HATTN_F32,
+    MASK_CAUSAL,
+    MASK_KEY_PADDING,
+    MASK_NONE,
+    HattnError,
+    attn_fwd,
+    attn_fwd_raw,
+    check_device_error,
+    load,
+    mha_fwd,
+    mha_fwd_raw,
+    mha_workspace_bytes,
+    status_str,
+    version,
+)
+from .builder import build  # noqa: F401

@@ -1,0 +1,163 @@
+"""ctypes binding of libhattn.so: argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+turns torch tensors into raw device pointers and sizes, calls the C ABI and
+turns status codes into exceptions. There is no fallback path: if the library
+is missing, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import builder as _build
+
+HATTN_F32, HATTN_BF16 = 0, 1
+MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING = 0, 1, 2
+OK, EINVAL, EUNSUPPORTED, ECUDA, ETIMEOUT, EKEYLEN, EWORKSPACE = 0, -1, -2, -3, -4, -5, -6
+
+# Every symbol include/hattn.h declares.
+EXPORTED = ("attn_fwd", "mha_fwd", "mha_workspace_bytes", "hattn_status_str",
+            "hattn_check_device_error", "hattn_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class HattnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_str(status)} ({status})")
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Loads libhattn.so (built in-tree by head_attention_gb300.build)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with head_attention_gb300.build()")
+        lib = ctypes.CDLL(path)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.attn_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, vp]
+        lib.attn_fwd.restype = i
+        lib.mha_fwd.argtypes = [vp] * 8 + [f, vp, i, i, i, i, i, i, i, i, i, vp, vp, sz, vp]
+        lib.mha_fwd.restype = i
+        lib.mha_workspace_bytes.argtypes = [i] * 8
+        lib.mha_workspace_bytes.restype = sz
+        lib.hattn_status_str.argtypes = [i]
+        lib.hattn_status_str.restype = ctypes.c_char_p
+        lib.hattn_check_device_error.argtypes = [vp]
+        lib.hattn_check_device_error.restype = i
+        lib.hattn_version.argtypes = []
+        lib.hattn_version.restype = i
+        _lib = lib
+        return lib
+
+
+def status_str(status: int) -> str:
+    return load().hattn_status_str(int(status)).decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return HATTN_F32
+    if t.dtype == torch.bfloat16:
+        return HATTN_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def attn_fwd_raw(q, k, v, out, dtype, B, h, n_q, n_k, d_k, d_v, scale, mask_kind, key_lens,
+                 stream) -> int:
+    """The C entry point with raw pointers (ints) or tensors; returns the status code."""
+    return load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), int(dtype), int(B), int(h),
+                           int(n_q), int(n_k), int(d_k), int(d_v), float(scale), int(mask_kind),
+                           _ptr(key_lens), _stream(stream))
+
+
+def attn_fwd(q, k, v, out=None, scale=None, mask_kind=MASK_NONE, key_lens=None, stream=None):
+    """Multi-head attention on [B, n, h, d] CUDA tensors (fp32 or bf16). Returns out."""
+    import torch
+    B, n_q, h, d_k = q.shape
+    n_k, d_v = k.shape[1], v.shape[3]
+    if out is None:
+        out = torch.empty((B, n_q, h, d_v), dtype=q.dtype, device=q.device)
+    if scale is None:
+        scale = d_k ** -0.5
+    for t in (q, k, v, out):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("attn_fwd needs contiguous CUDA tensors")
+    rc = attn_fwd_raw(q, k, v, out, _dtype_code(q), B, h, n_q, n_k, d_k, d_v, scale, mask_kind,
+                      key_lens, stream)
+    if rc != OK:
+        raise HattnError(rc, "attn_fwd")
+    return out
+
+
+def mha_workspace_bytes(dtype, B, n_q, n_k, d_model, h, d_k, d_v) -> int:
+    return int(load().mha_workspace_bytes(int(dtype), int(B), int(n_q), int(n_k), int(d_model),
+                                          int(h), int(d_k), int(d_v)))
+
+
+def mha_fwd_raw(x_q, x_kv, wq, wk, wv, wo, gamma, beta, eps, y, dtype, B, n_q, n_k, d_model, h,
+                d_k, d_v, mask_kind, key_lens, workspace, ws_bytes, stream) -> int:
+    return load().mha_fwd(_ptr(x_q), _ptr(x_kv), _ptr(wq), _ptr(wk), _ptr(wv), _ptr(wo),
+                          _ptr(gamma), _ptr(beta), float(eps), _ptr(y), int(dtype), int(B),
+                          int(n_q), int(n_k), int(d_model), int(h), int(d_k), int(d_v),
+                          int(mask_kind), _ptr(key_lens), _ptr(workspace), int(ws_bytes),
+                          _stream(stream))
+
+
+def mha_fwd(x_q, x_kv, wq, wk, wv, wo, gamma, beta, eps, h, y=None, mask_kind=MASK_NONE,
+            key_lens=None, workspace=None, stream=None):
+    """Post-norm MHA sublayer on bf16 CUDA tensors x_q [B, n_q, d_model], x_kv [B, n_k, d_model]."""
+    import torch
+    B, n_q, d_model = x_q.shape
+    n_k = x_kv.shape[1]
+    d_k = wq.shape[1] // h
+    d_v = wv.shape[1] // h
+    if y is None:
+        y = torch.empty_like(x_q)
+    need = mha_workspace_bytes(HATTN_BF16, B, n_q, n_k, d_model, h, d_k, d_v)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x_q.device)
+    rc = mha_fwd_raw(x_q, x_kv, wq, wk, wv, wo, gamma, beta, eps, y, _dtype_code(x_q), B, n_q, n_k,
+                     d_model, h, d_k, d_v, mask_kind, key_lens, workspace, workspace.numel(),
+                     stream)
+    if rc != OK:
+        raise HattnError(rc, "mha_fwd")
+    return y
+
+
+def check_device_error(stream=None) -> int:
+    return int(load().hattn_check_device_error(_stream(stream)))
+
+
+def version() -> int:
+    return int(load().hattn_version())

@@ -1,0 +1,348 @@
+// C ABI of libhattn.so: argument validation, kernel dispatch, tensor-map
+// construction and caching, and the device error word. See include/hattn.h
+// for the contract of every entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "internal.h"
+
+namespace hattn {
+
+// First device-side error raised by a kernel of this library on this device.
+__device__ int g_device_error = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int* device_error_ptr()
+{
+    static int* cache[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<int*>(p);
+    }
+    return cache[dev];
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Tensor maps depend only on (pointer, shape, box); cache them so repeated
+// calls on the same buffers skip the host-side encode.
+struct MapKey {
+    const void* base;
+    uint64_t dims[4];
+    uint32_t box_rows;
+    int rank;
+    bool operator==(const MapKey& o) const
+    {
+        return base == o.base && rank == o.rank && box_rows == o.box_rows &&
+               std::memcmp(dims, o.dims, sizeof(dims)) == 0;
+    }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey& k) const
+    {
+        size_t h = std::hash<const void*>()(k.base);
+        for (int i = 0; i < 4; ++i) h = h * 1000003u ^ std::hash<uint64_t>()(k.dims[i]);
+        return h * 31u + k.box_rows * 7u + k.rank;
+    }
+};
+std::mutex g_map_mu;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+constexpr size_t kMaxCachedMaps = 4096;
+
+bool cached_map(CUtensorMap* out, const MapKey& key, bool (*make)(CUtensorMap*, const MapKey&))
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    MapKey k = key;
+    k.dims[3] ^= static_cast<uint64_t>(dev) << 48;  // maps are per device
+    {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        auto it = g_maps.find(k);
+        if (it != g_maps.end()) {
+            *out = it->second;
+            return true;
+        }
+    }
+    if (!make(out, key)) return false;
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    if (g_maps.size() >= kMaxCachedMaps) g_maps.clear();
+    g_maps.emplace(k, *out);
+    return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? HATTN_OK : HATTN_ECUDA; }
+
+bool make_bnhd_uncached(CUtensorMap* map, const MapKey& k)
+{
+    // dims = {d, h, n, B}
+    const uint64_t d = k.dims[0], h = k.dims[1], n = k.dims[2], B = k.dims[3];
+    const uint64_t dims[4] = {d, h, n, B};
+    const uint64_t strides[3] = {d * 2, h * d * 2, n * h * d * 2};
+    const uint32_t box[4] = {64, 1, k.box_rows, 1};
+    return encode_tmap(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, k.base, dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool make_2d_uncached(CUtensorMap* map, const MapKey& k)
+{
+    // dims = {cols, rows}, box = {64, box_rows}
+    const uint64_t dims[2] = {k.dims[0], k.dims[1]};
+    const uint64_t strides[1] = {k.dims[0] * 2};
+    const uint32_t box[2] = {64, k.box_rows};
+    return encode_tmap(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k.base, dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Row-major bf16 [rows][cols] matrix, boxes of 64 columns x box_rows rows.
+bool make_2d_map(CUtensorMap* map, const void* base, int rows, int cols, int box_rows)
+{
+    MapKey k{base, {(uint64_t)cols, (uint64_t)rows, 0, 0}, (uint32_t)box_rows, 2};
+    return cached_map(map, k, make_2d_uncached);
+}
+
+}  // namespace
+
+bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                 CUtensorMapSwizzle swizzle)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t gdim[5], gstride[4];
+    cuuint32_t bdim[5], estride[5];
+    for (int i = 0; i < rank; ++i) {
+        gdim[i] = dims[i];
+        bdim[i] = box[i];
+        estride[i] = 1;
+    }
+    for (int i = 0; i < rank - 1; ++i) gstride[i] = strides_bytes[i];
+    CUresult r = fn(map, dtype, rank, const_cast<void*>(base), gdim, gstride, bdim, estride,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int n, int h, int d, int box_rows)
+{
+    MapKey k{base, {(uint64_t)d, (uint64_t)h, (uint64_t)n, (uint64_t)B}, (uint32_t)box_rows, 4};
+    return cached_map(map, k, make_bnhd_uncached);
+}
+
+namespace {
+
+int validate_attn(const void* q, const void* k, const void* v, void* out, int dtype, int B, int h,
+                  int n_q, int n_k, int d_k, int d_v, float scale, int mask_kind,
+                  const int32_t* key_lens)
+{
+    if (!q || !k || !v || !out) return HATTN_EINVAL;
+    if (dtype != HATTN_F32 && dtype != HATTN_BF16) return HATTN_EINVAL;
+    if (B <= 0 || h <= 0 || n_q <= 0 || n_k <= 0 || d_k <= 0 || d_v <= 0) return HATTN_EINVAL;
+    if (mask_kind & ~(HATTN_MASK_CAUSAL | HATTN_MASK_KEY_PADDING)) return HATTN_EINVAL;
+    if ((mask_kind & HATTN_MASK_CAUSAL) && n_q != n_k) return HATTN_EINVAL;
+    if ((mask_kind & HATTN_MASK_KEY_PADDING) && !key_lens) return HATTN_EINVAL;
+    if (!std::isfinite(scale)) return HATTN_EINVAL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return HATTN_EINVAL;
+    const size_t esz = dtype == HATTN_F32 ? 4 : 2;
+    if ((d_k * esz) % 16 != 0 || (d_v * esz) % 16 != 0) return HATTN_EINVAL;
+    if (dtype == HATTN_F32 && (d_k > 128 || d_v > 128)) return HATTN_EUNSUPPORTED;
+    if (dtype == HATTN_BF16 && (d_k > 256 || d_v > 256)) return HATTN_EUNSUPPORTED;
+    return HATTN_OK;
+}
+
+int run_attn(const AttnArgs& a)
+{
+    if (attn_tc_supported(a)) {
+        AttnMaps m;
+        if (!make_bnhd_map(&m.q, a.q, a.B, a.n_q, a.h, a.d_k, 128) ||
+            !make_bnhd_map(&m.k, a.k, a.B, a.n_k, a.h, a.d_k, 128) ||
+            !make_bnhd_map(&m.v, a.v, a.B, a.n_k, a.h, a.d_v, 128))
+            return HATTN_ECUDA;
+        return from_cuda(launch_attn_tc(a, m));
+    }
+    if (a.h > 65535 || a.B > 65535) return HATTN_EUNSUPPORTED;
+    return from_cuda(launch_attn_simt(a));
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct MhaLayout {
+    size_t q, k, v, a, total;
+};
+
+bool mha_layout(int B, int n_q, int n_k, int h, int d_k, int d_v, MhaLayout* L)
+{
+    if (B <= 0 || n_q <= 0 || n_k <= 0 || h <= 0 || d_k <= 0 || d_v <= 0) return false;
+    const size_t q = (size_t)B * n_q * h * d_k * 2, k = (size_t)B * n_k * h * d_k * 2;
+    const size_t v = (size_t)B * n_k * h * d_v * 2, a = (size_t)B * n_q * h * d_v * 2;
+    L->q = 0;
+    L->k = L->q + align256(q);
+    L->v = L->k + align256(k);
+    L->a = L->v + align256(v);
+    L->total = L->a + align256(a);
+    return true;
+}
+
+}  // namespace
+}  // namespace hattn
+
+using namespace hattn;
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* out, int dtype, int B, int h,
+             int n_q, int n_k, int d_k, int d_v, float scale, int mask_kind,
+             const int32_t* key_lens, hattn_stream_t stream)
+{
+    int rc = validate_attn(q, k, v, out, dtype, B, h, n_q, n_k, d_k, d_v, scale, mask_kind,
+                           key_lens);
+    if (rc != HATTN_OK) return rc;
+    AttnArgs a{q, k, v, out, dtype, B, h, n_q, n_k, d_k, d_v, scale, mask_kind,
+               (mask_kind & HATTN_MASK_KEY_PADDING) ? key_lens : nullptr,
+               reinterpret_cast<cudaStream_t>(stream), device_error_ptr()};
+    if (!a.err_word) return HATTN_ECUDA;
+    return run_attn(a);
+}
+
+size_t mha_workspace_bytes(int dtype, int B, int n_q, int n_k, int d_model, int h, int d_k,
+                           int d_v)
+{
+    MhaLayout L;
+    if (dtype != HATTN_BF16 || d_model <= 0 || !mha_layout(B, n_q, n_k, h, d_k, d_v, &L)) return 0;
+    return L.total;
+}
+
+int mha_fwd(const void* x_q, const void* x_kv, const void* Wq, const void* Wk, const void* Wv,
+            const void* Wo, const float* gamma, const float* beta, float eps, void* y, int dtype,
+            int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v, int mask_kind,
+            const int32_t* key_lens, void* workspace, size_t ws_bytes, hattn_stream_t stream)
+{
+    if (!x_q || !x_kv || !Wq || !Wk || !Wv || !Wo || !gamma || !beta || !y) return HATTN_EINVAL;
+    if (dtype != HATTN_BF16) return dtype == HATTN_F32 ? HATTN_EUNSUPPORTED : HATTN_EINVAL;
+    if (B <= 0 || n_q <= 0 || n_k <= 0 || d_model <= 0 || h <= 0 || d_k <= 0 || d_v <= 0)
+        return HATTN_EINVAL;
+    if (mask_kind & ~(HATTN_MASK_CAUSAL | HATTN_MASK_KEY_PADDING)) return HATTN_EINVAL;
+    if ((mask_kind & HATTN_MASK_CAUSAL) && n_q != n_k) return HATTN_EINVAL;
+    if ((mask_kind & HATTN_MASK_KEY_PADDING) && !key_lens) return HATTN_EINVAL;
+    if (!(eps > 0.0f) || !std::isfinite(eps)) return HATTN_EINVAL;
+    const void* ptrs[] = {x_q, x_kv, Wq, Wk, Wv, Wo, gamma, beta, y};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return HATTN_EINVAL;
+    if (d_k != d_v || (d_k != 64 && d_k != 128)) return HATTN_EUNSUPPORTED;
+    if (d_model % 64 != 0 || d_model > 512 || (h * d_k) % 64 != 0) return HATTN_EUNSUPPORTED;
+    MhaLayout L;
+    if (!mha_layout(B, n_q, n_k, h, d_k, d_v, &L)) return HATTN_EINVAL;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || ws_bytes < L.total)
+        return HATTN_EWORKSPACE;
+    int* err = device_error_ptr();
+    if (!err) return HATTN_ECUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    void* Q = ws + L.q;
+    void* K = ws + L.k;
+    void* V = ws + L.v;
+    void* A = ws + L.a;
+    const int Mq = B * n_q, Mk = B * n_k, hdk = h * d_k, hdv = h * d_v;
+
+    ProjProblem pr[3];
+    const void* xs[3] = {x_q, x_kv, x_kv};
+    const void* ws3[3] = {Wq, Wk, Wv};
+    void* outs[3] = {Q, K, V};
+    const int Ms[3] = {Mq, Mk, Mk};
+    const int Ns[3] = {hdk, hdk, hdv};
+    for (int i = 0; i < 3; ++i) {
+        if (!make_2d_map(&pr[i].a, xs[i], Ms[i], d_model, 128) ||
+            !make_2d_map(&pr[i].w, ws3[i], d_model, Ns[i], 64))
+            return HATTN_ECUDA;
+        pr[i].c = outs[i];
+        pr[i].M = Ms[i];
+        pr[i].N = Ns[i];
+        pr[i].K = d_model;
+    }
+    int rc = from_cuda(launch_proj_gemm(pr, 3, st, err));
+    if (rc != HATTN_OK) return rc;
+
+    AttnArgs a{Q, K, V, A, HATTN_BF16, B, h, n_q, n_k, d_k, d_v,
+               1.0f / std::sqrt(static_cast<float>(d_k)), mask_kind,
+               (mask_kind & HATTN_MASK_KEY_PADDING) ? key_lens : nullptr, st, err};
+    rc = run_attn(a);
+    if (rc != HATTN_OK) return rc;
+
+    OutProjLnArgs o;
+    if (!make_2d_map(&o.a, A, Mq, hdv, 128) || !make_2d_map(&o.wo, Wo, hdv, d_model, 64))
+        return HATTN_ECUDA;
+    o.x = x_q;
+    o.gamma = gamma;
+    o.beta = beta;
+    o.eps = eps;
+    o.y = y;
+    o.M = Mq;
+    o.N = d_model;
+    o.K = hdv;
+    return from_cuda(launch_outproj_ln(o, st, err));
+}
+
+const char* hattn_status_str(int status)
+{
+    switch (status) {
+    case HATTN_OK: return "ok";
+    case HATTN_EINVAL: return "invalid argument";
+    case HATTN_EUNSUPPORTED: return "unsupported configuration";
+    case HATTN_ECUDA: return "CUDA error";
+    case HATTN_ETIMEOUT: return "device pipeline wait timed out";
+    case HATTN_EKEYLEN: return "key length outside [1, n_k]";
+    case HATTN_EWORKSPACE: return "workspace missing, misaligned or too small";
+    default: return "unknown status";
+    }
+}
+
+int hattn_check_device_error(hattn_stream_t stream)
+{
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return HATTN_ECUDA;
+    int value = 0;
+    if (cudaMemcpyFromSymbol(&value, g_device_error, sizeof(int)) != cudaSuccess)
+        return HATTN_ECUDA;
+    if (value != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess)
+            return HATTN_ECUDA;
+    }
+    return value;
+}
+
+int hattn_version(void) { return 100; }
+
+}  // extern "C"

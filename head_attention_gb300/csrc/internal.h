@@ -1,0 +1,79 @@
+// Declarations shared between the C-ABI host code and the kernel translation
+// units of libhattn.so. Nothing here is part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "hattn.h"
+
+namespace hattn {
+
+// One validated attention request (see attn_fwd in hattn.h).
+struct AttnArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* out;
+    int dtype;
+    int B, h, n_q, n_k, d_k, d_v;
+    float scale;
+    int mask_kind;
+    const int32_t* key_lens;
+    cudaStream_t stream;
+    int* err_word;  // device error word of the current device
+};
+
+// Tensor maps of one attention call on the tensor-core path: Q, K, V viewed as
+// 4-D [B][n][h][d] bf16 tensors, loaded as 128-row x 64-column boxes.
+struct AttnMaps {
+    CUtensorMap q, k, v;
+};
+
+// CUDA-core kernel: fp32 (d <= 128) and bf16 (d <= 256), any d_k / d_v.
+cudaError_t launch_attn_simt(const AttnArgs& a);
+
+// Tensor-core (tcgen05) kernel: bf16, d_k == d_v in {64, 128}.
+bool attn_tc_supported(const AttnArgs& a);
+cudaError_t launch_attn_tc(const AttnArgs& a, const AttnMaps& maps);
+
+// Encodes a tensor map through the driver entry point. Returns false on failure.
+bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                 CUtensorMapSwizzle swizzle);
+
+// [B][n][h][d] bf16 tensor as a 4-D map with 64-element x `box_rows` boxes,
+// 128-byte swizzle, zero fill past n within each batch element.
+bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int n, int h, int d, int box_rows);
+
+// ---- tcgen05 GEMMs of the MHA sublayer
+
+// One output problem of the projection GEMM: C[M, N] = A[M, K] . W[K, N] (bf16, row-major).
+struct ProjProblem {
+    CUtensorMap a;  // A [M][K], 64 x 128 boxes, K-major
+    CUtensorMap w;  // W [K][N], 64 x 64 boxes, N-major
+    void* c;        // bf16 [M][N]
+    int M, N, K;
+};
+
+// Up to three independent projection GEMMs in one launch (Q, K, V).
+cudaError_t launch_proj_gemm(const ProjProblem* problems, int count, cudaStream_t stream,
+                             int* err_word);
+
+// y = LayerNorm(x + A . Wo) * gamma + beta over rows of length N = d_model.
+struct OutProjLnArgs {
+    CUtensorMap a;   // A [M][K] bf16, K-major boxes 64 x 128
+    CUtensorMap wo;  // Wo [K][N] bf16, N-major boxes 64 x 64
+    const void* x;   // residual, bf16 [M][N]
+    const float* gamma;
+    const float* beta;
+    float eps;
+    void* y;  // bf16 [M][N]
+    int M, N, K;
+};
+cudaError_t launch_outproj_ln(const OutProjLnArgs& args, cudaStream_t stream, int* err_word);
+
+}  // namespace hattn

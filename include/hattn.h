@@ -1,0 +1,146 @@
+/*
+ * hattn — multi-head scaled dot-product attention for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libhattn.so. Every entry point takes plain pointers and sizes; no
+ * PyTorch or C++ types cross this boundary. The caller owns every buffer and
+ * the stream. All compute entry points are asynchronous: a return of HATTN_OK
+ * means "validated and enqueued on `stream`"; device-side conditions (a bad
+ * key length, a pipeline wait that gave up) are reported later by
+ * hattn_check_device_error().
+ *
+ * Sources for the operations (explanatory pages on "Attention Is All You
+ * Need"):
+ *   [P1] hex4c59.cc, "读懂 Attention Is All You Need：从一次加权求和到完整
+ *        Transformer"
+ *   [P4] devpress.csdn.net, "【深度学习】Transformer（Attention Is All You Need）"
+ *
+ * Layout. Activations are row-major [B, n, h, d]: head i of token t of batch
+ * element b is the d-vector starting at element ((b*n + t)*h + i)*d. This is
+ * the concatenation of heads along the feature axis, i.e. exactly the
+ * row-major [B*n, h*d] matrix that X.W produces ([P1] §多头注意力让一次读取
+ * 有多组投影: head outputs are concatenated along the feature dimension).
+ */
+#ifndef HATTN_H
+#define HATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* hattn_stream_t;
+
+/* Element types. */
+#define HATTN_F32 0  /* fp32 in, fp32 out, fp32 arithmetic                    */
+#define HATTN_BF16 1 /* bf16 in, bf16 out, fp32 accumulation                   */
+
+/* mask_kind bits; they may be combined. */
+#define HATTN_MASK_NONE 0
+#define HATTN_MASK_CAUSAL 1      /* key j invisible to query t when j > t      */
+#define HATTN_MASK_KEY_PADDING 2 /* key j invisible when j >= key_lens[b]      */
+
+/* Status codes (0 or negative). */
+#define HATTN_OK 0
+#define HATTN_EINVAL (-1)       /* null pointer, bad size, bad mask bits, misaligned pointer */
+#define HATTN_EUNSUPPORTED (-2) /* a valid request no kernel here implements          */
+#define HATTN_ECUDA (-3)        /* a CUDA runtime/driver call failed (launch, tensor map) */
+#define HATTN_ETIMEOUT (-4)     /* device: a pipeline wait gave up (reported asynchronously) */
+#define HATTN_EKEYLEN (-5)      /* device: key_lens[b] outside [1, n_k] (reported asynchronously) */
+#define HATTN_EWORKSPACE (-6)   /* workspace NULL or smaller than mha_workspace_bytes()   */
+
+/*
+ * attn_fwd — multi-head scaled dot-product attention,
+ *     out[b,t,i,:] = sum_j softmax_j( scale * q[b,t,i,:].k[b,j,i,:] ) v[b,j,i,:]
+ * over the keys j visible to query t.
+ *
+ * Defined in [P1] §六步算完一行注意力 (dot products, scaling, row softmax,
+ * weighted sum of values) and §把所有位置合并，就是那条核心公式
+ * (Attention(Q,K,V) = softmax(QK^T/sqrt(d_k))V); masking before the softmax in
+ * [P1] §掩码必须在 softmax 之前生效 and [P4] §3.1 (triu -inf, diagonal
+ * visible); cross-attention with n_q != n_k in [P1] §解码器有两种读取 and
+ * [P4] §3.2. A masked key gets weight exactly 0.
+ *
+ *   q        device, [B, n_q, h, d_k], dtype elements, 16-byte aligned
+ *   k        device, [B, n_k, h, d_k]
+ *   v        device, [B, n_k, h, d_v]
+ *   out      device, [B, n_q, h, d_v]; written, never read; must not overlap inputs
+ *   dtype    HATTN_F32 or HATTN_BF16
+ *   scale    multiplies q.k; normally 1/sqrt(d_k)
+ *   mask_kind  bitwise OR of HATTN_MASK_*; CAUSAL requires n_q == n_k
+ *   key_lens device int32[B], read only with HATTN_MASK_KEY_PADDING (else may
+ *            be NULL). Each value must lie in [1, n_k]; a value outside makes
+ *            the kernel zero that batch element's output and raise
+ *            HATTN_EKEYLEN in the device error word.
+ *   stream   the CUDA stream to enqueue on
+ *
+ * Supported: HATTN_F32 with d_k, d_v <= 128; HATTN_BF16 with d_k, d_v <= 256
+ * (d_k == d_v in {64, 128} runs on the tensor-core kernel, other sizes on a
+ * CUDA-core kernel). Returns HATTN_OK, HATTN_EINVAL, HATTN_EUNSUPPORTED or
+ * HATTN_ECUDA; on an error return nothing was enqueued.
+ * Allocates nothing; caches tensor-map descriptors per (pointer, shape).
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* out, int dtype, int B, int h,
+             int n_q, int n_k, int d_k, int d_v, float scale, int mask_kind,
+             const int32_t* key_lens, hattn_stream_t stream);
+
+/*
+ * mha_fwd — the post-norm multi-head-attention sublayer,
+ *     Q = x_q Wq,  K = x_kv Wk,  V = x_kv Wv                      (no biases)
+ *     A = Concat_i attn(Q_i, K_i, V_i)        (scale 1/sqrt(d_k), mask_kind)
+ *     y = LayerNorm(x_q + A Wo) * gamma + beta
+ * with LayerNorm over the d_model features of each token, biased variance
+ * and eps inside the square root.
+ *
+ * Defined in [P1] §Q、K、V 是三种计算角色 (Q = X W^Q, W^Q of shape
+ * d_model x d_k per head), §多头注意力让一次读取有多组投影 (heads, concat,
+ * W^O), §Add & Norm 里究竟发生了什么？ (LayerNorm(x + F(x)), post-LN) and
+ * [P4] §2.2 (W^O of shape h*d_v x d_model).
+ *
+ *   x_q      device, [B, n_q, d_model] bf16
+ *   x_kv     device, [B, n_k, d_model] bf16; pass x_q (and n_k = n_q) for self-attention
+ *   Wq, Wk   device, [d_model, h*d_k] bf16 row-major; column block i is head i
+ *   Wv       device, [d_model, h*d_v] bf16
+ *   Wo       device, [h*d_v, d_model] bf16; row block i is head i
+ *   gamma, beta  device, fp32 [d_model]
+ *   eps      LayerNorm epsilon (> 0)
+ *   y        device, [B, n_q, d_model] bf16 output
+ *   dtype    HATTN_BF16 (the only type this entry point implements)
+ *   workspace  device scratch of at least mha_workspace_bytes(...) bytes,
+ *            256-byte aligned, owned by the caller, not used concurrently by
+ *            another call; holds Q, K, V and the concatenated heads A.
+ *
+ * Supported: d_model a multiple of 64 and <= 512, d_k == d_v in {64, 128},
+ * h*d_k a multiple of 64. Returns HATTN_OK, HATTN_EINVAL, HATTN_EUNSUPPORTED,
+ * HATTN_EWORKSPACE or HATTN_ECUDA.
+ */
+int mha_fwd(const void* x_q, const void* x_kv, const void* Wq, const void* Wk, const void* Wv,
+            const void* Wo, const float* gamma, const float* beta, float eps, void* y, int dtype,
+            int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v, int mask_kind,
+            const int32_t* key_lens, void* workspace, size_t ws_bytes, hattn_stream_t stream);
+
+/* Bytes of caller-owned workspace mha_fwd needs for these sizes (0 on bad sizes). */
+size_t mha_workspace_bytes(int dtype, int B, int n_q, int n_k, int d_model, int h, int d_k,
+                           int d_v);
+
+/* Static text for a status code. */
+const char* hattn_status_str(int status);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word that the
+ * kernels of this library set on the current device. Returns HATTN_OK,
+ * HATTN_ETIMEOUT, HATTN_EKEYLEN, or HATTN_ECUDA when the synchronisation
+ * itself failed.
+ */
+int hattn_check_device_error(hattn_stream_t stream);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int hattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HATTN_H */

@@ -1,8 +1,9 @@
 """Seeded synthetic inputs for the attention workloads.
 
 Draws come from numpy's Philox counter-based generator, keyed by
-``(seed, stream_id)`` so that every tensor of a workload has its own
-independent, reproducible stream. Normal draws are fp64; they are rounded
+``(seed, stream_id, chunk)``: every tensor of a workload has its own
+independent stream, cut into fixed 2^22-element chunks that are drawn in
+parallel, so the values do not depend on the host or its thread count. Normal draws are fp64; they are rounded
 to the dtype the kernel reads (fp32, or bf16 by round-to-nearest-even via
 fp32) *before* either side sees them, and the oracle receives the rounded
 values widened back to fp64.
@@ -12,8 +13,10 @@ Nothing here computes attention: no dot product, softmax or normalisation.
 
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
 import math
+import os
 
 import numpy as np
 
@@ -28,16 +31,45 @@ MASK_CAUSAL = 1
 MASK_KEY_PADDING = 2
 
 
-def _rng(seed: int, stream: int) -> np.random.Generator:
-    return np.random.Generator(np.random.Philox(np.random.SeedSequence([int(seed), int(stream)])))
+_CHUNK = 1 << 22  # elements per independently keyed chunk
+
+
+def _rng(seed: int, stream: int, chunk: int = 0) -> np.random.Generator:
+    return np.random.Generator(
+        np.random.Philox(np.random.SeedSequence([int(seed), int(stream), int(chunk)])))
+
+
+def _threads() -> int:
+    return max(1, min(32, os.cpu_count() or 1))
+
+
+def _chunked(n: int, fill) -> None:
+    """Runs fill(chunk_index, start, stop) over fixed-size chunks on a thread pool.
+
+    Chunk boundaries and keys do not depend on the thread count, so the draws
+    are the same on every host.
+    """
+    starts = list(range(0, n, _CHUNK))
+    if len(starts) <= 1:
+        for i, a in enumerate(starts):
+            fill(i, a, min(n, a + _CHUNK))
+        return
+    with concurrent.futures.ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(lambda ia: fill(ia[0], ia[1], min(n, ia[1] + _CHUNK)), enumerate(starts)))
 
 
 def draw_normal(seed: int, stream: int, shape, std: float = 1.0) -> np.ndarray:
     """i.i.d. N(0, std^2) draws in fp64."""
-    x = _rng(seed, stream).standard_normal(size=shape, dtype=np.float64)
-    if std != 1.0:
-        x *= std
-    return x
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.float64)
+
+    def fill(i, a, b):
+        _rng(seed, stream, i).standard_normal(size=b - a, dtype=np.float64, out=out[a:b])
+        if std != 1.0:
+            out[a:b] *= std
+
+    _chunked(n, fill)
+    return out.reshape(shape)
 
 
 def draw_key_lens(seed: int, stream: int, batch: int, lo: int, hi: int) -> np.ndarray:
@@ -49,17 +81,36 @@ def round_to_f32(x: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(x, dtype=np.float64).astype(np.float32)
 
 
+def _bf16_bits_from_f32(x32: np.ndarray) -> np.ndarray:
+    u = x32.view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    return ((u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
+
+
 def round_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """fp64 -> fp32 (RNE) -> bf16 (RNE); returns the bf16 bit patterns as uint16."""
-    u = round_to_f32(x).view(np.uint32)
-    lsb = (u >> np.uint32(16)) & np.uint32(1)
-    rounded = (u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)
-    return rounded.astype(np.uint16)
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    flat = x.reshape(-1)
+    out = np.empty(flat.size, dtype=np.uint16)
+
+    def fill(i, a, b):
+        out[a:b] = _bf16_bits_from_f32(flat[a:b].astype(np.float32))
+
+    _chunked(flat.size, fill)
+    return out.reshape(x.shape)
 
 
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     """Widen bf16 bit patterns exactly to fp64."""
-    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    bits = np.ascontiguousarray(bits)
+    flat = bits.reshape(-1)
+    out = np.empty(flat.size, dtype=np.float64)
+
+    def fill(i, a, b):
+        out[a:b] = (flat[a:b].astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+    _chunked(flat.size, fill)
+    return out.reshape(bits.shape)
 
 
 @dataclasses.dataclass(frozen=True)

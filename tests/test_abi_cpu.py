@@ -1,0 +1,117 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds, loads,
+exports every declared symbol, and rejects bad arguments before touching the
+device (a rejected call enqueues nothing, so none of these reach CUDA)."""
+
+import os
+import re
+
+import pytest
+
+import head_attention_gb300 as hattn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    hattn.build()
+    return hattn.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "hattn.h"), encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(",
+                                 text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    assert declared_functions() == sorted(hattn.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert hattn.status_str(code) not in ("", "unknown status")
+    assert hattn.status_str(12345) == "unknown status"
+    assert hattn.version() >= 100
+
+
+A = 0x10000  # 16-byte aligned fake device addresses: validation never dereferences them
+GOOD = dict(q=A, k=2 * A, v=3 * A, out=4 * A, dtype=1, B=2, h=4, n_q=128, n_k=128, d_k=64, d_v=64,
+            scale=0.125, mask_kind=0, key_lens=None, stream=0)
+
+
+def call(**kw):
+    args = dict(GOOD)
+    args.update(kw)
+    return hattn.attn_fwd_raw(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), hattn._binding.EINVAL),
+    (dict(out=None), hattn._binding.EINVAL),
+    (dict(B=0), hattn._binding.EINVAL),
+    (dict(h=-1), hattn._binding.EINVAL),
+    (dict(n_q=0), hattn._binding.EINVAL),
+    (dict(d_v=0), hattn._binding.EINVAL),
+    (dict(dtype=7), hattn._binding.EINVAL),
+    (dict(mask_kind=4), hattn._binding.EINVAL),
+    (dict(mask_kind=1, n_k=127), hattn._binding.EINVAL),        # causal needs n_q == n_k
+    (dict(mask_kind=2, key_lens=None), hattn._binding.EINVAL),  # padding needs key_lens
+    (dict(q=A + 8), hattn._binding.EINVAL),                     # misaligned
+    (dict(out=A + 2), hattn._binding.EINVAL),
+    (dict(d_k=60, d_v=60), hattn._binding.EINVAL),              # row not a multiple of 16 bytes
+    (dict(scale=float("nan")), hattn._binding.EINVAL),
+    (dict(scale=float("inf")), hattn._binding.EINVAL),
+    (dict(dtype=0, d_k=192, d_v=192), hattn._binding.EUNSUPPORTED),
+    (dict(d_k=512, d_v=512), hattn._binding.EUNSUPPORTED),
+])
+def test_attn_fwd_rejects_bad_arguments(lib, kw, code):
+    assert call(**kw) == code
+
+
+MHA = dict(x_q=A, x_kv=A, wq=2 * A, wk=3 * A, wv=4 * A, wo=5 * A, gamma=6 * A, beta=7 * A, eps=1e-6,
+           y=8 * A, dtype=1, B=16, n_q=512, n_k=512, d_model=512, h=8, d_k=64, d_v=64, mask_kind=0,
+           key_lens=None, workspace=0x100000, ws_bytes=1 << 40, stream=0)
+
+
+def mha_call(**kw):
+    args = dict(MHA)
+    args.update(kw)
+    return hattn.mha_fwd_raw(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x_q=None), hattn._binding.EINVAL),
+    (dict(gamma=None), hattn._binding.EINVAL),
+    (dict(dtype=0), hattn._binding.EUNSUPPORTED),
+    (dict(dtype=3), hattn._binding.EINVAL),
+    (dict(eps=0.0), hattn._binding.EINVAL),
+    (dict(eps=float("nan")), hattn._binding.EINVAL),
+    (dict(mask_kind=1, n_k=256), hattn._binding.EINVAL),
+    (dict(wo=5 * A + 4), hattn._binding.EINVAL),
+    (dict(d_k=32, d_v=32), hattn._binding.EUNSUPPORTED),
+    (dict(d_model=1024), hattn._binding.EUNSUPPORTED),
+    (dict(d_model=500), hattn._binding.EUNSUPPORTED),
+    (dict(workspace=None), hattn._binding.EWORKSPACE),
+    (dict(workspace=0x100010), hattn._binding.EWORKSPACE),   # not 256-byte aligned
+    (dict(ws_bytes=1024), hattn._binding.EWORKSPACE),
+])
+def test_mha_fwd_rejects_bad_arguments(lib, kw, code):
+    assert mha_call(**kw) == code
+
+
+def test_workspace_size_is_q_k_v_and_heads(lib):
+    # Q, K, V, A in bf16, each region rounded up to 256 bytes.
+    n = hattn.mha_workspace_bytes(1, 16, 512, 512, 512, 8, 64, 64)
+    assert n == 4 * 16 * 512 * 512 * 2
+    n2 = hattn.mha_workspace_bytes(1, 1, 3, 5, 64, 1, 64, 64)
+    up = lambda x: (x + 255) // 256 * 256
+    assert n2 == up(3 * 64 * 2) + 2 * up(5 * 64 * 2) + up(3 * 64 * 2)
+    assert hattn.mha_workspace_bytes(0, 16, 512, 512, 512, 8, 64, 64) == 0
+    assert hattn.mha_workspace_bytes(1, 0, 512, 512, 512, 8, 64, 64) == 0
