@@ -1,0 +1,499 @@
+#!/usr/bin/env python3
+"""Attention forward throughput on GB300: TFLOP/s, % of dense bf16 peak, tokens/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step is one attn_fwd call (the whole hot path: tile loads, QK^T, masking,
+streaming softmax, PV, epilogue) over one batch of seeded synthetic inputs
+already resident in HBM. Default workload: long-sequence causal
+self-attention, bf16, B=4 h=16 n=8192 d=128 (Q, K, V and O are 134 MB each, so
+the 402 MB of inputs are larger than the 129 MB L2 and every step streams
+them from HBM).
+
+FLOPs per step are the defined count 4*B*h*n_q*n_k*d, halved for causal.
+Timing: W untimed warm-up steps, then exactly K steps between two CUDA events
+on the launching stream, bracketed by a barrier and a device synchronize;
+max over ranks. SM clocks and throttle reasons are sampled with nvidia-smi
+during the timed region. The e2e leg repeats the measurement with the host
+copies in the timed region: pinned host Q/K/V -> device, attn_fwd, output ->
+pinned host. The CPU baseline is the fp64 oracle on a bounded sample of the
+same workload on this host's cores.
+
+--impl reference times the fp64 CPU oracle itself (the only other
+implementation of this method) on the same workload, metric and unit.
+
+With N > 1 (torchrun, one rank per GPU) every rank runs the full workload on
+its own GPU with no data-path collective (attention over (batch, head) is
+embarrassingly parallel): weak scaling, value = all ranks' FLOPs / max time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s and % of GB300 BF16 tensor peak (1 GPU); tokens/s"
+DEFAULT_WORKLOAD = "long_causal_d128"
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+KERNEL_SOURCES = ("head_attention_gb300/csrc/attn_tc.cu", "head_attention_gb300/csrc/ptx.cuh")
+
+
+# ---------------------------------------------------------------- helpers
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="hattn", choices=["hattn", "reference"])
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0,
+                    help="CPU seconds of oracle work for the CPU baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max of a float over ranks (identity at world size 1)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    path = os.path.join(PROFILE_DIR, f"attn_tc_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path, encoding="utf-8").read()
+    sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    traffic = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not sha or not traffic or sha.group(1) != kernel_source_sha():
+        return None
+    return float(traffic.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.window = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        rows = self.samples
+        if self.window:
+            t0, t1 = self.window
+            inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.15]
+            rows = inside or sorted(rows, key=lambda r: abs(r[0] - (t0 + t1) / 2))[:3]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        mhz, max_mhz, watts = [], [], []
+        for _, v in rows:
+            try:
+                mhz.append(float(v[0]))
+                max_mhz.append(float(v[1]))
+                watts.append(float(v[2]))
+            except (ValueError, IndexError):
+                continue
+            for name, flag in zip(names, v[4:8]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None,
+                "sm_max_mhz": max(max_mhz) if max_mhz else None,
+                "power_w_median": statistics.median(watts) if watts else None,
+                "samples": len(mhz), "reasons": sorted(reasons)}
+
+
+def gpu_uuid(dev_index: int) -> str:
+    import torch
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(dev_index).uuid)
+    except Exception:
+        return str(dev_index)
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def _head_arrays(inp, w, b, i):
+    """fp64 copies of one (batch, head) slice, shaped [1, n, 1, d]."""
+    from synth import inputs as synth
+    out = []
+    for name in ("q", "k", "v"):
+        a = inp[name][b:b + 1, :, i:i + 1, :]
+        out.append(synth.widen(a.copy(), w.dtype))
+    return out
+
+
+def _rows_flops(w, rows, kv_len):
+    """Exact visible-pair FLOPs (4*d per visible (query, key) pair) of these query rows."""
+    if w.mask_kind & 1:
+        return float(sum(4 * w.d_k * min(t + 1, kv_len) for t in rows))
+    return float(4 * w.d_k * kv_len * len(rows))
+
+
+def oracle_sample_rate(w, inp, budget_s: float, sample_index: int = 0):
+    """Times the oracle on query rows of one (batch, head) until ~budget_s of
+    work; returns (TFLOP/s, threads, description)."""
+    import oracle
+    threads = os.cpu_count() or 1
+    b = sample_index % w.B
+    i = (sample_index // w.B) % w.h
+    q, k, v = _head_arrays(inp, w, b, i)
+    kv_len = int(inp["key_lens"][b]) if inp.get("key_lens") is not None else w.n_k
+    kl = None if inp.get("key_lens") is None else inp["key_lens"][b:b + 1]
+    # Calibrate on a strided subset, then scale the row count to the budget.
+    stride = max(1, w.n_q // 64)
+    rows = list(range(stride // 2, w.n_q, stride))
+    t0 = time.perf_counter()
+    sel = [(0, t, 0) for t in rows]
+    oracle.attn_rows(q, k, v, w.scale, sel, w.mask_kind, kl, nthreads=threads)
+    dt = time.perf_counter() - t0
+    flops = _rows_flops(w, rows, kv_len)
+    rate = flops / max(dt, 1e-9)
+    want = budget_s * rate
+    total_flops = _rows_flops(w, range(w.n_q), kv_len)
+    frac = min(1.0, want / total_flops)
+    n_rows = max(1, int(frac * w.n_q))
+    stride = max(1, w.n_q // n_rows)
+    rows = list(range(stride // 2, w.n_q, stride))
+    sel = [(0, t, 0) for t in rows]
+    t0 = time.perf_counter()
+    oracle.attn_rows(q, k, v, w.scale, sel, w.mask_kind, kl, nthreads=threads)
+    dt = time.perf_counter() - t0
+    flops = _rows_flops(w, rows, kv_len)
+    desc = (f"{len(rows)} of {w.n_q} query rows (every {stride}th) of (batch {b}, head {i}); "
+            f"{flops / 1e9:.2f} GFLOP of visible (query, key) pairs in {dt:.2f} s")
+    return flops / dt / 1e12, threads, desc
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_gpu(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import head_attention_gb300 as hattn
+    from synth import inputs as synth
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    hattn.build()
+    hattn.load()
+    w = synth.workload(args.workload)
+    if w.is_mha:
+        raise SystemExit("bench.py times attn_fwd; use an attention workload")
+    inp = synth.attn_inputs(w)
+
+    def dev(a):
+        if w.dtype == "f32":
+            return torch.from_numpy(a).cuda()
+        return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+
+    q, k, v = dev(inp["q"]), dev(inp["k"]), dev(inp["v"])
+    kl = None if inp["key_lens"] is None else torch.from_numpy(inp["key_lens"]).cuda()
+    out = torch.empty((w.B, w.n_q, w.h, w.d_v), dtype=q.dtype, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        hattn.attn_fwd(q, k, v, out=out, scale=w.scale, mask_kind=w.mask_kind, key_lens=kl,
+                       stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if hattn.check_device_error(stream) != 0:
+        raise RuntimeError("device error during warm-up")
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_uuid(local))
+    with sampler:
+        time.sleep(0.25)  # let the sampler start
+        barrier(world)
+        torch.cuda.synchronize()
+        t_wall0 = time.time()
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize()
+        t_wall1 = time.time()
+        barrier(world)
+        sampler.mark(t_wall0, t_wall1)
+        time.sleep(0.15)
+    ms_local = start.elapsed_time(end)
+    if hattn.check_device_error(stream) != 0:
+        raise RuntimeError("device error during the timed region")
+    ms_total = reduce_max(ms_local, world)
+    ms_step = ms_total / args.steps
+    flops = w.attn_flops()
+    tflops = flops * world / (ms_step * 1e-3) / 1e12
+    tokens_s = w.tokens() * world / (ms_step * 1e-3)
+
+    peaks, peak_src = load_peaks()
+    kernel_ms = ms_local / args.steps  # one launch per step on this stream
+    achieved = flops / (kernel_ms * 1e-3) / 1e12
+    esize = 4 if w.dtype == "f32" else 2
+    bytes_in = (w.B * w.n_q * w.h * w.d_k + w.B * w.n_k * w.h * (w.d_k + w.d_v)) * esize
+    bytes_alg = bytes_in + w.B * w.n_q * w.h * w.d_v * esize
+    roofline = {
+        "kernel": f"attn_tc_kernel<{w.d_k}>" if w.dtype == "bf16" and w.d_k == w.d_v
+        and w.d_k in (64, 128) else "attn_simt_kernel",
+        "bound": "tensor",
+        "achieved": round(achieved, 2),
+        "peak": peaks["bf16_tflops"],
+        "unit": "TFLOP/s",
+        "frac": round(achieved / peaks["bf16_tflops"], 4),
+        "peak_source": f"{peak_src} (burst, MEASURED_PEAKS.json bf16_tflops)",
+        "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
+        "frac_of_nominal_2250": round(achieved / NOMINAL_BF16_TFLOPS, 4),
+        "algorithmic_flops_per_launch": flops,
+        "algorithmic_bytes_per_launch": bytes_alg,
+        "hbm_gbs_at_algorithmic_bytes": round(bytes_alg / (kernel_ms * 1e-3) / 1e9, 1),
+        "traffic": profiled_traffic(w.name),
+    }
+
+    result = {
+        "metric": METRIC,
+        "value": round(tflops, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic: seeded Philox N(0,1) inputs rounded to bf16 (no dataset)",
+        "config": {"workload": w.name, "description": w.description, "B": w.B, "h": w.h,
+                   "n_q": w.n_q, "n_k": w.n_k, "d": w.d_k,
+                   "mask": {0: "none", 1: "causal", 2: "key_padding", 3: "causal+key_padding"}[
+                       w.mask_kind],
+                   "parallelism": f"replicas x{world} (independent (batch, head) work per GPU)",
+                   "l2": (f"inputs {bytes_in / 1e6:.0f} MB > 129 MB L2: streamed from HBM every step, no flush"
+                          if bytes_in > 129e6 else
+                          f"inputs {bytes_in / 1e6:.1f} MB fit in L2: warm-L2 number")},
+        "tokens_per_s": round(tokens_s, 1),
+        "pct_of_measured_bf16_peak": round(100 * tflops / world / peaks["bf16_tflops"], 2),
+        "pct_of_nominal_bf16_peak": round(100 * tflops / world / NOMINAL_BF16_TFLOPS, 2),
+        "roofline": roofline,
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(),
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = e2e_leg(args, w, inp, q, k, v, kl, out, stream, world)
+        result["gpu_launches"] += result["e2e"].pop("launches")
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, threads, desc = oracle_sample_rate(w, inp, args.cpu_budget_s)
+        result["cpu_baseline"] = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads,
+                                  "kind": "oracle", "sample": desc}
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return result
+
+
+def e2e_leg(args, w, inp, q, k, v, kl, out, stream, world):
+    """Same metric with host buffers: every step copies Q, K, V from pinned host
+    memory, runs attn_fwd, and copies the output back to pinned host memory."""
+    import numpy as np
+    import torch
+
+    import head_attention_gb300 as hattn
+
+    def pinned(a):
+        t = torch.from_numpy(a if w.dtype == "f32" else a.view(np.int16))
+        t = t.pin_memory()
+        return t if w.dtype == "f32" else t.view(torch.bfloat16)
+
+    hq, hk, hv = pinned(inp["q"]), pinned(inp["k"]), pinned(inp["v"])
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    steps = max(1, min(args.steps, 100))
+
+    def step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        hattn.attn_fwd(q, k, v, out=out, scale=w.scale, mask_kind=w.mask_kind, key_lens=kl,
+                       stream=stream)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = reduce_max(start.elapsed_time(end), world) / steps
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = hout.numel() * hout.element_size()
+    return {"value": round(w.attn_flops() * world / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4), "steps": steps, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "launches": steps}
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args, rank, world):
+    from synth import inputs as synth
+    if rank != 0:
+        return None
+    w = synth.workload(args.workload)
+    inp = synth.attn_inputs(w)
+    total_budget_s = 150.0
+    per_step = max(0.5, total_budget_s / max(1, args.steps + args.warmup))
+    for i in range(args.warmup):
+        oracle_sample_rate(w, inp, per_step, sample_index=i)
+    rates = []
+    descs = []
+    t0 = time.perf_counter()
+    threads = os.cpu_count() or 1
+    for i in range(args.steps):
+        rate, threads, desc = oracle_sample_rate(w, inp, per_step, sample_index=args.warmup + i)
+        rates.append(rate)
+        descs.append(desc)
+    elapsed = time.perf_counter() - t0
+    value = statistics.median(rates)
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * elapsed / max(1, args.steps), 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic: seeded Philox N(0,1) inputs rounded to bf16 (no dataset)",
+        "config": {"workload": w.name, "description": w.description, "B": w.B, "h": w.h,
+                   "n_q": w.n_q, "n_k": w.n_k, "d": w.d_k},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"each step: {descs[0] if descs else ''} (median over steps)"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.gpus != world and world > 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    if args.impl == "reference":
+        result = run_reference(args, rank, world)
+    else:
+        result = run_gpu(args, rank, world, local)
+    if rank == 0 and result is not None:
+        print(json.dumps(result), flush=True)
+
+
+if __name__ == "__main__":
+    main()

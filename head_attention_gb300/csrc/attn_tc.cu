@@ -1,5 +1,5 @@
 // Tensor-core attention forward for sm_103a (bf16 in/out, fp32 accumulation,
-// d_k == d_v == D in {64, 128}).
+// d_k == d_v == D in {64, 128}, scale > 0).
 //
 // What it computes: for every (batch b, head i, query t)
 //     out[b,t,i,:] = sum_j softmax_j(scale * q.k_j) v_j     (visible keys j only)
@@ -7,25 +7,35 @@
 // Is All You Need" (hex4c59 §把所有位置合并，就是那条核心公式; masks per
 // §掩码必须在 softmax 之前生效).
 //
-// How (one CTA = one (b, i) and 256 consecutive query rows = two 128-row tiles):
-//   warp 8      TMA producer: loads the two Q tiles once, then streams K_j and
-//               V_j (128 keys each) through a ring of shared-memory stages.
-//   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T into TMEM, and
-//               O_t += P_t V_j with P_t read from TMEM; completion is reported
-//               through tcgen05.commit onto mbarriers.
-//   warps 0-3   softmax of tile 0, warps 4-7 softmax of tile 1: thread r owns
+// How. One CTA = one (b, i) and 256 consecutive query rows = two 128-row tiles.
+// 12 warps in three warpgroups; a register split gives the softmax warps 200
+// registers and the control warps 88.
+//   warp 8      TMA: the two Q tiles once, then K_j (128 keys) through a
+//               3-stage (D=128) / 5-stage (D=64) shared-memory ring.
+//   warp 10     TMA: V_j through a 2-stage (D=128) / 4-stage (D=64) ring. K
+//               runs one block ahead of V because S(j+1) follows PV(j).
+//   warps 9, 11 MMA issuers, one thread per tile: S_t = Q_t K_j^T into TMEM,
+//               then per block PV_t(j) (O_t += P_t V_j, P_t read from TMEM)
+//               followed at once by S_t(j+1). Completion is reported by
+//               tcgen05.commit onto mbarriers. With one issuer per tile, a tile
+//               whose P is ready never waits behind the other tile's MMA issue,
+//               and one tile's softmax overlaps the other tile's MMAs.
+//   warps 0-3   softmax of tile 0, warps 4-7 softmax of tile 1, taking turns
+//               on the exponentials (two named barriers), so that the MUFU work
+//               of one tile overlaps the MMAs of the other: thread r owns
 //               query row r (TMEM lane r), so the row max and row sum are
-//               thread-local. Streaming softmax in base 2: running max m, sum l,
-//               p = 2^(s*scale*log2e - m), P written back to TMEM as bf16 over
-//               the first half of S's columns. O is rescaled only when the
-//               max grows by more than 2^8 (the final 1/l uses the same stale
-//               max, so the result is unchanged; p stays <= 2^8).
-//   The issue order S_0(j), S_1(j), then per tile PV_t(j) followed at once by
-//   S_t(j+1) lets one tile's softmax overlap the other tile's MMAs.
+//               thread-local. Streaming softmax in base 2: running max m and
+//               sum l, p = 2^(s*scale*log2e - m), P stored back to TMEM as bf16
+//               over the first half of S's columns. The exponentials of a block
+//               use the running max while the block's own max is computed
+//               alongside; O is rescaled (and the block redone) only when a
+//               row's max grows by more than 2^8. The final 1/l uses the same
+//               max as the numerator, so the result is unchanged; p <= 2^8.
 //   Causal: key blocks above the diagonal are never loaded or multiplied; only
 //   the diagonal block is masked element-wise. Key padding: blocks at or past
-//   key_lens[b] are skipped; the last block is masked column-wise.
-//   Epilogue: O / l packed to bf16, 16-byte stores into [B, n_q, h, D].
+//   key_lens[b] are skipped and the last block is masked column-wise.
+//   Epilogue (softmax warps): O / l packed to bf16, 16-byte stores into
+//   [B, n_q, h, D].
 //
 // TMEM columns: tile t holds S at [256t, 256t+128) and O at [256t+128, 256t+128+D).
 // Every mbarrier wait is bounded; on a timeout the CTA records HATTN_ETIMEOUT in
@@ -40,9 +50,21 @@
 namespace hattn {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kWarpLoad = 8;
-constexpr int kWarpMma = 9;
+constexpr int kThreads = 384;
+constexpr int kWarpLoadK = 8;
+constexpr int kWarpMma0 = 9;   // MMA issuer of tile 0 (also owns the TMEM allocation)
+constexpr int kWarpLoadV = 10;
+constexpr int kWarpMma1 = 11;  // MMA issuer of tile 1
+// Launched at 168 registers per thread (384 x 168 = 64512 of the SM's 65536).
+constexpr int kRegsSoftmax = 200;
+constexpr int kRegsControl = 88;
+static_assert(256 * kRegsSoftmax + 128 * kRegsControl <= kThreads * 168, "register split");
+
+// Named barriers that make the two softmax warpgroups take turns on the
+// exponentials (barrier 0 is __syncthreads): tile 0 waits on kTurn0, tile 1 on kTurn1.
+constexpr uint32_t kTurn0 = 1, kTurn1 = 2;
+constexpr bool kPingPong = true;
+
 constexpr int kRowsPerCta = 256;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr uint32_t kBoxBytes = 128 * 64 * 2;  // one 128-row x 64-column bf16 box
@@ -51,22 +73,23 @@ template <int D>
 struct Cfg {
     static constexpr int kBoxes = D / 64;
     static constexpr int kTileBytes = 128 * D * 2;
-    static constexpr int kStages = (D == 128) ? 2 : 4;
+    static constexpr int kKStages = (D == 128) ? 3 : 5;
+    static constexpr int kVStages = (D == 128) ? 2 : 4;
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + 2 * kTileBytes;
-    static constexpr int kOffV = kOffK + kStages * kTileBytes;
-    static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+    static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+    static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
     // barrier indices
     static constexpr int kBarQ = 0;
     static constexpr int kBarKFull = 1;
-    static constexpr int kBarKEmpty = kBarKFull + kStages;
-    static constexpr int kBarVFull = kBarKEmpty + kStages;
-    static constexpr int kBarVEmpty = kBarVFull + kStages;
-    static constexpr int kBarS = kBarVEmpty + kStages;  // 2
-    static constexpr int kBarP = kBarS + 2;             // 2
-    static constexpr int kBarO = kBarP + 2;             // 2
-    static constexpr int kBarDrain = kBarO + 2;
-    static constexpr int kNumBars = kBarDrain + 1;
+    static constexpr int kBarKEmpty = kBarKFull + kKStages;
+    static constexpr int kBarVFull = kBarKEmpty + kKStages;
+    static constexpr int kBarVEmpty = kBarVFull + kVStages;
+    static constexpr int kBarS = kBarVEmpty + kVStages;  // 2: S_t ready
+    static constexpr int kBarP = kBarS + 2;              // 2: P_t written (one arrival per warp)
+    static constexpr int kBarO = kBarP + 2;              // 2: final O_t ready
+    static constexpr int kBarDrain = kBarO + 2;  // 2: one per issuer
+    static constexpr int kNumBars = kBarDrain + 2;
     static constexpr int kOffSlot = kOffBar + 8 * kNumBars;  // TMEM base address + abort flag
     static constexpr int kSmemUsed = kOffSlot + 16;
     static constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base to 1024 B
@@ -85,31 +108,342 @@ struct TcParams {
     int* err_word;
 };
 
+// Per-CTA state shared by the role functions.
+struct Cta {
+    uint32_t sbase;       // shared-memory base (1024-aligned)
+    uint32_t bar0;        // address of barrier 0
+    uint32_t tmem;        // TMEM base address
+    volatile int* abort;  // set when any wait gave up
+    int b, head;
+    int row0[2];          // first query row of each tile
+    int nblk[2];          // key blocks each tile multiplies (0: tile absent)
+    int nblk_max;
+    int kv_len;
+    bool causal;
+    __device__ uint32_t bar(int i) const { return bar0 + 8u * i; }
+};
+
+__device__ __forceinline__ void give_up(const Cta& c, int* err_word)
+{
+    *c.abort = 1;
+    raise_device_error(err_word, HATTN_ETIMEOUT);
+}
+
+// The MMA issue loops run on warps that share their SM sub-partition with busy
+// softmax warps, so each MMA costs as few instructions as possible: shared-memory
+// descriptors are built once per operand tile and stepped by adding the K-step
+// offset (in 16-byte units) to the start-address field.
+
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem)
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc)
 {
     using C = Cfg<D>;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
         // 16-element K step: box (ks / 4), 32-byte offset inside the swizzled 128-byte row.
-        const uint32_t off = (ks / 4) * kBoxBytes + (ks % 4) * 32;
-        mma_ss(d_tmem, sdesc_sw128(q_smem + off, 16, 1024), sdesc_sw128(k_smem + off, 16, 1024),
-               C::kIdescS, ks > 0 ? 1u : 0u);
+        const uint64_t off = ((ks / 4) * kBoxBytes + (ks % 4) * 32) >> 4;
+        mma_ss(d_tmem, q_desc + off, k_desc + off, C::kIdescS, ks > 0 ? 1u : 0u);
     }
 }
 
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
                                          bool accumulate)
 {
     using C = Cfg<D>;
 #pragma unroll
-    for (int ks = 0; ks < 128 / 16; ++ks) {
+    for (int ks = 0; ks < 8; ++ks) {
         // 16 keys = 16 rows of the V tile (2 swizzle atoms of 8 rows); P columns hold bf16 pairs.
-        mma_ts(d_tmem, p_tmem + ks * 8, sdesc_sw128(v_smem + ks * 2048, kBoxBytes, 1024),
-               C::kIdescPV, (accumulate || ks > 0) ? 1u : 0u);
+        mma_ts(d_tmem, p_tmem + ks * 8, v_desc + ((ks * 2048) >> 4), C::kIdescPV,
+               (accumulate || ks > 0) ? 1u : 0u);
     }
 }
+
+// ---------------------------------------------------------------- TMA producers
+
+template <int D>
+__device__ void produce_qk(const Cta& c, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                           int* err_word)
+{
+    using C = Cfg<D>;
+    const int n_tiles = c.nblk[1] > 0 ? 2 : 1;
+    mbar_arrive_expect_tx(c.bar(C::kBarQ), n_tiles * C::kTileBytes);
+    for (int t = 0; t < n_tiles; ++t)
+        for (int x = 0; x < C::kBoxes; ++x)
+            tma_load_4d(c.sbase + C::kOffQ + t * C::kTileBytes + x * kBoxBytes, tm_q,
+                        c.bar(C::kBarQ), x * 64, c.head, c.row0[t], c.b);
+    int issued = 0;
+    for (int j = 0; j < c.nblk_max; ++j) {
+        const int s = j % C::kKStages;
+        if (*c.abort || !mbar_wait(c.bar(C::kBarKEmpty + s), ((j / C::kKStages) & 1) ^ 1)) {
+            give_up(c, err_word);
+            break;
+        }
+        mbar_arrive_expect_tx(c.bar(C::kBarKFull + s), C::kTileBytes);
+        for (int x = 0; x < C::kBoxes; ++x)
+            tma_load_4d(c.sbase + C::kOffK + s * C::kTileBytes + x * kBoxBytes, tm_k,
+                        c.bar(C::kBarKFull + s), x * 64, c.head, j * 128, c.b);
+        ++issued;
+    }
+    // Every copy this CTA started must land before the CTA may exit.
+    mbar_wait(c.bar(C::kBarQ), 0);
+    for (int j = max(0, issued - C::kKStages); j < issued; ++j)
+        mbar_wait(c.bar(C::kBarKFull + j % C::kKStages), (j / C::kKStages) & 1);
+}
+
+template <int D>
+__device__ void produce_v(const Cta& c, const CUtensorMap* tm_v, int* err_word)
+{
+    using C = Cfg<D>;
+    int issued = 0;
+    for (int j = 0; j < c.nblk_max; ++j) {
+        const int s = j % C::kVStages;
+        if (*c.abort || !mbar_wait(c.bar(C::kBarVEmpty + s), ((j / C::kVStages) & 1) ^ 1)) {
+            give_up(c, err_word);
+            break;
+        }
+        mbar_arrive_expect_tx(c.bar(C::kBarVFull + s), C::kTileBytes);
+        for (int x = 0; x < C::kBoxes; ++x)
+            tma_load_4d(c.sbase + C::kOffV + s * C::kTileBytes + x * kBoxBytes, tm_v,
+                        c.bar(C::kBarVFull + s), x * 64, c.head, j * 128, c.b);
+        ++issued;
+    }
+    for (int j = max(0, issued - C::kVStages); j < issued; ++j)
+        mbar_wait(c.bar(C::kBarVFull + j % C::kVStages), (j / C::kVStages) & 1);
+}
+
+// ---------------------------------------------------------------- MMA issuers
+
+// Issues every MMA of tile t (one thread). The K/V "empty" barriers expect one
+// arrival per issuer and block: a block this tile does not multiply is
+// released by a plain arrive once its copy has landed (so the arrival belongs
+// to the phase of that block).
+template <int D>
+__device__ void issue_tile_mmas(const Cta& c, int t, int nb, uint32_t sQ, int* err_word)
+{
+    using C = Cfg<D>;
+    const uint32_t tS = c.tmem + 256u * t, tO = tS + 128u;
+    // K-major Q/K tiles: SBO = 1024 (8-row groups); MN-major V: LBO = one 64-column box.
+    const uint64_t q_desc = sdesc_sw128(sQ, 16, 1024);
+    const uint64_t k_desc0 = sdesc_sw128(c.sbase + C::kOffK, 16, 1024);
+    const uint64_t v_desc0 = sdesc_sw128(c.sbase + C::kOffV, kBoxBytes, 1024);
+    auto kdesc = [&](int s) { return k_desc0 + static_cast<uint64_t>((s * C::kTileBytes) >> 4); };
+    auto vdesc = [&](int s) { return v_desc0 + static_cast<uint64_t>((s * C::kTileBytes) >> 4); };
+
+    bool ok = mbar_wait(c.bar(C::kBarQ), 0) && mbar_wait(c.bar(C::kBarKFull), 0);
+    if (ok) {
+        tc_fence_after();
+        issue_qk<D>(tS, q_desc, kdesc(0));
+        mma_commit(c.bar(C::kBarS + t));
+        mma_commit(c.bar(C::kBarKEmpty));
+    }
+    for (int j = 0; ok && j < c.nblk_max; ++j) {
+        const int sv = j % C::kVStages, sk1 = (j + 1) % C::kKStages;
+        const uint32_t phv = (j / C::kVStages) & 1, phk1 = ((j + 1) / C::kKStages) & 1;
+        const bool has_next = j + 1 < c.nblk_max;
+        if (!mbar_wait(c.bar(C::kBarVFull + sv), phv)) { ok = false; break; }
+        if (j < nb) {
+            if (*c.abort || !mbar_wait(c.bar(C::kBarP + t), j & 1)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv<D>(tO, tS, vdesc(sv), j > 0);
+            if (j == nb - 1) mma_commit(c.bar(C::kBarO + t));
+            mma_commit(c.bar(C::kBarVEmpty + sv));
+            if (has_next) {
+                if (!mbar_wait(c.bar(C::kBarKFull + sk1), phk1)) { ok = false; break; }
+                if (j + 1 < nb) {
+                    tc_fence_after();
+                    issue_qk<D>(tS, q_desc, kdesc(sk1));
+                    mma_commit(c.bar(C::kBarS + t));
+                    mma_commit(c.bar(C::kBarKEmpty + sk1));
+                } else {
+                    mbar_arrive(c.bar(C::kBarKEmpty + sk1));
+                }
+            }
+        } else {
+            mbar_arrive(c.bar(C::kBarVEmpty + sv));
+            if (has_next) {
+                if (!mbar_wait(c.bar(C::kBarKFull + sk1), phk1)) { ok = false; break; }
+                mbar_arrive(c.bar(C::kBarKEmpty + sk1));
+            }
+        }
+    }
+    if (!ok) give_up(c, err_word);
+    // All issued MMAs must complete before TMEM is released.
+    mma_commit(c.bar(C::kBarDrain + t));
+    mbar_wait(c.bar(C::kBarDrain + t), 0);
+}
+
+// ---------------------------------------------------------------- softmax + epilogue
+
+// p = 2^(s * c - m) for the 128 scores of this thread's row, packed to bf16 and
+// stored over the first 64 TMEM columns of S; the fp32 sum goes to acc. With
+// kMax, the row max of the raw scores is computed alongside (on the ALU pipe,
+// while the exponentials occupy MUFU and FMA) and returned.
+template <bool kMax>
+__device__ __forceinline__ float exp_block(const uint32_t (&sr)[128], uint64_t c2, uint64_t nm2,
+                                           uint64_t (&acc)[4], uint32_t p_taddr)
+{
+    float mx = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int e = 32 * q + 2 * i;
+            const uint64_t x2 =
+                fma_f32x2(f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nm2);
+            float t0, t1;
+            f32x2_split(x2, t0, t1);
+            const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+            acc[i & 3] = add_f32x2(acc[i & 3], f32x2(p0, p1));
+            pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st_x16(p_taddr + 16 * q, pk);
+        if (kMax) {
+            const uint32_t* v = sr + 32 * q;
+            float g[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t* v8 = v + 8 * k;
+                g[k] = max3f(max3f(__uint_as_float(v8[0]), __uint_as_float(v8[1]), __uint_as_float(v8[2])),
+                             max3f(__uint_as_float(v8[3]), __uint_as_float(v8[4]), __uint_as_float(v8[5])),
+                             fmaxf(__uint_as_float(v8[6]), __uint_as_float(v8[7])));
+            }
+            mx = max3f(mx, max3f(g[0], g[1], g[2]), g[3]);
+        }
+    }
+    return mx;
+}
+
+// Row max of the 128 raw scores (a tree of independent 3-input maxima).
+__device__ __forceinline__ float row_max(const uint32_t (&sr)[128])
+{
+    float part[16];
+#pragma unroll
+    for (int g = 0; g < 16; ++g) {
+        const uint32_t* v8 = sr + 8 * g;
+        const float a = max3f(__uint_as_float(v8[0]), __uint_as_float(v8[1]), __uint_as_float(v8[2]));
+        const float e = max3f(__uint_as_float(v8[3]), __uint_as_float(v8[4]), __uint_as_float(v8[5]));
+        part[g] = max3f(a, e, fmaxf(__uint_as_float(v8[6]), __uint_as_float(v8[7])));
+    }
+#pragma unroll
+    for (int g = 0; g < 5; ++g) part[g] = max3f(part[g], part[g + 5], part[g + 10]);
+    return max3f(max3f(part[0], part[1], part[2]), part[3], fmaxf(part[4], part[15]));
+}
+
+template <int D>
+__device__ void softmax_tile(const Cta& c, const TcParams& p, int t, int wq, int lane)
+{
+    using C = Cfg<D>;
+    const int r = wq * 32 + lane;
+    const int my_row0 = c.row0[t];
+    const int row = my_row0 + r;
+    const uint32_t lane_base = c.tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t cS = 256u * t, cO = 256u * t + 128u;
+    const int nb = c.nblk[t];
+    const uint32_t my_turn = t ? kTurn1 : kTurn0, other_turn = t ? kTurn0 : kTurn1;
+    float m_used = -INFINITY, l = 0.0f;
+    bool ok = true;
+    // Turn protocol over nblk_max rounds (every round is taken, with or without
+    // work, so both warpgroups pass the named barriers the same number of times):
+    // tile 0 waits for its turn, works, hands the turn over; tile 1 hands tile 0
+    // the first turn, then waits, works, and hands it back (except after the last).
+    if (kPingPong && t == 1) named_arrive(kTurn0, 256);
+    for (int j = 0; j < c.nblk_max; ++j) {
+        const bool work = ok && j < nb;
+        uint32_t sr[128];  // raw scores q.k of this row for keys kbase .. kbase + 127
+        if (work) {
+            const bool got = mbar_wait(c.bar(C::kBarS + t), j & 1);
+            ok = __all_sync(0xffffffffu, got);
+        }
+        if (work && ok) {
+            tc_fence_after();
+            tmem_ld_x128(lane_base + cS, sr);
+            const int kbase = j * 128;
+            const bool need_mask = (kbase + 128 > c.kv_len) || (c.causal && kbase + 127 > my_row0);
+            if (need_mask) {
+#pragma unroll
+                for (int i = 0; i < 128; ++i) {
+                    const int kj = kbase + i;
+                    const bool visible = (kj < c.kv_len) && !(c.causal && kj > row);
+                    if (!visible) sr[i] = __float_as_uint(-INFINITY);
+                }
+            }
+            // The first block sets the running max before its exponentials.
+            if (j == 0) m_used = row_max(sr) * p.scale_log2;
+        }
+        if (kPingPong) named_sync(my_turn, 256);
+        if (work && ok) {
+            // p = 2^(s * scale * log2(e) - m) with the running max m (scale > 0, so
+            // the max of scale * s is scale * max s). After the first block the
+            // block's own max is found alongside the exponentials; a row whose max
+            // grows by more than 2^8 (rare) rescales O and l and redoes the block.
+            const uint64_t c2 = f32x2(p.scale_log2, p.scale_log2);
+            uint64_t acc[4] = {0, 0, 0, 0};
+            const float mx = exp_block<true>(sr, c2, f32x2(-m_used, -m_used), acc, lane_base + cS) *
+                             p.scale_log2;
+            const bool grow = j > 0 && mx > m_used + kRescaleLog2;
+            if (__any_sync(0xffffffffu, grow)) {
+                const float m_new = grow ? mx : m_used;
+                const float alpha = ex2_approx(m_used - m_new);  // 1 where the max is kept
+#pragma unroll
+                for (int q = 0; q < D / 16; ++q) {
+                    uint32_t o[16];
+                    tmem_ld_x16(lane_base + cO + 16 * q, o);  // PV up to block j-1 is complete
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st_x16(lane_base + cO + 16 * q, o);
+                }
+                l *= alpha;
+                m_used = m_new;
+                acc[0] = acc[1] = acc[2] = acc[3] = 0;
+                exp_block<false>(sr, c2, f32x2(-m_used, -m_used), acc, lane_base + cS);
+            }
+            if (kPingPong && (t == 0 || j + 1 < c.nblk_max)) named_arrive(other_turn, 256);
+            float a0, a1;
+            f32x2_split(add_f32x2(add_f32x2(acc[0], acc[1]), add_f32x2(acc[2], acc[3])), a0, a1);
+            l += a0 + a1;
+            // Each thread's TMEM stores are complete and fenced before the warp
+            // synchronises; one arrival per warp (128 single-thread arrivals on one
+            // barrier word would serialise).
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(c.bar(C::kBarP + t));
+        } else if (kPingPong && (t == 0 || j + 1 < c.nblk_max)) {
+            named_arrive(other_turn, 256);
+        }
+    }
+    if (nb > 0 && ok) {
+        const bool got = mbar_wait(c.bar(C::kBarO + t), 0);
+        ok = __all_sync(0xffffffffu, got);
+    }
+    if (!ok) {
+        give_up(c, p.err_word);
+        return;
+    }
+    if (nb == 0) return;
+    tc_fence_after();
+    const float inv = 1.0f / l;
+    __nv_bfloat16* orow = p.out + (((size_t)c.b * p.n_q + row) * p.h + c.head) * D;
+#pragma unroll
+    for (int q = 0; q < D / 32; ++q) {
+        uint32_t o[32];
+        tmem_ld_x32(lane_base + cO + 32 * q, o);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+        if (row < p.n_q) {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+                st_global_v4(orow + 32 * q + 8 * v4, pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
+                             pk[4 * v4 + 3]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- kernel
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -120,269 +454,101 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const uint32_t sbase = smem_u32(smem);
-    auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffSlot);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffSlot + 4);
-
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const bool causal = (p.mask_kind & HATTN_MASK_CAUSAL) != 0;
 
-    // ---- work unit: heaviest causal rows first
-    const int bh_count = p.B * p.h;
-    int pair = blockIdx.x / bh_count;
-    const int bh = blockIdx.x % bh_count;
-    if (causal) pair = p.n_pairs - 1 - pair;
-    const int b = bh / p.h, head = bh % p.h;
-    const int row0_0 = pair * kRowsPerCta, row0_1 = row0_0 + 128;
+    Cta c;
+    c.sbase = smem_u32(smem);
+    c.bar0 = c.sbase + C::kOffBar;
+    c.abort = reinterpret_cast<volatile int*>(smem + C::kOffSlot + 4);
+    c.causal = (p.mask_kind & HATTN_MASK_CAUSAL) != 0;
+    // Work unit: (batch, head)-major so that the CTAs resident at one time share
+    // K/V in L2; within a head, the heaviest causal rows first.
+    const int bh = blockIdx.x / p.n_pairs;
+    int pair = blockIdx.x % p.n_pairs;
+    if (c.causal) pair = p.n_pairs - 1 - pair;
+    c.b = bh / p.h;
+    c.head = bh % p.h;
+    c.row0[0] = pair * kRowsPerCta;
+    c.row0[1] = c.row0[0] + 128;
 
-    int kv_len = p.n_k;
-    if (p.mask_kind & HATTN_MASK_KEY_PADDING) kv_len = p.key_lens[b];
-    if (kv_len < 1 || kv_len > p.n_k) {
+    c.kv_len = p.n_k;
+    if (p.mask_kind & HATTN_MASK_KEY_PADDING) c.kv_len = p.key_lens[c.b];
+    if (c.kv_len < 1 || c.kv_len > p.n_k) {
         if (threadIdx.x < 256) {
-            const int row = (threadIdx.x < 128 ? row0_0 : row0_1) + threadIdx.x % 128;
+            const int row = c.row0[threadIdx.x / 128] + threadIdx.x % 128;
             if (row < p.n_q) {
-                __nv_bfloat16* orow = p.out + (((size_t)b * p.n_q + row) * p.h + head) * D;
-                for (int c = 0; c < D; c += 8) st_global_v4(orow + c, 0u, 0u, 0u, 0u);
+                __nv_bfloat16* orow = p.out + (((size_t)c.b * p.n_q + row) * p.h + c.head) * D;
+                for (int k = 0; k < D; k += 8) st_global_v4(orow + k, 0u, 0u, 0u, 0u);
             }
         }
         if (threadIdx.x == 0) raise_device_error(p.err_word, HATTN_EKEYLEN);
         return;
     }
-    const int kv_blocks = (kv_len + 127) / 128;
-    auto blocks_for = [&](int r0) {
-        if (r0 >= p.n_q) return 0;
-        return causal ? min(kv_blocks, r0 / 128 + 1) : kv_blocks;
-    };
-    const int nblk_0 = blocks_for(row0_0), nblk_1 = blocks_for(row0_1);
-    const int nblk_max = max(nblk_0, nblk_1);
+    const int kv_blocks = (c.kv_len + 127) / 128;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        if (c.row0[t] >= p.n_q) c.nblk[t] = 0;
+        else c.nblk[t] = c.causal ? min(kv_blocks, c.row0[t] / 128 + 1) : kv_blocks;
+    }
+    c.nblk_max = max(c.nblk[0], c.nblk[1]);
 
-    // ---- setup
     if (threadIdx.x == 0) {
-        mbar_init(bar(C::kBarQ), 1);
-        for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(bar(C::kBarKFull + s), 1);
-            mbar_init(bar(C::kBarKEmpty + s), 1);
-            mbar_init(bar(C::kBarVFull + s), 1);
-            mbar_init(bar(C::kBarVEmpty + s), 1);
+        mbar_init(c.bar(C::kBarQ), 1);
+        const int issuers = c.nblk[1] > 0 ? 2 : 1;
+        for (int s = 0; s < C::kKStages; ++s) {
+            mbar_init(c.bar(C::kBarKFull + s), 1);
+            mbar_init(c.bar(C::kBarKEmpty + s), issuers);
+        }
+        for (int s = 0; s < C::kVStages; ++s) {
+            mbar_init(c.bar(C::kBarVFull + s), 1);
+            mbar_init(c.bar(C::kBarVEmpty + s), issuers);
         }
         for (int t = 0; t < 2; ++t) {
-            mbar_init(bar(C::kBarS + t), 1);
-            mbar_init(bar(C::kBarP + t), 128);
-            mbar_init(bar(C::kBarO + t), 1);
+            mbar_init(c.bar(C::kBarS + t), 1);
+            mbar_init(c.bar(C::kBarP + t), 4);
+            mbar_init(c.bar(C::kBarO + t), 1);
         }
-        mbar_init(bar(C::kBarDrain), 1);
-        *abort_flag = 0;
+        mbar_init(c.bar(C::kBarDrain), 1);
+        mbar_init(c.bar(C::kBarDrain + 1), 1);
+        *c.abort = 0;
         fence_barrier_init();
     }
-    if (warp == kWarpMma) {
+    if (warp == kWarpMma0) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
-    if (warp == kWarpLoad && lane == 0) {
+    if (warp == kWarpLoadK && lane == 0) {
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
-        prefetch_tmap(&tm_v);
     }
+    if (warp == kWarpLoadV && lane == 0) prefetch_tmap(&tm_v);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    c.tmem = *tmem_slot;
 
-    auto give_up = [&]() {
-        *abort_flag = 1;
-        raise_device_error(p.err_word, HATTN_ETIMEOUT);
-    };
-
-    if (warp == kWarpLoad) {
-        // ================================================================ TMA producer
+    if (warp >= 8) {
+        regs_dec<kRegsControl>();
         if (lane == 0) {
-            const int n_tiles = nblk_1 > 0 ? 2 : 1;
-            mbar_arrive_expect_tx(bar(C::kBarQ), n_tiles * C::kTileBytes);
-            for (int t = 0; t < n_tiles; ++t)
-                for (int x = 0; x < C::kBoxes; ++x)
-                    tma_load_4d(sbase + C::kOffQ + t * C::kTileBytes + x * kBoxBytes, &tm_q,
-                                bar(C::kBarQ), x * 64, head, t ? row0_1 : row0_0, b);
-            int k_issued = 0, v_issued = 0;
-            bool ok = true;
-            for (int j = 0; j < nblk_max; ++j) {
-                const int s = j % C::kStages;
-                const uint32_t ph = (j / C::kStages) & 1;
-                if (*abort_flag || !mbar_wait(bar(C::kBarKEmpty + s), ph ^ 1)) { ok = false; break; }
-                mbar_arrive_expect_tx(bar(C::kBarKFull + s), C::kTileBytes);
-                for (int x = 0; x < C::kBoxes; ++x)
-                    tma_load_4d(sbase + C::kOffK + s * C::kTileBytes + x * kBoxBytes, &tm_k,
-                                bar(C::kBarKFull + s), x * 64, head, j * 128, b);
-                ++k_issued;
-                if (*abort_flag || !mbar_wait(bar(C::kBarVEmpty + s), ph ^ 1)) { ok = false; break; }
-                mbar_arrive_expect_tx(bar(C::kBarVFull + s), C::kTileBytes);
-                for (int x = 0; x < C::kBoxes; ++x)
-                    tma_load_4d(sbase + C::kOffV + s * C::kTileBytes + x * kBoxBytes, &tm_v,
-                                bar(C::kBarVFull + s), x * 64, head, j * 128, b);
-                ++v_issued;
-            }
-            if (!ok) give_up();
-            // Every copy this CTA started must land before the CTA may exit.
-            mbar_wait(bar(C::kBarQ), 0);
-            for (int j = max(0, k_issued - C::kStages); j < k_issued; ++j)
-                mbar_wait(bar(C::kBarKFull + j % C::kStages), (j / C::kStages) & 1);
-            for (int j = max(0, v_issued - C::kStages); j < v_issued; ++j)
-                mbar_wait(bar(C::kBarVFull + j % C::kStages), (j / C::kStages) & 1);
-        }
-    } else if (warp == kWarpMma) {
-        // ================================================================ MMA issuer
-        if (lane == 0) {
-            const uint32_t sQ0 = sbase + C::kOffQ, sQ1 = sQ0 + C::kTileBytes;
-            auto sK = [&](int s) { return sbase + C::kOffK + s * C::kTileBytes; };
-            auto sV = [&](int s) { return sbase + C::kOffV + s * C::kTileBytes; };
-            bool ok = mbar_wait(bar(C::kBarQ), 0) && mbar_wait(bar(C::kBarKFull), 0);
-            if (ok) {
-                tc_fence_after();
-                if (nblk_0 > 0) {
-                    issue_qk<D>(tmem, sQ0, sK(0));
-                    mma_commit(bar(C::kBarS));
-                }
-                if (nblk_1 > 0) {
-                    issue_qk<D>(tmem + 256, sQ1, sK(0));
-                    mma_commit(bar(C::kBarS + 1));
-                }
-                mma_commit(bar(C::kBarKEmpty));
-            }
-            // PV of tile t for block j, then at once S of tile t for block j + 1.
-            auto tile_step = [&](int t, int nb, uint32_t sQ, int j, int s, int s1) -> bool {
-                if (j >= nb) return true;
-                if (*abort_flag || !mbar_wait(bar(C::kBarP + t), j & 1)) return false;
-                tc_fence_after();
-                issue_pv<D>(tmem + 256 * t + 128, tmem + 256 * t, sV(s), j > 0);
-                if (j == nb - 1) mma_commit(bar(C::kBarO + t));
-                if (j + 1 < nb) {
-                    issue_qk<D>(tmem + 256 * t, sQ, sK(s1));
-                    mma_commit(bar(C::kBarS + t));
-                }
-                return true;
-            };
-            for (int j = 0; ok && j < nblk_max; ++j) {
-                const int s = j % C::kStages, s1 = (j + 1) % C::kStages;
-                const uint32_t ph = (j / C::kStages) & 1, ph1 = ((j + 1) / C::kStages) & 1;
-                const bool next = j + 1 < nblk_max;
-                if (!mbar_wait(bar(C::kBarVFull + s), ph)) { ok = false; break; }
-                if (next && !mbar_wait(bar(C::kBarKFull + s1), ph1)) { ok = false; break; }
-                tc_fence_after();
-                if (!tile_step(0, nblk_0, sQ0, j, s, s1) || !tile_step(1, nblk_1, sQ1, j, s, s1)) {
-                    ok = false;
-                    break;
-                }
-                mma_commit(bar(C::kBarVEmpty + s));
-                if (next) mma_commit(bar(C::kBarKEmpty + s1));
-            }
-            if (!ok) give_up();
-            // All issued MMAs must complete before TMEM is released.
-            mma_commit(bar(C::kBarDrain));
-            mbar_wait(bar(C::kBarDrain), 0);
+            if (warp == kWarpLoadK) produce_qk<D>(c, &tm_q, &tm_k, p.err_word);
+            else if (warp == kWarpLoadV) produce_v<D>(c, &tm_v, p.err_word);
+            else if (warp == kWarpMma0)
+                issue_tile_mmas<D>(c, 0, c.nblk[0], c.sbase + C::kOffQ, p.err_word);
+            else if (warp == kWarpMma1 && c.nblk[1] > 0)
+                issue_tile_mmas<D>(c, 1, c.nblk[1], c.sbase + C::kOffQ + C::kTileBytes, p.err_word);
         }
         __syncwarp();
     } else {
-        // ================================================================ softmax + epilogue
-        const int t = warp / 4;
-        const int wq = warp % 4;
-        const int r = wq * 32 + lane;
-        const int my_row0 = t ? row0_1 : row0_0;
-        const int row = my_row0 + r;
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-        const uint32_t cS = 256u * t, cO = 256u * t + 128u;
-        const int nb = t ? nblk_1 : nblk_0;
-        float m_used = -INFINITY, l = 0.0f;
-        bool ok = true;
-        for (int j = 0; j < nb; ++j) {
-            bool got = mbar_wait(bar(C::kBarS + t), j & 1);
-            if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-            tc_fence_after();
-            float x[128];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t raw[32];
-                tmem_ld_x32(lane_base + cS + 32 * c, raw);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) x[32 * c + i] = __uint_as_float(raw[i]) * p.scale_log2;
-            }
-            const int kbase = j * 128;
-            const bool need_mask = (kbase + 128 > kv_len) || (causal && kbase + 127 > my_row0);
-            if (need_mask) {
-#pragma unroll
-                for (int i = 0; i < 128; ++i) {
-                    const int kj = kbase + i;
-                    const bool visible = (kj < kv_len) && !(causal && kj > row);
-                    if (!visible) x[i] = -INFINITY;
-                }
-            }
-            float mx = x[0];
-#pragma unroll
-            for (int i = 1; i < 128; ++i) mx = fmaxf(mx, x[i]);
-            const float m_new = fmaxf(m_used, mx);
-            const bool grow = m_new > m_used + kRescaleLog2;
-            if (j > 0 && __any_sync(0xffffffffu, grow)) {
-                const float alpha = grow ? ex2_approx(m_used - m_new) : 1.0f;
-#pragma unroll
-                for (int c = 0; c < D / 16; ++c) {
-                    uint32_t o[16];
-                    tmem_ld_x16(lane_base + cO + 16 * c, o);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st_x16(lane_base + cO + 16 * c, o);
-                }
-                l *= alpha;
-            }
-            if (grow) m_used = m_new;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float p0 = ex2_approx(x[32 * c + 2 * i] - m_used);
-                    const float p1 = ex2_approx(x[32 * c + 2 * i + 1] - m_used);
-                    l += p0 + p1;
-                    pk[i] = pack_bf16x2(p0, p1);
-                }
-                tmem_st_x16(lane_base + cS + 16 * c, pk);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(bar(C::kBarP + t));
-        }
-        if (nb > 0 && ok) {
-            bool got = mbar_wait(bar(C::kBarO + t), 0);
-            ok = __all_sync(0xffffffffu, got);
-        }
-        if (!ok) {
-            give_up();
-        } else if (nb > 0) {
-            tc_fence_after();
-            const float inv = 1.0f / l;
-            __nv_bfloat16* orow = p.out + (((size_t)b * p.n_q + row) * p.h + head) * D;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld_x32(lane_base + cO + 32 * c, o);
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv,
-                                        __uint_as_float(o[2 * i + 1]) * inv);
-                if (row < p.n_q) {
-#pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4)
-                        st_global_v4(orow + 32 * c + 8 * v4, pk[4 * v4], pk[4 * v4 + 1],
-                                     pk[4 * v4 + 2], pk[4 * v4 + 3]);
-                }
-            }
-        }
+        regs_inc<kRegsSoftmax>();
+        softmax_tile<D>(c, p, warp / 4, warp % 4, lane);
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kWarpMma) {
+    if (warp == kWarpMma0) {
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc(c.tmem, 512);
     }
 }
 
@@ -415,7 +581,8 @@ cudaError_t launch_d(const AttnArgs& a, const AttnMaps& m)
 
 bool attn_tc_supported(const AttnArgs& a)
 {
-    return a.dtype == HATTN_BF16 && a.d_k == a.d_v && (a.d_k == 64 || a.d_k == 128);
+    return a.dtype == HATTN_BF16 && a.d_k == a.d_v && (a.d_k == 64 || a.d_k == 128) &&
+           a.scale > 0.0f;
 }
 
 cudaError_t launch_attn_tc(const AttnArgs& a, const AttnMaps& maps)
