@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     check_device_error,
     load,
     mha_fwd,
+    mha_fwd_noalloc_raw,
     mha_fwd_raw,
     mha_workspace_bytes,
     status_str,

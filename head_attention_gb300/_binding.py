@@ -16,10 +16,11 @@ from . import builder as _build
 
 HATTN_F32, HATTN_BF16 = 0, 1
 MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING = 0, 1, 2
-OK, EINVAL, EUNSUPPORTED, ECUDA, ETIMEOUT, EKEYLEN, EWORKSPACE = 0, -1, -2, -3, -4, -5, -6
+OK, EINVAL, EUNSUPPORTED, ECUDA, ETIMEOUT, EKEYLEN, EWORKSPACE, ESCRATCH = 0, -1, -2, -3, -4, -5, -6, -7
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 # Every symbol include/hattn.h declares.
-EXPORTED = ("attn_fwd", "mha_fwd", "mha_workspace_bytes", "hattn_status_str",
+EXPORTED = ("attn_fwd", "mha_fwd", "mha_fwd_noalloc", "mha_workspace_bytes", "hattn_status_str",
             "hattn_check_device_error", "hattn_version")
 
 _lock = threading.Lock()
@@ -51,6 +52,8 @@ def load() -> ctypes.CDLL:
         lib.attn_fwd.restype = i
         lib.mha_fwd.argtypes = [vp] * 8 + [f, vp, i, i, i, i, i, i, i, i, i, vp, vp, sz, vp]
         lib.mha_fwd.restype = i
+        lib.mha_fwd_noalloc.argtypes = [vp] * 8 + [f, vp, i, i, i, i, i, i, i, i, i, vp, vp]
+        lib.mha_fwd_noalloc.restype = i
         lib.mha_workspace_bytes.argtypes = [i] * 8
         lib.mha_workspace_bytes.restype = sz
         lib.hattn_status_str.argtypes = [i]
@@ -153,6 +156,15 @@ def mha_fwd(x_q, x_kv, wq, wk, wv, wo, gamma, beta, eps, h, y=None, mask_kind=MA
     if rc != OK:
         raise HattnError(rc, "mha_fwd")
     return y
+
+
+def mha_fwd_noalloc_raw(x_q, x_kv, wq, wk, wv, wo, gamma, beta, eps, y, dtype, B, n_q, n_k,
+                        d_model, h, d_k, d_v, mask_kind, key_lens, stream) -> int:
+    """mha_fwd without a workspace argument: the library's static scratch is used."""
+    return load().mha_fwd_noalloc(_ptr(x_q), _ptr(x_kv), _ptr(wq), _ptr(wk), _ptr(wv), _ptr(wo),
+                                  _ptr(gamma), _ptr(beta), float(eps), _ptr(y), int(dtype), int(B),
+                                  int(n_q), int(n_k), int(d_model), int(h), int(d_k), int(d_v),
+                                  int(mask_kind), _ptr(key_lens), _stream(stream))
 
 
 def check_device_error(stream=None) -> int:

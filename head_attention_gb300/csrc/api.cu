@@ -314,6 +314,57 @@ int mha_fwd(const void* x_q, const void* x_kv, const void* Wq, const void* Wk, c
     return from_cuda(launch_outproj_ln(o, st, err));
 }
 
+}  // extern "C"
+
+namespace hattn {
+namespace {
+
+// The static scratch of mha_fwd_noalloc: Q, K, V and the concatenated heads of
+// one call, laid out exactly as mha_fwd lays out its workspace.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[HATTN_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on the current device, looked up once per
+// device with that device current (host code only has a stand-in for the name).
+void* noalloc_scratch_ptr()
+{
+    static void* cache[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        cache[dev] = p;
+    }
+    return cache[dev];
+}
+
+}  // namespace
+}  // namespace hattn
+
+extern "C" {
+
+int mha_fwd_noalloc(const void* x_q, const void* x_kv, const void* Wq, const void* Wk,
+                    const void* Wv, const void* Wo, const float* gamma, const float* beta,
+                    float eps, void* y, int dtype, int B, int n_q, int n_k, int d_model, int h,
+                    int d_k, int d_v, int mask_kind, const int32_t* key_lens,
+                    hattn_stream_t stream)
+{
+    // Sizes first: an oversized request is rejected before any CUDA call.
+    const size_t need = mha_workspace_bytes(dtype, B, n_q, n_k, d_model, h, d_k, d_v);
+    if (need > HATTN_NOALLOC_SCRATCH_BYTES) return HATTN_ESCRATCH;
+    if (need == 0) {
+        // Bad sizes or dtype: let mha_fwd's own checks report them (no workspace needed).
+        return mha_fwd(x_q, x_kv, Wq, Wk, Wv, Wo, gamma, beta, eps, y, dtype, B, n_q, n_k,
+                       d_model, h, d_k, d_v, mask_kind, key_lens, nullptr, 0, stream);
+    }
+    void* scratch = noalloc_scratch_ptr();
+    if (!scratch) return HATTN_ECUDA;
+    return mha_fwd(x_q, x_kv, Wq, Wk, Wv, Wo, gamma, beta, eps, y, dtype, B, n_q, n_k, d_model,
+                   h, d_k, d_v, mask_kind, key_lens, scratch, HATTN_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 const char* hattn_status_str(int status)
 {
     switch (status) {
@@ -324,6 +375,7 @@ const char* hattn_status_str(int status)
     case HATTN_ETIMEOUT: return "device pipeline wait timed out";
     case HATTN_EKEYLEN: return "key length outside [1, n_k]";
     case HATTN_EWORKSPACE: return "workspace missing, misaligned or too small";
+    case HATTN_ESCRATCH: return "problem needs more than the 32 MiB static scratch of mha_fwd_noalloc";
     default: return "unknown status";
     }
 }

@@ -50,6 +50,7 @@ typedef struct CUstream_st* hattn_stream_t;
 #define HATTN_ETIMEOUT (-4)     /* device: a pipeline wait gave up (reported asynchronously) */
 #define HATTN_EKEYLEN (-5)      /* device: key_lens[b] outside [1, n_k] (reported asynchronously) */
 #define HATTN_EWORKSPACE (-6)   /* workspace NULL or smaller than mha_workspace_bytes()   */
+#define HATTN_ESCRATCH (-7)     /* problem needs more scratch than mha_fwd_noalloc's static buffer */
 
 /*
  * attn_fwd — multi-head scaled dot-product attention,
@@ -120,6 +121,41 @@ int mha_fwd(const void* x_q, const void* x_kv, const void* Wq, const void* Wk, c
             const void* Wo, const float* gamma, const float* beta, float eps, void* y, int dtype,
             int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v, int mask_kind,
             const int32_t* key_lens, void* workspace, size_t ws_bytes, hattn_stream_t stream);
+
+/*
+ * mha_fwd_noalloc — mha_fwd for callers that must not allocate device memory.
+ *
+ * The explanatory pages have no counterpart to this entry point; it exists
+ * for deployment. Some callers are not allowed to allocate device memory
+ * themselves: a plugin inside a host process that owns the whole device-memory
+ * budget, or latency-critical code that forbids allocation after start-up
+ * (cudaMalloc can synchronise the device and can fail under memory pressure).
+ * Such callers cannot provide the workspace mha_fwd needs. This entry point
+ * takes the same arguments as mha_fwd minus the workspace and uses instead a
+ * scratch buffer of HATTN_NOALLOC_SCRATCH_BYTES (32 MiB) that the library
+ * holds as a static device array: every GPU that loads the library keeps those
+ * 32 MiB until the process exits. It allocates no device memory: neither this
+ * function nor anything it calls calls cudaMalloc, cudaFree or a device
+ * allocator (only the host-side cache of tensor-map descriptors that every
+ * entry point of this library shares may grow).
+ *
+ *   - The first call on a device looks up the buffer's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Sizes whose mha_workspace_bytes() exceeds the buffer are rejected with
+ *     HATTN_ESCRATCH before anything is enqueued (the B=16, n=512,
+ *     d_model=512, h=8, d=64 sublayer needs exactly 32 MiB).
+ *   - Every call shares the one buffer and overwrites it completely before
+ *     reading it (nothing in it has to start at zero); calls whose work overlaps
+ *     on the GPU (different streams, or different host threads) race on it and
+ *     give undefined results. Serialise them, e.g. on one stream.
+ * Other arguments, supported sizes and status codes are those of mha_fwd.
+ */
+#define HATTN_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+int mha_fwd_noalloc(const void* x_q, const void* x_kv, const void* Wq, const void* Wk,
+                    const void* Wv, const void* Wo, const float* gamma, const float* beta,
+                    float eps, void* y, int dtype, int B, int n_q, int n_k, int d_model, int h,
+                    int d_k, int d_v, int mask_kind, const int32_t* key_lens,
+                    hattn_stream_t stream);
 
 /* Bytes of caller-owned workspace mha_fwd needs for these sizes (0 on bad sizes). */
 size_t mha_workspace_bytes(int dtype, int B, int n_q, int n_k, int d_model, int h, int d_k,

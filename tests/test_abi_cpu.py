@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in (0, -1, -2, -3, -4, -5, -6):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
         assert hattn.status_str(code) not in ("", "unknown status")
     assert hattn.status_str(12345) == "unknown status"
     assert hattn.version() >= 100
@@ -115,3 +115,14 @@ def test_workspace_size_is_q_k_v_and_heads(lib):
     assert n2 == up(3 * 64 * 2) + 2 * up(5 * 64 * 2) + up(3 * 64 * 2)
     assert hattn.mha_workspace_bytes(0, 16, 512, 512, 512, 8, 64, 64) == 0
     assert hattn.mha_workspace_bytes(1, 0, 512, 512, 512, 8, 64, 64) == 0
+
+
+def test_noalloc_rejects_problems_beyond_its_static_scratch(lib):
+    # Checked before any CUDA call, so it runs without a GPU.
+    args = dict(MHA)
+    del args["workspace"], args["ws_bytes"]
+    assert hattn.mha_workspace_bytes(1, 16, 512, 512, 512, 8, 64, 64) == hattn._binding.NOALLOC_SCRATCH_BYTES
+    args.update(B=17)
+    assert hattn.mha_fwd_noalloc_raw(**args) == hattn._binding.ESCRATCH
+    args.update(B=16, n_q=1024, n_k=1024)
+    assert hattn.mha_fwd_noalloc_raw(**args) == hattn._binding.ESCRATCH
