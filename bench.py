@@ -5,12 +5,16 @@
 
 One step is one attn_fwd call (the whole hot path: tile loads, QK^T, masking,
 streaming softmax, PV, epilogue) over one batch of seeded synthetic inputs
-already resident in HBM. Default workload: long-sequence causal
+already resident in HBM; for the MHA sublayer workload it is one mha_fwd call
+(Q/K/V projections, attention, output projection with residual + LayerNorm).
+The timed steps replay a CUDA graph of one step (no per-call host overhead;
+--no-graph times eager calls instead). Default workload: long-sequence causal
 self-attention, bf16, B=4 h=16 n=8192 d=128 (Q, K, V and O are 134 MB each, so
 the 402 MB of inputs are larger than the 129 MB L2 and every step streams
 them from HBM).
 
-FLOPs per step are the defined count 4*B*h*n_q*n_k*d, halved for causal.
+FLOPs per step are the defined count 4*B*h*n_q*n_k*d, halved for causal (plus
+2*M*N*K for each of the four projections of the MHA sublayer).
 Timing: W untimed warm-up steps, then exactly K steps between two CUDA events
 on the launching stream, bracketed by a barrier and a device synchronize;
 max over ranks. SM clocks and throttle reasons are sampled with nvidia-smi
@@ -67,6 +71,8 @@ def parse_args(argv=None):
                     help="CPU seconds of oracle work for the CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time eager calls instead of CUDA-graph replays of one step")
     return ap.parse_args(argv)
 
 
@@ -87,6 +93,12 @@ def reduce_max(value: float, world: int) -> float:
     t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_tflops(flops_per_rank_step: float, world: int, ms_per_step_max: float) -> float:
+    """Whole-job throughput under weak scaling: every rank processes one step's
+    FLOPs per step, and the job takes the slowest rank's time."""
+    return flops_per_rank_step * world / (ms_per_step_max * 1e-3) / 1e12
 
 
 def barrier(world: int):
@@ -226,44 +238,115 @@ def _rows_flops(w, rows, kv_len):
 
 
 def oracle_sample_rate(w, inp, budget_s: float, sample_index: int = 0):
-    """Times the oracle on query rows of one (batch, head) until ~budget_s of
-    work; returns (TFLOP/s, threads, description)."""
+    """Times the oracle on whole (batch, head) units of the workload, one after
+    another from unit `sample_index` on, until about budget_s seconds of work;
+    returns (TFLOP/s, threads, description) counting the exact FLOPs of the
+    visible (query, key) pairs the oracle computed."""
     import oracle
     threads = os.cpu_count() or 1
-    b = sample_index % w.B
-    i = (sample_index // w.B) % w.h
-    q, k, v = _head_arrays(inp, w, b, i)
-    kv_len = int(inp["key_lens"][b]) if inp.get("key_lens") is not None else w.n_k
-    kl = None if inp.get("key_lens") is None else inp["key_lens"][b:b + 1]
-    # Calibrate on a strided subset, then scale the row count to the budget.
-    stride = max(1, w.n_q // 64)
-    rows = list(range(stride // 2, w.n_q, stride))
-    t0 = time.perf_counter()
-    sel = [(0, t, 0) for t in rows]
-    oracle.attn_rows(q, k, v, w.scale, sel, w.mask_kind, kl, nthreads=threads)
-    dt = time.perf_counter() - t0
-    flops = _rows_flops(w, rows, kv_len)
-    rate = flops / max(dt, 1e-9)
-    want = budget_s * rate
-    total_flops = _rows_flops(w, range(w.n_q), kv_len)
-    frac = min(1.0, want / total_flops)
-    n_rows = max(1, int(frac * w.n_q))
-    stride = max(1, w.n_q // n_rows)
-    rows = list(range(stride // 2, w.n_q, stride))
-    sel = [(0, t, 0) for t in rows]
-    t0 = time.perf_counter()
-    oracle.attn_rows(q, k, v, w.scale, sel, w.mask_kind, kl, nthreads=threads)
-    dt = time.perf_counter() - t0
-    flops = _rows_flops(w, rows, kv_len)
-    desc = (f"{len(rows)} of {w.n_q} query rows (every {stride}th) of (batch {b}, head {i}); "
-            f"{flops / 1e9:.2f} GFLOP of visible (query, key) pairs in {dt:.2f} s")
-    return flops / dt / 1e12, threads, desc
+    n_units = w.B * w.h
+    done, flops, elapsed = [], 0.0, 0.0
+    while elapsed < budget_s and len(done) < n_units:
+        u = (sample_index + len(done)) % n_units
+        b, i = u % w.B, u // w.B
+        q, k, v = _head_arrays(inp, w, b, i)
+        kv_len = int(inp["key_lens"][b]) if inp.get("key_lens") is not None else w.n_k
+        kl = None if inp.get("key_lens") is None else inp["key_lens"][b:b + 1]
+        t0 = time.perf_counter()
+        oracle.attn(q, k, v, w.scale, w.mask_kind, kl, nthreads=threads)
+        elapsed += time.perf_counter() - t0
+        flops += _rows_flops(w, range(w.n_q), kv_len)
+        done.append((b, i))
+    desc = (f"{len(done)} of {n_units} (batch, head) units, all {w.n_q} query rows each; "
+            f"{flops / 1e9:.2f} GFLOP of visible (query, key) pairs in {elapsed:.2f} s")
+    return flops / elapsed / 1e12, threads, desc
+
+
+def oracle_mha_sample_rate(w, inp, budget_s: float, sample_index: int = 0):
+    """Times the oracle's MHA sublayer on whole batch elements (all their query
+    rows, their K/V projections included), one after another, until about
+    budget_s seconds of work; returns (TFLOP/s, threads, description) counting
+    the FLOPs the oracle performed."""
+    import oracle
+    from synth import inputs as synth
+    threads = os.cpu_count() or 1
+    wd = {n: synth.widen(inp[n], "bf16") for n in ("wq", "wk", "wv", "wo")}
+    g64, b64 = inp["gamma"].astype("float64"), inp["beta"].astype("float64")
+    hdk, hdv = w.h * w.d_k, w.h * w.d_v
+    per_elem = (2.0 * w.n_k * w.d_model * (hdk + hdv)
+                + w.n_q * (2.0 * w.d_model * hdk + 4.0 * w.n_k * w.h * w.d_k + 2.0 * hdv * w.d_model))
+    done, elapsed = 0, 0.0
+    while elapsed < budget_s and done < w.B:
+        b = (sample_index + done) % w.B
+        x_q = synth.widen(inp["x_q"][b:b + 1].copy(), "bf16")
+        x_kv = synth.widen(inp["x_kv"][b:b + 1].copy(), "bf16")
+        kl = None if inp["key_lens"] is None else inp["key_lens"][b:b + 1]
+        t0 = time.perf_counter()
+        oracle.mha(x_q, x_kv, wd["wq"], wd["wk"], wd["wv"], wd["wo"], g64, b64, inp["eps"], w.h,
+                   w.mask_kind, kl, nthreads=threads)
+        elapsed += time.perf_counter() - t0
+        done += 1
+    flops = per_elem * done
+    desc = (f"{done} of {w.B} batch elements, whole sublayer (projections, attention, "
+            f"output projection, LayerNorm); {flops / 1e9:.2f} GFLOP in {elapsed:.2f} s")
+    return flops / elapsed / 1e12, threads, desc
+
+
+def sample_rate(w, inp, budget_s: float, sample_index: int = 0):
+    if w.is_mha:
+        return oracle_mha_sample_rate(w, inp, budget_s, sample_index)
+    return oracle_sample_rate(w, inp, budget_s, sample_index)
 
 
 # ---------------------------------------------------------------- GPU arm
 
-def run_gpu(args, rank, world, local):
+def _device_array(a, dtype):
     import numpy as np
+    import torch
+    if dtype == "f32":
+        return torch.from_numpy(a).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def _setup_attention(w, inp):
+    """Device tensors and a step closure for one attn_fwd call."""
+    import torch
+
+    import head_attention_gb300 as hattn
+    q, k, v = (_device_array(inp[n], w.dtype) for n in ("q", "k", "v"))
+    kl = None if inp["key_lens"] is None else torch.from_numpy(inp["key_lens"]).cuda()
+    out = torch.empty((w.B, w.n_q, w.h, w.d_v), dtype=q.dtype, device="cuda")
+
+    def step():
+        hattn.attn_fwd(q, k, v, out=out, scale=w.scale, mask_kind=w.mask_kind, key_lens=kl)
+
+    host = {"inputs": {"q": (inp["q"], q), "k": (inp["k"], k), "v": (inp["v"], v)},
+            "output": out}
+    return step, host, 1
+
+
+def _setup_mha(w, inp):
+    """Device tensors, workspace and a step closure for one mha_fwd call."""
+    import torch
+
+    import head_attention_gb300 as hattn
+    dev = {n: _device_array(inp[n], "bf16") for n in ("x_q", "x_kv", "wq", "wk", "wv", "wo")}
+    gamma = torch.from_numpy(inp["gamma"]).cuda()
+    beta = torch.from_numpy(inp["beta"]).cuda()
+    kl = None if inp["key_lens"] is None else torch.from_numpy(inp["key_lens"]).cuda()
+    y = torch.empty_like(dev["x_q"])
+    ws = torch.empty(hattn.mha_workspace_bytes(hattn.HATTN_BF16, w.B, w.n_q, w.n_k, w.d_model, w.h,
+                                               w.d_k, w.d_v), dtype=torch.uint8, device="cuda")
+
+    def step():
+        hattn.mha_fwd(dev["x_q"], dev["x_kv"], dev["wq"], dev["wk"], dev["wv"], dev["wo"], gamma,
+                      beta, inp["eps"], w.h, y=y, mask_kind=w.mask_kind, key_lens=kl, workspace=ws)
+
+    host = {"inputs": {"x_q": (inp["x_q"], dev["x_q"])}, "output": y}
+    return step, host, 3
+
+
+def run_gpu(args, rank, world, local):
     import torch
 
     import head_attention_gb300 as hattn
@@ -277,28 +360,28 @@ def run_gpu(args, rank, world, local):
     hattn.load()
     w = synth.workload(args.workload)
     if w.is_mha:
-        raise SystemExit("bench.py times attn_fwd; use an attention workload")
-    inp = synth.attn_inputs(w)
-
-    def dev(a):
-        if w.dtype == "f32":
-            return torch.from_numpy(a).cuda()
-        return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
-
-    q, k, v = dev(inp["q"]), dev(inp["k"]), dev(inp["v"])
-    kl = None if inp["key_lens"] is None else torch.from_numpy(inp["key_lens"]).cuda()
-    out = torch.empty((w.B, w.n_q, w.h, w.d_v), dtype=q.dtype, device="cuda")
+        inp = synth.mha_inputs(w)
+        step, host, launches_per_step = _setup_mha(w, inp)
+        flops = w.attn_flops() + w.proj_flops()
+    else:
+        inp = synth.attn_inputs(w)
+        step, host, launches_per_step = _setup_attention(w, inp)
+        flops = w.attn_flops()
     stream = torch.cuda.current_stream()
-
-    def step():
-        hattn.attn_fwd(q, k, v, out=out, scale=w.scale, mask_kind=w.mask_kind, key_lens=kl,
-                       stream=stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     if hattn.check_device_error(stream) != 0:
         raise RuntimeError("device error during warm-up")
+    run_step = step
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        graph.replay()
+        torch.cuda.synchronize()
+        run_step = graph.replay
 
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(gpu_uuid(local))
@@ -309,7 +392,7 @@ def run_gpu(args, rank, world, local):
         t_wall0 = time.time()
         start.record(stream)
         for _ in range(args.steps):
-            step()
+            run_step()
         end.record(stream)
         torch.cuda.synchronize()
         t_wall1 = time.time()
@@ -321,19 +404,24 @@ def run_gpu(args, rank, world, local):
         raise RuntimeError("device error during the timed region")
     ms_total = reduce_max(ms_local, world)
     ms_step = ms_total / args.steps
-    flops = w.attn_flops()
-    tflops = flops * world / (ms_step * 1e-3) / 1e12
+    tflops = aggregate_tflops(flops, world, ms_step)
     tokens_s = w.tokens() * world / (ms_step * 1e-3)
 
     peaks, peak_src = load_peaks()
-    kernel_ms = ms_local / args.steps  # one launch per step on this stream
-    achieved = flops / (kernel_ms * 1e-3) / 1e12
+    step_ms = ms_local / args.steps
+    achieved = flops / (step_ms * 1e-3) / 1e12
     esize = 4 if w.dtype == "f32" else 2
-    bytes_in = (w.B * w.n_q * w.h * w.d_k + w.B * w.n_k * w.h * (w.d_k + w.d_v)) * esize
-    bytes_alg = bytes_in + w.B * w.n_q * w.h * w.d_v * esize
+    if w.is_mha:
+        bytes_in = (2 * w.B * w.n_q * w.d_model + 4 * w.d_model * w.h * w.d_k) * esize
+        bytes_alg = bytes_in + w.B * w.n_q * w.d_model * esize
+    else:
+        bytes_in = (w.B * w.n_q * w.h * w.d_k + w.B * w.n_k * w.h * (w.d_k + w.d_v)) * esize
+        bytes_alg = bytes_in + w.B * w.n_q * w.h * w.d_v * esize
+    tc_attn = w.dtype == "bf16" and w.d_k == w.d_v and w.d_k in (64, 128)
+    kernel = ("mha sublayer: proj_gemm + attn_tc_kernel + outproj_ln (one step)" if w.is_mha
+              else f"attn_tc_kernel<{w.d_k}>" if tc_attn else "attn_simt_kernel")
     roofline = {
-        "kernel": f"attn_tc_kernel<{w.d_k}>" if w.dtype == "bf16" and w.d_k == w.d_v
-        and w.d_k in (64, 128) else "attn_simt_kernel",
+        "kernel": kernel,
         "bound": "tensor",
         "achieved": round(achieved, 2),
         "peak": peaks["bf16_tflops"],
@@ -344,7 +432,8 @@ def run_gpu(args, rank, world, local):
         "frac_of_nominal_2250": round(achieved / NOMINAL_BF16_TFLOPS, 4),
         "algorithmic_flops_per_launch": flops,
         "algorithmic_bytes_per_launch": bytes_alg,
-        "hbm_gbs_at_algorithmic_bytes": round(bytes_alg / (kernel_ms * 1e-3) / 1e9, 1),
+        "hbm_gbs_at_algorithmic_bytes": round(bytes_alg / (step_ms * 1e-3) / 1e9, 1),
+        "hbm_frac_at_algorithmic_bytes": round(bytes_alg / (step_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
         "traffic": profiled_traffic(w.name),
     }
 
@@ -360,11 +449,12 @@ def run_gpu(args, rank, world, local):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": w.dtype,
-        "data": "synthetic: seeded Philox N(0,1) inputs rounded to bf16 (no dataset)",
+        "data": "synthetic: seeded Philox N(0,1) inputs rounded to the kernel dtype (no dataset)",
         "config": {"workload": w.name, "description": w.description, "B": w.B, "h": w.h,
                    "n_q": w.n_q, "n_k": w.n_k, "d": w.d_k,
                    "mask": {0: "none", 1: "causal", 2: "key_padding", 3: "causal+key_padding"}[
                        w.mask_kind],
+                   "timing": "CUDA-graph replay of one step" if not args.no_graph else "eager calls",
                    "parallelism": f"replicas x{world} (independent (batch, head) work per GPU)",
                    "l2": (f"inputs {bytes_in / 1e6:.0f} MB > 129 MB L2: streamed from HBM every step, no flush"
                           if bytes_in > 129e6 else
@@ -373,15 +463,17 @@ def run_gpu(args, rank, world, local):
         "pct_of_measured_bf16_peak": round(100 * tflops / world / peaks["bf16_tflops"], 2),
         "pct_of_nominal_bf16_peak": round(100 * tflops / world / NOMINAL_BF16_TFLOPS, 2),
         "roofline": roofline,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": sampler.summary(),
     }
+    if w.is_mha:
+        result["config"]["d_model"] = w.d_model
 
     if not args.no_e2e:
-        result["e2e"] = e2e_leg(args, w, inp, q, k, v, kl, out, stream, world)
-        result["gpu_launches"] += result["e2e"].pop("launches")
+        result["e2e"] = e2e_leg(args, w, host, step, flops, world)
+        result["gpu_launches"] += result["e2e"].pop("launches") * launches_per_step
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, threads, desc = oracle_sample_rate(w, inp, args.cpu_budget_s)
+        rate, threads, desc = sample_rate(w, inp, args.cpu_budget_s)
         result["cpu_baseline"] = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads,
                                   "kind": "oracle", "sample": desc}
     if world > 1:
@@ -390,47 +482,47 @@ def run_gpu(args, rank, world, local):
     return result
 
 
-def e2e_leg(args, w, inp, q, k, v, kl, out, stream, world):
-    """Same metric with host buffers: every step copies Q, K, V from pinned host
-    memory, runs attn_fwd, and copies the output back to pinned host memory."""
+def e2e_leg(args, w, host, step, flops, world):
+    """Same metric through the public API with host buffers: every step copies
+    the step's inputs from pinned host memory to the device, runs the eager
+    call, and copies the result back to pinned host memory."""
     import numpy as np
     import torch
 
-    import head_attention_gb300 as hattn
-
     def pinned(a):
-        t = torch.from_numpy(a if w.dtype == "f32" else a.view(np.int16))
+        t = torch.from_numpy(np.ascontiguousarray(a) if w.dtype == "f32"
+                             else np.ascontiguousarray(a).view(np.int16))
         t = t.pin_memory()
         return t if w.dtype == "f32" else t.view(torch.bfloat16)
 
-    hq, hk, hv = pinned(inp["q"]), pinned(inp["k"]), pinned(inp["v"])
+    pairs = [(pinned(h), d) for h, d in host["inputs"].values()]
+    out = host["output"]
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    stream = torch.cuda.current_stream()
     steps = max(1, min(args.steps, 100))
 
-    def step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        hattn.attn_fwd(q, k, v, out=out, scale=w.scale, mask_kind=w.mask_kind, key_lens=kl,
-                       stream=stream)
+    def e2e_step():
+        for h, d in pairs:
+            d.copy_(h, non_blocking=True)
+        step()
         hout.copy_(out, non_blocking=True)
 
     for _ in range(3):
-        step()
+        e2e_step()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     start.record(stream)
     for _ in range(steps):
-        step()
+        e2e_step()
     end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     ms = reduce_max(start.elapsed_time(end), world) / steps
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    h2d = sum(h.numel() * h.element_size() for h, _ in pairs)
     d2h = hout.numel() * hout.element_size()
-    return {"value": round(w.attn_flops() * world / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+    return {"value": round(flops * world / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 4), "steps": steps, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "launches": steps}
 
@@ -442,17 +534,17 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     w = synth.workload(args.workload)
-    inp = synth.attn_inputs(w)
+    inp = synth.mha_inputs(w) if w.is_mha else synth.attn_inputs(w)
     total_budget_s = 150.0
     per_step = max(0.5, total_budget_s / max(1, args.steps + args.warmup))
     for i in range(args.warmup):
-        oracle_sample_rate(w, inp, per_step, sample_index=i)
+        sample_rate(w, inp, per_step, sample_index=i)
     rates = []
     descs = []
     t0 = time.perf_counter()
     threads = os.cpu_count() or 1
     for i in range(args.steps):
-        rate, threads, desc = oracle_sample_rate(w, inp, per_step, sample_index=args.warmup + i)
+        rate, threads, desc = sample_rate(w, inp, per_step, sample_index=args.warmup + i)
         rates.append(rate)
         descs.append(desc)
     elapsed = time.perf_counter() - t0
