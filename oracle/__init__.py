@@ -76,6 +76,8 @@ def _load():
         lib.oracle_mha_rows.argtypes = ([dp] * 8 + [c_double] + [c_int] * 8 + [ip, ip, c_int, dp,
                                                                                c_int])
         lib.oracle_mha_rows.restype = c_int
+        lib.oracle_pos_encoding.argtypes = [dp, dp, c_int, c_int, c_int, c_double, c_int]
+        lib.oracle_pos_encoding.restype = c_int
         _lib = lib
         return lib
 
@@ -231,3 +233,15 @@ def mha_rows(x_q, x_kv, wq, wk, wv, wo, gamma, beta, eps, h, sel, mask_kind=MASK
                              int(nthreads))
     _check(rc, "oracle_mha_rows")
     return y
+
+
+def pos_encoding(B, n, d_model, emb=None, emb_scale=1.0, pos0=0) -> np.ndarray:
+    """Sinusoidal encoding of positions pos0 .. pos0+n-1 added to emb * emb_scale
+    (emb [B, n, d_model] fp64, or None for the encoding alone) -> [B, n, d_model]."""
+    lib = _load()
+    out = np.empty((B, n, d_model), dtype=np.float64)
+    e = None if emb is None else _f64(emb)
+    rc = lib.oracle_pos_encoding(None if e is None else _dp(e), _dp(out), int(B), int(n),
+                                 int(d_model), float(emb_scale), int(pos0))
+    _check(rc, "oracle_pos_encoding")
+    return out

@@ -371,3 +371,30 @@ done:
     free(vis);
     return rc;
 }
+
+/*
+ * Sinusoidal positional encoding added to scaled embeddings:
+ *   out[b,t,2i]   = emb_scale * emb[b,t,2i]   + sin((pos0 + t) / 10000^(2i/d_model))
+ *   out[b,t,2i+1] = emb_scale * emb[b,t,2i+1] + cos((pos0 + t) / 10000^(2i/d_model))
+ * [research-heat "做法 · Attention Is All You Need", §去掉循环，因而须补回顺序]:
+ * PE(pos, 2i) = sin(pos / 10000^(2i/d_model)), PE(pos, 2i+1) = cos(...);
+ * [hex4c59, §没有循环，模型怎样知道词序？]: the embedding, multiplied by
+ * sqrt(d_model), and the encoding are added. emb may be NULL (encoding only).
+ * d_model must be even.
+ */
+int oracle_pos_encoding(const double* emb, double* out, int B, int n, int d_model,
+                        double emb_scale, int pos0)
+{
+    if (B <= 0 || n <= 0 || d_model <= 0 || (d_model & 1)) return ORACLE_EINVAL;
+    for (int b = 0; b < B; ++b)
+        for (int t = 0; t < n; ++t)
+            for (int i = 0; i < d_model / 2; ++i) {
+                const double angle = (double)(pos0 + t) / pow(10000.0, 2.0 * i / d_model);
+                const size_t at = ((size_t)b * n + t) * d_model + 2 * i;
+                const double e0 = emb ? emb_scale * emb[at] : 0.0;
+                const double e1 = emb ? emb_scale * emb[at + 1] : 0.0;
+                out[at] = e0 + sin(angle);
+                out[at + 1] = e1 + cos(angle);
+            }
+    return ORACLE_OK;
+}

@@ -356,3 +356,42 @@ def test_generator_rounding_and_key_lengths():
     kl = synth.draw_key_lens(2, synth.STREAM_KEYLEN, 20000, 64, 256)
     assert kl.min() == 64 and kl.max() == 256
     assert np.array_equal(kl, synth.draw_key_lens(2, synth.STREAM_KEYLEN, 20000, 64, 256))
+
+
+# ---------------------------------------------------------------- positional encoding
+
+def test_pos_encoding_printed_table():
+    rows = []
+    with open(os.path.join(GOLDEN, "pe_table_5x4.txt"), encoding="utf-8") as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                rows.append([float(x) for x in line.split()])
+    pe = oracle.pos_encoding(1, 5, 4)[0]
+    # Within one unit of the last printed digit: the page prints cos(0.01) =
+    # 0.99995000... as 0.9999 (correct rounding gives 1.0000); every other entry
+    # matches to the printed four decimals.
+    np.testing.assert_allclose(pe, np.array(rows), rtol=0, atol=1e-4)
+    mismatched = np.round(pe, 4) != np.array(rows)
+    assert mismatched.sum() == 1 and mismatched[1, 3]
+
+
+def test_pos_encoding_relative_shift_is_a_rotation():
+    # For each frequency pair, PE(pos + k) is PE(pos) rotated by the angle k * w_i:
+    # a linear map that depends only on k (the pages' motivation for sin/cos pairs).
+    d, k = 16, 7
+    pe = oracle.pos_encoding(1, 64, d)[0]
+    for i in range(d // 2):
+        w = 10000.0 ** (-2.0 * i / d)
+        rot = np.array([[math.cos(k * w), -math.sin(k * w)], [math.sin(k * w), math.cos(k * w)]])
+        pair = pe[:, 2 * i:2 * i + 2]
+        np.testing.assert_allclose(pair[k:], pair[:-k] @ rot, atol=1e-12)
+
+
+def test_pos_encoding_embedding_scale_and_offset():
+    rng = np.random.default_rng(15)
+    emb = rng.standard_normal((2, 6, 8))
+    full = oracle.pos_encoding(2, 6, 8, emb=emb, emb_scale=math.sqrt(8), pos0=3)
+    pe = oracle.pos_encoding(1, 9, 8)[0]
+    np.testing.assert_allclose(full, emb * math.sqrt(8) + pe[3:9][None], atol=1e-14)
+    # Position 0: sin(0) = 0 on even dimensions, cos(0) = 1 on odd ones.
+    np.testing.assert_array_equal(oracle.pos_encoding(1, 1, 8)[0, 0], [0, 1] * 4)
