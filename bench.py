@@ -50,6 +50,12 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd TFLOP/s and % of GB300 BF16 tensor peak (1 GPU); tokens/s"
+PE_METRIC = "positional encoding GB/s (HBM-bound elementwise)"
+
+
+def metric_of(w):
+    """(metric, unit) of a workload's bench line."""
+    return (PE_METRIC, "GB/s") if w.kind == "pe" else (METRIC, "TFLOP/s")
 DEFAULT_WORKLOAD = "long_causal_d128"
 NOMINAL_BF16_TFLOPS = 2250.0
 NOMINAL_HBM_GBS = 8000.0
@@ -73,6 +79,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="time eager calls instead of CUDA-graph replays of one step")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch size B (smaller cases for profiler "
+                         "captures; the default keeps the named workload)")
     return ap.parse_args(argv)
 
 
@@ -292,7 +301,50 @@ def oracle_mha_sample_rate(w, inp, budget_s: float, sample_index: int = 0):
     return flops / elapsed / 1e12, threads, desc
 
 
+def oracle_pe_sample_rate(w, inp, budget_s: float, sample_index: int = 0):
+    """Times the oracle's positional encoding on whole batch elements until about
+    budget_s seconds of work; returns (GB/s of algorithmic bytes: one read of the
+    embeddings and one write of the result, at the kernel's element size,
+    threads, description)."""
+    import oracle
+    from synth import inputs as synth
+    done, elapsed, nbytes = 0, 0.0, 0.0
+    while elapsed < budget_s and done < w.B:
+        b = (sample_index + done) % w.B
+        emb = synth.widen(inp["emb"][b:b + 1].copy(), "bf16")
+        t0 = time.perf_counter()
+        oracle.pos_encoding(1, w.n_q, w.d_model, emb, w.d_model ** 0.5)
+        elapsed += time.perf_counter() - t0
+        nbytes += 2.0 * w.n_q * w.d_model * 2
+        done += 1
+    desc = (f"{done} of {w.B} batch elements ({w.n_q} x {w.d_model} each), single-threaded; "
+            f"{nbytes / 1e6:.1f} MB in {elapsed:.2f} s")
+    return nbytes / elapsed / 1e9, 1, desc
+
+
+def pe_inputs(w):
+    from synth import inputs as synth
+    return {"emb": synth.round_to_bf16_bits(synth.draw_normal(w.seed, 0, (w.B, w.n_q, w.d_model)))}
+
+
+def workload_inputs(w):
+    from synth import inputs as synth
+    if w.kind == "pe":
+        return pe_inputs(w)
+    return synth.mha_inputs(w) if w.kind == "mha" else synth.attn_inputs(w)
+
+
+def load_workload(args):
+    from synth import inputs as synth
+    w = synth.workload(args.workload)
+    if args.batch > 0:
+        w = w.with_(B=args.batch)
+    return w
+
+
 def sample_rate(w, inp, budget_s: float, sample_index: int = 0):
+    if w.kind == "pe":
+        return oracle_pe_sample_rate(w, inp, budget_s, sample_index)
     if w.is_mha:
         return oracle_mha_sample_rate(w, inp, budget_s, sample_index)
     return oracle_sample_rate(w, inp, budget_s, sample_index)
@@ -346,6 +398,39 @@ def _setup_mha(w, inp):
     return step, host, 3
 
 
+def _setup_decode(w, inp):
+    """Device tensors, workspace and a step closure for one attn_decode_fwd call."""
+    import torch
+
+    import head_attention_gb300 as hattn
+    q, k, v = (_device_array(inp[n], "bf16") for n in ("q", "k", "v"))
+    kl = torch.from_numpy(inp["key_lens"]).cuda()
+    out = torch.empty_like(q)
+    ws = torch.empty(hattn.attn_decode_workspace_bytes(w.B, w.h, w.n_k, w.d_k), dtype=torch.uint8,
+                     device="cuda")
+
+    def step():
+        hattn.attn_decode_fwd(q, k, v, kl, out=out, scale=w.scale, workspace=ws)
+
+    host = {"inputs": {"q": (inp["q"], q)}, "output": out}
+    return step, host, 2
+
+
+def _setup_pe(w, inp):
+    """Embeddings on the device and a step closure for one pos_encoding_fwd call."""
+    import torch
+
+    import head_attention_gb300 as hattn
+    emb = _device_array(inp["emb"], "bf16")
+    out = torch.empty_like(emb)
+
+    def step():
+        hattn.pos_encoding_fwd(out, emb=emb, emb_scale=w.d_model ** 0.5)
+
+    host = {"inputs": {"emb": (inp["emb"], emb)}, "output": out}
+    return step, host, 1
+
+
 def run_gpu(args, rank, world, local):
     import torch
 
@@ -358,11 +443,19 @@ def run_gpu(args, rank, world, local):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     hattn.build()
     hattn.load()
-    w = synth.workload(args.workload)
-    if w.is_mha:
+    w = load_workload(args)
+    if w.kind == "mha":
         inp = synth.mha_inputs(w)
         step, host, launches_per_step = _setup_mha(w, inp)
         flops = w.attn_flops() + w.proj_flops()
+    elif w.kind == "decode":
+        inp = synth.attn_inputs(w)
+        step, host, launches_per_step = _setup_decode(w, inp)
+        flops = 4.0 * w.h * w.d_k * float(inp["key_lens"].sum())  # visible (query, key) pairs
+    elif w.kind == "pe":
+        inp = pe_inputs(w)
+        step, host, launches_per_step = _setup_pe(w, inp)
+        flops = 0.0
     else:
         inp = synth.attn_inputs(w)
         step, host, launches_per_step = _setup_attention(w, inp)
@@ -411,25 +504,36 @@ def run_gpu(args, rank, world, local):
     step_ms = ms_local / args.steps
     achieved = flops / (step_ms * 1e-3) / 1e12
     esize = 4 if w.dtype == "f32" else 2
-    if w.is_mha:
+    if w.kind == "mha":
         bytes_in = (2 * w.B * w.n_q * w.d_model + 4 * w.d_model * w.h * w.d_k) * esize
         bytes_alg = bytes_in + w.B * w.n_q * w.d_model * esize
+    elif w.kind == "decode":
+        bytes_in = (float(inp["key_lens"].sum()) * w.h * (w.d_k + w.d_v) + w.B * w.h * w.d_k) * esize
+        bytes_alg = bytes_in + w.B * w.h * w.d_v * esize
+    elif w.kind == "pe":
+        bytes_in = w.B * w.n_q * w.d_model * esize
+        bytes_alg = 2 * bytes_in
     else:
         bytes_in = (w.B * w.n_q * w.h * w.d_k + w.B * w.n_k * w.h * (w.d_k + w.d_v)) * esize
         bytes_alg = bytes_in + w.B * w.n_q * w.h * w.d_v * esize
     tc_attn = w.dtype == "bf16" and w.d_k == w.d_v and w.d_k in (64, 128)
-    kernel = ("mha sublayer: proj_gemm + attn_tc_kernel + outproj_ln (one step)" if w.is_mha
-              else f"attn_tc_kernel<{w.d_k}>" if tc_attn else "attn_simt_kernel")
+    kernel = {"mha": "mha sublayer: proj_gemm + attn_tc_kernel + outproj_ln (one step)",
+              "decode": f"decode_split_kernel<{w.d_k}> + decode_combine_kernel (one step)",
+              "pe": "pos_encoding_kernel"}.get(
+                  w.kind, f"attn_tc_kernel<{w.d_k}>" if tc_attn else "attn_simt_kernel")
+    hbm_bound = w.kind in ("decode", "pe")
+    gbs = bytes_alg / (step_ms * 1e-3) / 1e9
     roofline = {
         "kernel": kernel,
-        "bound": "tensor",
-        "achieved": round(achieved, 2),
-        "peak": peaks["bf16_tflops"],
-        "unit": "TFLOP/s",
-        "frac": round(achieved / peaks["bf16_tflops"], 4),
-        "peak_source": f"{peak_src} (burst, MEASURED_PEAKS.json bf16_tflops)",
-        "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
-        "frac_of_nominal_2250": round(achieved / NOMINAL_BF16_TFLOPS, 4),
+        "bound": "hbm" if hbm_bound else "tensor",
+        "achieved": round(gbs if hbm_bound else achieved, 2),
+        "peak": peaks["hbm_gbs"] if hbm_bound else peaks["bf16_tflops"],
+        "unit": "GB/s" if hbm_bound else "TFLOP/s",
+        "frac": round(gbs / peaks["hbm_gbs"] if hbm_bound else achieved / peaks["bf16_tflops"], 4),
+        "peak_source": (f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if hbm_bound else
+                        f"{peak_src} (burst, MEASURED_PEAKS.json bf16_tflops)"),
+        "frac_of_sustained": None if hbm_bound else round(achieved / peaks["bf16_tflops_sustained"], 4),
+        "frac_of_nominal_2250": None if hbm_bound else round(achieved / NOMINAL_BF16_TFLOPS, 4),
         "algorithmic_flops_per_launch": flops,
         "algorithmic_bytes_per_launch": bytes_alg,
         "hbm_gbs_at_algorithmic_bytes": round(bytes_alg / (step_ms * 1e-3) / 1e9, 1),
@@ -438,9 +542,9 @@ def run_gpu(args, rank, world, local):
     }
 
     result = {
-        "metric": METRIC,
-        "value": round(tflops, 2),
-        "unit": "TFLOP/s",
+        "metric": metric_of(w)[0],
+        "value": round(tflops, 2) if w.kind != "pe" else round(gbs * world, 1),
+        "unit": metric_of(w)[1],
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
@@ -469,12 +573,12 @@ def run_gpu(args, rank, world, local):
     if w.is_mha:
         result["config"]["d_model"] = w.d_model
 
-    if not args.no_e2e:
+    if not args.no_e2e and w.kind != "pe":
         result["e2e"] = e2e_leg(args, w, host, step, flops, world)
         result["gpu_launches"] += result["e2e"].pop("launches") * launches_per_step
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, threads, desc = sample_rate(w, inp, args.cpu_budget_s)
-        result["cpu_baseline"] = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads,
+        result["cpu_baseline"] = {"value": round(rate, 6), "unit": metric_of(w)[1], "cores": threads,
                                   "kind": "oracle", "sample": desc}
     if world > 1:
         import torch.distributed as dist
@@ -533,8 +637,8 @@ def run_reference(args, rank, world):
     from synth import inputs as synth
     if rank != 0:
         return None
-    w = synth.workload(args.workload)
-    inp = synth.mha_inputs(w) if w.is_mha else synth.attn_inputs(w)
+    w = load_workload(args)
+    inp = workload_inputs(w)
     total_budget_s = 150.0
     per_step = max(0.5, total_budget_s / max(1, args.steps + args.warmup))
     for i in range(args.warmup):
@@ -551,9 +655,9 @@ def run_reference(args, rank, world):
     value = statistics.median(rates)
     return {
         "impl": "reference",
-        "metric": METRIC,
+        "metric": metric_of(w)[0],
         "value": round(value, 6),
-        "unit": "TFLOP/s",
+        "unit": metric_of(w)[1],
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
@@ -565,10 +669,10 @@ def run_reference(args, rank, world):
         "data": "synthetic: seeded Philox N(0,1) inputs rounded to bf16 (no dataset)",
         "config": {"workload": w.name, "description": w.description, "B": w.B, "h": w.h,
                    "n_q": w.n_q, "n_k": w.n_k, "d": w.d_k},
-        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
+        "cpu_baseline": {"value": round(value, 6), "unit": metric_of(w)[1], "cores": threads,
                          "kind": "oracle",
                          "sample": f"each step: {descs[0] if descs else ''} (median over steps)"},
-        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": round(value, 6), "unit": metric_of(w)[1], "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }

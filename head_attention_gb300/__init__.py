@@ -12,6 +12,9 @@ from ._binding import (  # noqa: F401
     MASK_KEY_PADDING,
     MASK_NONE,
     HattnError,
+    attn_decode_fwd,
+    attn_decode_fwd_raw,
+    attn_decode_workspace_bytes,
     attn_fwd,
     attn_fwd_raw,
     check_device_error,
@@ -20,6 +23,8 @@ from ._binding import (  # noqa: F401
     mha_fwd_noalloc_raw,
     mha_fwd_raw,
     mha_workspace_bytes,
+    pos_encoding_fwd,
+    pos_encoding_fwd_raw,
     status_str,
     version,
 )

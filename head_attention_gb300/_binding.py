@@ -20,7 +20,8 @@ OK, EINVAL, EUNSUPPORTED, ECUDA, ETIMEOUT, EKEYLEN, EWORKSPACE, ESCRATCH = 0, -1
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 # Every symbol include/hattn.h declares.
-EXPORTED = ("attn_fwd", "mha_fwd", "mha_fwd_noalloc", "mha_workspace_bytes", "hattn_status_str",
+EXPORTED = ("attn_fwd", "attn_decode_fwd", "attn_decode_workspace_bytes", "mha_fwd",
+            "mha_fwd_noalloc", "mha_workspace_bytes", "pos_encoding_fwd", "hattn_status_str",
             "hattn_check_device_error", "hattn_version")
 
 _lock = threading.Lock()
@@ -54,6 +55,12 @@ def load() -> ctypes.CDLL:
         lib.mha_fwd.restype = i
         lib.mha_fwd_noalloc.argtypes = [vp] * 8 + [f, vp, i, i, i, i, i, i, i, i, i, vp, vp]
         lib.mha_fwd_noalloc.restype = i
+        lib.attn_decode_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, vp, vp, sz, vp]
+        lib.attn_decode_fwd.restype = i
+        lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i]
+        lib.attn_decode_workspace_bytes.restype = sz
+        lib.pos_encoding_fwd.argtypes = [vp, vp, i, i, i, i, f, i, vp]
+        lib.pos_encoding_fwd.restype = i
         lib.mha_workspace_bytes.argtypes = [i] * 8
         lib.mha_workspace_bytes.restype = sz
         lib.hattn_status_str.argtypes = [i]
@@ -165,6 +172,55 @@ def mha_fwd_noalloc_raw(x_q, x_kv, wq, wk, wv, wo, gamma, beta, eps, y, dtype, B
                                   _ptr(gamma), _ptr(beta), float(eps), _ptr(y), int(dtype), int(B),
                                   int(n_q), int(n_k), int(d_model), int(h), int(d_k), int(d_v),
                                   int(mask_kind), _ptr(key_lens), _stream(stream))
+
+
+def attn_decode_workspace_bytes(B, h, n_max, d) -> int:
+    return int(load().attn_decode_workspace_bytes(int(B), int(h), int(n_max), int(d)))
+
+
+def attn_decode_fwd_raw(q, k_cache, v_cache, out, dtype, B, h, n_max, d, scale, kv_lens,
+                        workspace, ws_bytes, stream) -> int:
+    return load().attn_decode_fwd(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), int(dtype),
+                                  int(B), int(h), int(n_max), int(d), float(scale), _ptr(kv_lens),
+                                  _ptr(workspace), int(ws_bytes), _stream(stream))
+
+
+def attn_decode_fwd(q, k_cache, v_cache, kv_lens, out=None, scale=None, workspace=None,
+                    stream=None):
+    """One decoding step: q [B, 1, h, d] against the first kv_lens[b] rows of the
+    caches [B, n_max, h, d] (bf16 CUDA tensors). Returns out [B, 1, h, d]."""
+    import torch
+    B, _, h, d = q.shape
+    n_max = k_cache.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if scale is None:
+        scale = d ** -0.5
+    if workspace is None:
+        workspace = torch.empty(attn_decode_workspace_bytes(B, h, n_max, d), dtype=torch.uint8,
+                                device=q.device)
+    rc = attn_decode_fwd_raw(q, k_cache, v_cache, out, _dtype_code(q), B, h, n_max, d, scale,
+                             kv_lens, workspace, workspace.numel(), stream)
+    if rc != OK:
+        raise HattnError(rc, "attn_decode_fwd")
+    return out
+
+
+def pos_encoding_fwd_raw(emb, out, dtype, B, n, d_model, emb_scale, pos0, stream) -> int:
+    return load().pos_encoding_fwd(_ptr(emb), _ptr(out), int(dtype), int(B), int(n),
+                                   int(d_model), float(emb_scale), int(pos0), _stream(stream))
+
+
+def pos_encoding_fwd(out, emb=None, emb_scale=None, pos0=0, stream=None):
+    """out [B, n, d_model] = emb * emb_scale + sinusoidal encoding (emb may be None).
+    emb_scale defaults to sqrt(d_model)."""
+    B, n, d_model = out.shape
+    if emb_scale is None:
+        emb_scale = d_model ** 0.5
+    rc = pos_encoding_fwd_raw(emb, out, _dtype_code(out), B, n, d_model, emb_scale, pos0, stream)
+    if rc != OK:
+        raise HattnError(rc, "pos_encoding_fwd")
+    return out
 
 
 def check_device_error(stream=None) -> int:

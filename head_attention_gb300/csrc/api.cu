@@ -365,6 +365,47 @@ int mha_fwd_noalloc(const void* x_q, const void* x_kv, const void* Wq, const voi
                    h, d_k, d_v, mask_kind, key_lens, scratch, HATTN_NOALLOC_SCRATCH_BYTES, stream);
 }
 
+size_t attn_decode_workspace_bytes(int B, int h, int n_max, int d)
+{
+    if (B <= 0 || h <= 0 || n_max <= 0 || (d != 64 && d != 128 && d != 256)) return 0;
+    int splits = 0, chunk = 0;
+    decode_split_plan(B, h, n_max, &splits, &chunk);
+    return sizeof(float) * (size_t)B * h * splits * (d + 2);
+}
+
+int attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, void* out, int dtype,
+                    int B, int h, int n_max, int d, float scale, const int32_t* kv_lens,
+                    void* workspace, size_t ws_bytes, hattn_stream_t stream)
+{
+    if (!q || !k_cache || !v_cache || !out || !kv_lens) return HATTN_EINVAL;
+    if (dtype != HATTN_BF16) return dtype == HATTN_F32 ? HATTN_EUNSUPPORTED : HATTN_EINVAL;
+    if (B <= 0 || h <= 0 || n_max <= 0 || d <= 0 || !std::isfinite(scale)) return HATTN_EINVAL;
+    if (B > 65535 || h > 65535) return HATTN_EUNSUPPORTED;
+    if (d != 64 && d != 128 && d != 256) return HATTN_EUNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return HATTN_EINVAL;
+    const size_t need = attn_decode_workspace_bytes(B, h, n_max, d);
+    if (!workspace || !aligned16(workspace) || ws_bytes < need) return HATTN_EWORKSPACE;
+    int* err = device_error_ptr();
+    if (!err) return HATTN_ECUDA;
+    DecodeLaunch a{q, k_cache, v_cache, out, kv_lens, workspace, B, h, n_max, d, 0, 0, scale,
+                   reinterpret_cast<cudaStream_t>(stream), err};
+    decode_split_plan(B, h, n_max, &a.splits, &a.chunk);
+    return from_cuda(launch_attn_decode(a));
+}
+
+int pos_encoding_fwd(const void* emb, void* out, int dtype, int B, int n, int d_model,
+                     float emb_scale, int pos0, hattn_stream_t stream)
+{
+    if (!out || (dtype != HATTN_F32 && dtype != HATTN_BF16)) return HATTN_EINVAL;
+    if (B <= 0 || n <= 0 || d_model <= 0 || (d_model & 1) || pos0 < 0) return HATTN_EINVAL;
+    if ((long long)pos0 + n > (1LL << 24) || !std::isfinite(emb_scale)) return HATTN_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(out) & 7u) || (reinterpret_cast<uintptr_t>(emb) & 7u))
+        return HATTN_EINVAL;
+    return from_cuda(launch_pos_encoding(emb, out, dtype, B, n, d_model, emb_scale, pos0,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
 const char* hattn_status_str(int status)
 {
     switch (status) {

@@ -1,13 +1,15 @@
 // CUDA-core attention kernel: exact fp32 arithmetic (expf, fp32 FMA dot
 // products), used for fp32 inputs and for bf16 shapes the tensor-core kernel
-// does not implement (d_k != d_v, or d not in {64, 128}).
+// does not implement (d_k != d_v, d not in {64, 128}, scale <= 0).
 //
-// Each CTA owns 16 query rows of one (batch, head); each warp owns 4 of them.
-// K/V stream through shared memory 32 keys at a time. For a row, lane j scores
-// key j of the tile, the row max and row sum are warp-shuffle reductions, and
-// the output columns are spread over the lanes (column c on lane c % 32). The
-// softmax is the streaming ("online") form: a running max m and sum l, with the
-// accumulator rescaled by exp(m_old - m_new) whenever m grows, so the score
+// Each CTA owns 8 query rows of one (batch, head); each warp owns 2 of them.
+// K/V stream through shared memory 32 keys at a time, staged with batched
+// 16-byte loads (every load of a tile is in flight before the first store). For
+// a row, lane j scores key j of the tile (four independent partial dot
+// products), the row max and row sum are warp-shuffle reductions, and the
+// output columns are spread over the lanes (column c on lane c % 32). The
+// softmax is the streaming ("online") form: a running max m and sum l, with
+// the accumulator rescaled by exp(m_old - m_new) whenever m grows, so the score
 // matrix is never stored.
 #include <cuda_bf16.h>
 
@@ -19,15 +21,30 @@
 namespace hattn {
 namespace {
 
-constexpr int kRows = 16;     // query rows per CTA
-constexpr int kKeys = 32;     // keys per shared-memory tile (one per lane)
-constexpr int kThreads = 128; // 4 warps
+constexpr int kRows = 8;       // query rows per CTA
+constexpr int kKeys = 32;      // keys per shared-memory tile (one per lane)
+constexpr int kThreads = 128;  // 4 warps
 constexpr int kRowsPerWarp = kRows / (kThreads / 32);
 constexpr int kMaxD = 256;
-constexpr int kColsPerLane = kMaxD / 32;
 
-__device__ __forceinline__ float load_f32(const float* p) { return *p; }
-__device__ __forceinline__ float load_f32(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void widen4(const uint4& v, const float*, float* out)
+{
+    out[0] = __uint_as_float(v.x);
+    out[1] = __uint_as_float(v.y);
+    out[2] = __uint_as_float(v.z);
+    out[3] = __uint_as_float(v.w);
+}
+
+__device__ __forceinline__ void widen4(const uint4& v, const __nv_bfloat16*, float* out)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        out[2 * i] = __uint_as_float(w[i] << 16);
+        out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
 __device__ __forceinline__ void store_f32(float* p, float x) { *p = x; }
 __device__ __forceinline__ void store_f32(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
@@ -43,7 +60,42 @@ __device__ __forceinline__ float warp_sum(float x)
     return x;
 }
 
+// Copies rows [row0, row0 + rows) of a [n, *] slice (row stride src_stride
+// elements, d elements per row) into fp32 shared memory with row stride
+// dst_stride, zero for rows >= n. All 16-byte loads are issued before any store.
 template <typename T>
+__device__ __forceinline__ void stage_rows(float* dst, int dst_stride, const T* src,
+                                           size_t src_stride, int row0, int rows, int n, int d)
+{
+    constexpr int V = 16 / sizeof(T);           // elements per 16-byte load
+    constexpr int kMaxLoads = kKeys * kMaxD / V / kThreads;
+    const int per_row = d / V;
+    const int total = rows * per_row;
+    uint4 buf[kMaxLoads];
+#pragma unroll
+    for (int u = 0; u < kMaxLoads; ++u) {
+        const int idx = threadIdx.x + u * kThreads;
+        buf[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (idx < total) {
+            const int r = row0 + idx / per_row;
+            if (r < n)
+                buf[u] = *reinterpret_cast<const uint4*>(src + (size_t)r * src_stride + (idx % per_row) * V);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kMaxLoads; ++u) {
+        const int idx = threadIdx.x + u * kThreads;
+        if (idx < total) {
+            float w[V];
+            widen4(buf[u], static_cast<const T*>(nullptr), w);
+            float* o = dst + (idx / per_row) * dst_stride + (idx % per_row) * V;
+#pragma unroll
+            for (int e = 0; e < V; ++e) o[e] = w[e];
+        }
+    }
+}
+
+template <typename T, int kCols>  // kCols = output columns per lane (d_v <= 32 * kCols)
 __global__ void __launch_bounds__(kThreads)
     attn_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                      T* __restrict__ out, int n_q, int n_k, int h, int d_k, int d_v, float scale,
@@ -60,11 +112,11 @@ __global__ void __launch_bounds__(kThreads)
     const int b = blockIdx.z;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const bool causal = (mask_kind & HATTN_MASK_CAUSAL) != 0;
-    const size_t q_row_stride = (size_t)h * d_k, o_row_stride = (size_t)h * d_v;
-    const T* q_bh = q + (size_t)b * n_q * q_row_stride + (size_t)head * d_k;
-    const T* k_bh = k + (size_t)b * n_k * q_row_stride + (size_t)head * d_k;
-    const T* v_bh = v + (size_t)b * n_k * o_row_stride + (size_t)head * d_v;
-    T* o_bh = out + (size_t)b * n_q * o_row_stride + (size_t)head * d_v;
+    const size_t qk_row_stride = (size_t)h * d_k, v_row_stride = (size_t)h * d_v;
+    const T* q_bh = q + (size_t)b * n_q * qk_row_stride + (size_t)head * d_k;
+    const T* k_bh = k + (size_t)b * n_k * qk_row_stride + (size_t)head * d_k;
+    const T* v_bh = v + (size_t)b * n_k * v_row_stride + (size_t)head * d_v;
+    T* o_bh = out + (size_t)b * n_q * v_row_stride + (size_t)head * d_v;
 
     int kv_len = n_k;
     if (mask_kind & HATTN_MASK_KEY_PADDING) {
@@ -72,7 +124,7 @@ __global__ void __launch_bounds__(kThreads)
         if (kv_len < 1 || kv_len > n_k) {
             for (int idx = threadIdx.x; idx < kRows * d_v; idx += kThreads) {
                 const int t = row0 + idx / d_v;
-                if (t < n_q) store_f32(o_bh + (size_t)t * o_row_stride + idx % d_v, 0.0f);
+                if (t < n_q) store_f32(o_bh + (size_t)t * v_row_stride + idx % d_v, 0.0f);
             }
             if (threadIdx.x == 0) raise_device_error(err_word, HATTN_EKEYLEN);
             return;
@@ -82,30 +134,21 @@ __global__ void __launch_bounds__(kThreads)
     int key_end = kv_len;
     if (causal) key_end = min(key_end, row0 + kRows);
 
-    for (int idx = threadIdx.x; idx < kRows * d_k; idx += kThreads) {
-        const int r = idx / d_k, c = idx % d_k, t = row0 + r;
-        q_s[r * dkp + c] = (t < n_q) ? load_f32(q_bh + (size_t)t * q_row_stride + c) : 0.0f;
-    }
+    stage_rows<T>(q_s, dkp, q_bh, qk_row_stride, row0, kRows, n_q, d_k);
 
-    float m[kRowsPerWarp], l[kRowsPerWarp], acc[kRowsPerWarp][kColsPerLane];
+    float m[kRowsPerWarp], l[kRowsPerWarp], acc[kRowsPerWarp][kCols];
 #pragma unroll
     for (int rr = 0; rr < kRowsPerWarp; ++rr) {
         m[rr] = -INFINITY;
         l[rr] = 0.0f;
 #pragma unroll
-        for (int i = 0; i < kColsPerLane; ++i) acc[rr][i] = 0.0f;
+        for (int i = 0; i < kCols; ++i) acc[rr][i] = 0.0f;
     }
 
     for (int kt = 0; kt < key_end; kt += kKeys) {
-        __syncthreads();  // the previous tile is no longer read
-        for (int idx = threadIdx.x; idx < kKeys * d_k; idx += kThreads) {
-            const int j = kt + idx / d_k, c = idx % d_k;
-            k_s[(idx / d_k) * dkp + c] = (j < n_k) ? load_f32(k_bh + (size_t)j * q_row_stride + c) : 0.0f;
-        }
-        for (int idx = threadIdx.x; idx < kKeys * d_v; idx += kThreads) {
-            const int j = kt + idx / d_v;
-            v_s[idx] = (j < n_k) ? load_f32(v_bh + (size_t)j * o_row_stride + idx % d_v) : 0.0f;
-        }
+        __syncthreads();  // q_s is staged and the previous tile is no longer read
+        stage_rows<T>(k_s, dkp, k_bh, qk_row_stride, kt, kKeys, n_k, d_k);
+        stage_rows<T>(v_s, d_v, v_bh, v_row_stride, kt, kKeys, n_k, d_v);
         __syncthreads();
 
 #pragma unroll
@@ -113,9 +156,18 @@ __global__ void __launch_bounds__(kThreads)
             const int r = warp * kRowsPerWarp + rr;
             const int t = row0 + r;
             const int j = kt + lane;
-            float s = 0.0f;
-            for (int c = 0; c < d_k; ++c) s = fmaf(q_s[r * dkp + c], k_s[lane * dkp + c], s);
-            s *= scale;
+            const float* qr = q_s + r * dkp;
+            const float* kr = k_s + lane * dkp;
+            float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+            int c = 0;
+            for (; c + 4 <= d_k; c += 4) {
+                s0 = fmaf(qr[c], kr[c], s0);
+                s1 = fmaf(qr[c + 1], kr[c + 1], s1);
+                s2 = fmaf(qr[c + 2], kr[c + 2], s2);
+                s3 = fmaf(qr[c + 3], kr[c + 3], s3);
+            }
+            for (; c < d_k; ++c) s0 = fmaf(qr[c], kr[c], s0);
+            float s = ((s0 + s1) + (s2 + s3)) * scale;
             const bool visible = (j < kv_len) && !(causal && j > t);
             s = visible ? s : -INFINITY;
             const float m_new = fmaxf(m[rr], warp_max(s));
@@ -124,14 +176,14 @@ __global__ void __launch_bounds__(kThreads)
             const float p = visible ? expf(s - m_new) : 0.0f;
             l[rr] = l[rr] * alpha + warp_sum(p);
 #pragma unroll
-            for (int i = 0; i < kColsPerLane; ++i) acc[rr][i] *= alpha;
+            for (int i = 0; i < kCols; ++i) acc[rr][i] *= alpha;
+#pragma unroll 8
             for (int jj = 0; jj < kKeys; ++jj) {
                 const float pj = __shfl_sync(0xffffffffu, p, jj);
-                if (pj == 0.0f) continue;  // warp-uniform: pj is broadcast
 #pragma unroll
-                for (int i = 0; i < kColsPerLane; ++i) {
-                    const int c = lane + 32 * i;
-                    if (c < d_v) acc[rr][i] = fmaf(pj, v_s[jj * d_v + c], acc[rr][i]);
+                for (int i = 0; i < kCols; ++i) {
+                    const int cc = lane + 32 * i;
+                    if (cc < d_v) acc[rr][i] = fmaf(pj, v_s[jj * d_v + cc], acc[rr][i]);
                 }
             }
             m[rr] = m_new;
@@ -144,35 +196,43 @@ __global__ void __launch_bounds__(kThreads)
         if (t >= n_q) continue;
         const float inv = l[rr] > 0.0f ? 1.0f / l[rr] : 0.0f;
 #pragma unroll
-        for (int i = 0; i < kColsPerLane; ++i) {
-            const int c = lane + 32 * i;
-            if (c < d_v) store_f32(o_bh + (size_t)t * o_row_stride + c, acc[rr][i] * inv);
+        for (int i = 0; i < kCols; ++i) {
+            const int cc = lane + 32 * i;
+            if (cc < d_v) store_f32(o_bh + (size_t)t * v_row_stride + cc, acc[rr][i] * inv);
         }
     }
 }
 
-template <typename T>
+template <typename T, int kCols>
 cudaError_t launch_typed(const AttnArgs& a)
 {
     const size_t smem = sizeof(float) * ((size_t)kRows * (a.d_k + 1) + (size_t)kKeys * (a.d_k + 1) +
                                          (size_t)kKeys * a.d_v);
-    cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel<T>,
+    cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel<T, kCols>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((a.n_q + kRows - 1) / kRows, a.h, a.B);
-    attn_simt_kernel<T><<<grid, kThreads, smem, a.stream>>>(
+    attn_simt_kernel<T, kCols><<<grid, kThreads, smem, a.stream>>>(
         static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v),
         static_cast<T*>(a.out), a.n_q, a.n_k, a.h, a.d_k, a.d_v, a.scale, a.mask_kind,
         a.key_lens, a.err_word);
     return cudaGetLastError();
 }
 
+template <typename T>
+cudaError_t launch_cols(const AttnArgs& a)
+{
+    if (a.d_v <= 64) return launch_typed<T, 2>(a);
+    if (a.d_v <= 128) return launch_typed<T, 4>(a);
+    return launch_typed<T, 8>(a);
+}
+
 }  // namespace
 
 cudaError_t launch_attn_simt(const AttnArgs& a)
 {
-    if (a.dtype == HATTN_F32) return launch_typed<float>(a);
-    return launch_typed<__nv_bfloat16>(a);
+    if (a.dtype == HATTN_F32) return launch_cols<float>(a);
+    return launch_cols<__nv_bfloat16>(a);
 }
 
 }  // namespace hattn

@@ -49,6 +49,26 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const vo
 // 128-byte swizzle, zero fill past n within each batch element.
 bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int n, int h, int d, int box_rows);
 
+// Sinusoidal positional encoding added to scaled embeddings (emb may be NULL).
+cudaError_t launch_pos_encoding(const void* emb, void* out, int dtype, int B, int n, int d_model,
+                                float emb_scale, int pos0, cudaStream_t stream);
+
+// Decode attention: one query per (b, h) over a per-sequence K/V prefix.
+struct DecodeLaunch {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* out;
+    const int32_t* kv_lens;
+    void* workspace;  // fp32 partials [B, h, splits, d + 2]
+    int B, h, n_max, d, splits, chunk;
+    float scale;
+    cudaStream_t stream;
+    int* err_word;
+};
+void decode_split_plan(int B, int h, int n_max, int* splits, int* chunk);
+cudaError_t launch_attn_decode(const DecodeLaunch& a);
+
 // ---- tcgen05 GEMMs of the MHA sublayer
 
 // One output problem of the projection GEMM: C[M, N] = A[M, K] . W[K, N] (bf16, row-major).

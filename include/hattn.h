@@ -157,6 +157,55 @@ int mha_fwd_noalloc(const void* x_q, const void* x_kv, const void* Wq, const voi
                     int d_k, int d_v, int mask_kind, const int32_t* key_lens,
                     hattn_stream_t stream);
 
+/*
+ * pos_encoding_fwd — sinusoidal positional encoding added to scaled embeddings,
+ *     out[b,t,2i]   = emb_scale * emb[b,t,2i]   + sin((pos0 + t) / 10000^(2i/d_model))
+ *     out[b,t,2i+1] = emb_scale * emb[b,t,2i+1] + cos((pos0 + t) / 10000^(2i/d_model))
+ *
+ * Defined in [P3] research-heat.pages.dev "做法 · Attention Is All You Need",
+ * §去掉循环，因而须补回顺序 (the sin/cos formulas) and [P1] §没有循环，模型怎样
+ * 知道词序？ (the embedding is multiplied by sqrt(d_model), then the encoding
+ * is added); values tabulated in [P4] §四、位置编码, table 4.1.
+ *
+ *   emb      device [B, n, d_model] (dtype elements), or NULL for the encoding alone
+ *   out      device [B, n, d_model]; may be the same buffer as emb (in place)
+ *   dtype    HATTN_F32 or HATTN_BF16
+ *   d_model  even; emb_scale normally sqrt(d_model); pos0 >= 0 is the position of row 0,
+ *            and pos0 + n <= 2^24 (positions are exact fp32 integers in the kernel)
+ * Pointers 8-byte aligned. The encoding term is within 1e-6 of the exact
+ * sin/cos; the sum is rounded once to dtype. Returns HATTN_OK, HATTN_EINVAL or
+ * HATTN_ECUDA.
+ */
+int pos_encoding_fwd(const void* emb, void* out, int dtype, int B, int n, int d_model,
+                     float emb_scale, int pos0, hattn_stream_t stream);
+
+/*
+ * attn_decode_fwd — one decoding step: a single new query per (batch, head)
+ * attends over that sequence's first kv_lens[b] cached keys and values,
+ *     out[b,0,i,:] = sum_{j < kv_lens[b]} softmax_j(scale * q[b,0,i,:].k[b,j,i,:]) v[b,j,i,:]
+ * (the same attention as attn_fwd with n_q = 1 and key padding).
+ *
+ * Defined by the autoregressive generation of [P1] §训练能并行，不意味着一次生成
+ * 整句话 (each step predicts from the prefix produced so far) and
+ * [research-heat] §解码器不能看见尚未写出的词 (generation proceeds word by word);
+ * the attention itself is [P1] §六步算完一行注意力.
+ *
+ *   q        device [B, 1, h, d] bf16;   out device [B, 1, h, d] bf16
+ *   k_cache, v_cache  device [B, n_max, h, d] bf16 (rows >= kv_lens[b] are not read)
+ *   kv_lens  device int32[B], each in [1, n_max]; a value outside zeroes that
+ *            output and raises HATTN_EKEYLEN in the device error word
+ *   workspace  device scratch of attn_decode_workspace_bytes() bytes (16-byte
+ *            aligned, caller-owned, not shared with a concurrent call)
+ * Supported: dtype HATTN_BF16, d in {64, 128, 256}; pointers 16-byte aligned.
+ * Returns HATTN_OK, HATTN_EINVAL, HATTN_EUNSUPPORTED, HATTN_EWORKSPACE or HATTN_ECUDA.
+ */
+int attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, void* out, int dtype,
+                    int B, int h, int n_max, int d, float scale, const int32_t* kv_lens,
+                    void* workspace, size_t ws_bytes, hattn_stream_t stream);
+
+/* Bytes of workspace attn_decode_fwd needs for these sizes (0 on bad sizes). */
+size_t attn_decode_workspace_bytes(int B, int h, int n_max, int d);
+
 /* Bytes of caller-owned workspace mha_fwd needs for these sizes (0 on bad sizes). */
 size_t mha_workspace_bytes(int dtype, int B, int n_q, int n_k, int d_model, int h, int d_k,
                            int d_v);

@@ -132,8 +132,9 @@ class Workload:
     mask_kind: int
     seed: int
     key_len_range: tuple | None = None  # inclusive (lo, hi) when KEY_PADDING
-    d_model: int = 0  # > 0 for the MHA sublayer
+    d_model: int = 0  # > 0 for the MHA sublayer (and the embedding width for "pe")
     description: str = ""
+    kind: str = "attn"  # "attn", "mha", "decode" (n_q = 1 over a K/V prefix) or "pe"
 
     @property
     def scale(self) -> float:
@@ -142,7 +143,7 @@ class Workload:
 
     @property
     def is_mha(self) -> bool:
-        return self.d_model > 0
+        return self.kind == "mha"
 
     def attn_flops(self) -> float:
         """4*B*h*n_q*n_k*d, halved for causal (the defined metric's FLOP count)."""
@@ -178,12 +179,22 @@ WORKLOADS = {
         description="cross-attention, bf16, B=64 h=8 n_q=128 n_k=256 d=64, key lengths U[64,256]"),
     "mha_bf16": Workload(
         "mha_bf16", "bf16", B=16, h=8, n_q=512, n_k=512, d_k=64, d_v=64,
-        mask_kind=MASK_NONE, seed=3, d_model=512,
+        mask_kind=MASK_NONE, seed=3, d_model=512, kind="mha",
         description="post-norm MHA sublayer, bf16, B=16 n=512 d_model=512 h=8 d=64"),
     "long_causal_d128": Workload(
         "long_causal_d128", "bf16", B=4, h=16, n_q=8192, n_k=8192, d_k=128, d_v=128,
         mask_kind=MASK_CAUSAL, seed=4,
         description="long-sequence causal self-attention, bf16, B=4 h=16 n=8192 d=128"),
+    "decode_bf16": Workload(
+        "decode_bf16", "bf16", B=32, h=32, n_q=1, n_k=8192, d_k=128, d_v=128,
+        mask_kind=MASK_KEY_PADDING, seed=6, key_len_range=(4096, 8192), kind="decode",
+        description="decode step, bf16, B=32 h=32 d=128, one query over a K/V prefix of "
+                    "U[4096,8192] keys (cache capacity 8192)"),
+    "pos_encoding_bf16": Workload(
+        "pos_encoding_bf16", "bf16", B=16, h=1, n_q=8192, n_k=8192, d_k=512, d_v=512,
+        mask_kind=MASK_NONE, seed=7, d_model=512, kind="pe",
+        description="sinusoidal positional encoding added to sqrt(d_model)-scaled embeddings, "
+                    "bf16, B=16 n=8192 d_model=512"),
     "long_causal_d64": Workload(
         "long_causal_d64", "bf16", B=4, h=32, n_q=8192, n_k=8192, d_k=64, d_v=64,
         mask_kind=MASK_CAUSAL, seed=5,

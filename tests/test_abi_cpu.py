@@ -126,3 +126,43 @@ def test_noalloc_rejects_problems_beyond_its_static_scratch(lib):
     assert hattn.mha_fwd_noalloc_raw(**args) == hattn._binding.ESCRATCH
     args.update(B=16, n_q=1024, n_k=1024)
     assert hattn.mha_fwd_noalloc_raw(**args) == hattn._binding.ESCRATCH
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(out=None), hattn._binding.EINVAL),
+    (dict(dtype=5), hattn._binding.EINVAL),
+    (dict(d_model=63), hattn._binding.EINVAL),
+    (dict(n=0), hattn._binding.EINVAL),
+    (dict(pos0=-1), hattn._binding.EINVAL),
+    (dict(pos0=(1 << 24) - 15), hattn._binding.EINVAL),
+    (dict(out=A + 4), hattn._binding.EINVAL),
+    (dict(emb_scale=float("nan")), hattn._binding.EINVAL),
+])
+def test_pos_encoding_rejects_bad_arguments(lib, kw, code):
+    args = dict(emb=None, out=A, dtype=1, B=2, n=16, d_model=64, emb_scale=8.0, pos0=0, stream=0)
+    args.update(kw)
+    assert hattn.pos_encoding_fwd_raw(**args) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), hattn._binding.EINVAL),
+    (dict(kv_lens=None), hattn._binding.EINVAL),
+    (dict(dtype=0), hattn._binding.EUNSUPPORTED),
+    (dict(d=96), hattn._binding.EUNSUPPORTED),
+    (dict(n_max=0), hattn._binding.EINVAL),
+    (dict(k_cache=A + 8), hattn._binding.EINVAL),
+    (dict(workspace=None), hattn._binding.EWORKSPACE),
+    (dict(ws_bytes=16), hattn._binding.EWORKSPACE),
+])
+def test_decode_rejects_bad_arguments(lib, kw, code):
+    args = dict(q=A, k_cache=2 * A, v_cache=3 * A, out=4 * A, dtype=1, B=2, h=4, n_max=512, d=128,
+                scale=0.088, kv_lens=5 * A, workspace=6 * A, ws_bytes=1 << 30, stream=0)
+    args.update(kw)
+    assert hattn.attn_decode_fwd_raw(**args) == code
+
+
+def test_decode_workspace_size():
+    n = hattn.attn_decode_workspace_bytes(32, 32, 8192, 128)
+    assert n > 0 and n % (4 * 130) == 0
+    assert hattn.attn_decode_workspace_bytes(1, 1, 1, 128) == 4 * 130
+    assert hattn.attn_decode_workspace_bytes(1, 1, 1, 100) == 0

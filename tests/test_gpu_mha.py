@@ -54,7 +54,7 @@ def test_named_mha_full_parity():
 def test_mha_shapes(B, n_q, n_k, d_model, h, d, mask_kind, cross):
     w = synth.Workload("mha_sweep", "bf16", B=B, h=h, n_q=n_q, n_k=n_k, d_k=d, d_v=d,
                        mask_kind=mask_kind, seed=500 + n_q + d_model, key_len_range=(1, n_k),
-                       d_model=d_model)
+                       d_model=d_model, kind="mha")
     inp = synth.mha_inputs(w, self_attention=not cross)
     rng = np.random.default_rng(7)
     inp["gamma"] = rng.uniform(0.5, 1.5, d_model).astype(np.float32)

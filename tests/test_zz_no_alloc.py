@@ -28,7 +28,7 @@ def test_noalloc_matches_workspace_entry_point_twice(name_or_shape):
     else:
         B, n_q, n_k, dm, h, d, mask = name_or_shape
         w = synth.Workload("noalloc_cross", "bf16", B=B, h=h, n_q=n_q, n_k=n_k, d_k=d, d_v=d,
-                           mask_kind=mask, seed=77, key_len_range=(1, n_k), d_model=dm)
+                           mask_kind=mask, seed=77, key_len_range=(1, n_k), d_model=dm, kind="mha")
         inp = synth.mha_inputs(w, self_attention=False)
     dev = {n: to_device(inp[n], "bf16") for n in ("x_q", "x_kv", "wq", "wk", "wv", "wo")}
     gamma = t.from_numpy(inp["gamma"]).cuda()
