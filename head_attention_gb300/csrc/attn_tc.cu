@@ -7,10 +7,18 @@
 // Is All You Need" (hex4c59 §把所有位置合并，就是那条核心公式; masks per
 // §掩码必须在 softmax 之前生效).
 //
-// How. One CTA = one (b, i) and 256 consecutive query rows = two 128-row tiles.
-// 12 warps in three warpgroups; a register split gives the softmax warps 200
-// registers and the control warps 88.
-//   warp 8      TMA: the two Q tiles once, then K_j (128 keys) through a
+// How. A persistent kernel: one CTA per SM loops over work units, a unit being
+// one (b, i) and 256 consecutive query rows = two 128-row tiles. Units are
+// ordered in groups of heads whose K/V fit in L2 together, heaviest causal
+// rows first within a group; for causal problems the host assigns units to
+// CTAs by greedy list scheduling on their block counts (a table passed with
+// the launch), otherwise CTAs take them in a snake order. All barrier phases
+// run on across units, so a CTA pays its set-up once, the next unit's Q tile
+// is loaded as soon as the previous unit's last S MMA of that tile retired,
+// and a tile's epilogue overlaps its first S MMA of the next unit.
+// 12 warps in three warpgroups; a register split gives the softmax warps 208
+// registers and the control warps 72.
+//   warp 8      TMA: the unit's Q tiles, then K_j (128 keys) through a
 //               3-stage (D=128) / 5-stage (D=64) shared-memory ring.
 //   warp 10     TMA: V_j through a 2-stage (D=128) / 4-stage (D=64) ring. K
 //               runs one block ahead of V because S(j+1) follows PV(j).
@@ -42,7 +50,14 @@
 // the device error word, drains its own copies and MMAs, frees TMEM and exits.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cmath>
+#include <cstring>
+#include <memory>
+#include <mutex>
+#include <queue>
+#include <utility>
+#include <vector>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -56,8 +71,8 @@ constexpr int kWarpMma0 = 9;   // MMA issuer of tile 0 (also owns the TMEM alloc
 constexpr int kWarpLoadV = 10;
 constexpr int kWarpMma1 = 11;  // MMA issuer of tile 1
 // Launched at 168 registers per thread (384 x 168 = 64512 of the SM's 65536).
-constexpr int kRegsSoftmax = 200;
-constexpr int kRegsControl = 88;
+constexpr int kRegsSoftmax = 208;
+constexpr int kRegsControl = 72;
 static_assert(256 * kRegsSoftmax + 128 * kRegsControl <= kThreads * 168, "register split");
 
 // Named barriers that make the two softmax warpgroups take turns on the
@@ -80,8 +95,9 @@ struct Cfg {
     static constexpr int kOffV = kOffK + kKStages * kTileBytes;
     static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
     // barrier indices
-    static constexpr int kBarQ = 0;
-    static constexpr int kBarKFull = 1;
+    static constexpr int kBarQFull = 0;   // 2: Q_t landed
+    static constexpr int kBarQEmpty = 2;  // 2: the unit's last S MMA of tile t retired
+    static constexpr int kBarKFull = 4;
     static constexpr int kBarKEmpty = kBarKFull + kKStages;
     static constexpr int kBarVFull = kBarKEmpty + kKStages;
     static constexpr int kBarVEmpty = kBarVFull + kVStages;
@@ -102,30 +118,96 @@ struct TcParams {
     int B, h, n_q, n_k;
     int mask_kind;
     float scale_log2;
-    int n_pairs;
+    int n_pairs;      // 256-row query pairs per (b, i)
+    int units;        // B * h * n_pairs
+    int group_heads;  // heads per L2 group in the unit order
+    int issuers;      // 2 when any unit has a second tile (n_q > 128), else 1
     const int32_t* key_lens;
     __nv_bfloat16* out;
     int* err_word;
 };
 
-// Per-CTA state shared by the role functions.
+// Units of every CTA, computed on the host (greedy list scheduling on the
+// units' block counts) and passed by value with the launch: CTA c takes the
+// unit slots list[first[c] .. first[c + 1]) in that (ascending) order.
+constexpr int kTableUnits = 4096;
+constexpr int kTableCtas = 256;
+struct SchedTable {
+    uint16_t first[kTableCtas + 1];
+    uint16_t list[kTableUnits];
+};
+struct SchedSnake {};
+
+// Per-CTA state shared by the role functions; the unit fields are rewritten
+// by unit_setup for every unit.
 struct Cta {
     uint32_t sbase;       // shared-memory base (1024-aligned)
     uint32_t bar0;        // address of barrier 0
     uint32_t tmem;        // TMEM base address
-    volatile int* abort;  // set when any wait gave up
+    uint32_t abort_flag;  // shared address of the word set when any wait gave up
+    bool causal;
     int b, head;
     int row0[2];          // first query row of each tile
     int nblk[2];          // key blocks each tile multiplies (0: tile absent)
     int nblk_max;
     int kv_len;
-    bool causal;
+    bool valid;           // key length within [1, n_k]
     __device__ uint32_t bar(int i) const { return bar0 + 8u * i; }
+    __device__ bool aborted() const { return ld_volatile_shared(abort_flag) != 0u; }
 };
+
+// Walks this CTA's unit slots in increasing order.
+template <bool kTable>
+struct UnitIter {
+    int pos = -1, end = 0;
+    template <class Sched>
+    __device__ __forceinline__ int next(const TcParams& p, const Sched& sch)
+    {
+        if constexpr (kTable) {
+            if (pos < 0) {
+                pos = sch.first[blockIdx.x];
+                end = sch.first[blockIdx.x + 1];
+            }
+            return pos < end ? static_cast<int>(sch.list[pos++]) : -1;
+        } else {
+            if (pos < 0) pos = 0;
+            // Snake: round r takes slots [r * grid, (r + 1) * grid), reversed on odd rounds.
+            const long long r = pos++;
+            const long long slot = r * gridDim.x + ((r & 1) ? gridDim.x - 1 - blockIdx.x : blockIdx.x);
+            return slot < p.units ? static_cast<int>(slot) : -1;
+        }
+    }
+};
+
+// Unit order: groups of group_heads (b, i) heads; within a group, query pairs
+// from the heaviest (causal: the last rows) down, heads inner.
+__device__ __forceinline__ void unit_setup(Cta& c, const TcParams& p, int slot)
+{
+    const int per_group = p.group_heads * p.n_pairs;
+    const int g = slot / per_group;
+    const int w = slot - g * per_group;
+    const int heads_here = min(p.group_heads, p.B * p.h - g * p.group_heads);
+    const int pi = w / heads_here;
+    const int bh = g * p.group_heads + (w - pi * heads_here);
+    const int pair = c.causal ? p.n_pairs - 1 - pi : pi;
+    c.b = bh / p.h;
+    c.head = bh % p.h;
+    c.row0[0] = pair * kRowsPerCta;
+    c.row0[1] = c.row0[0] + 128;
+    c.kv_len = (p.mask_kind & HATTN_MASK_KEY_PADDING) ? p.key_lens[c.b] : p.n_k;
+    c.valid = c.kv_len >= 1 && c.kv_len <= p.n_k;
+    const int kv_blocks = (c.kv_len + 127) / 128;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        if (!c.valid || c.row0[t] >= p.n_q) c.nblk[t] = 0;
+        else c.nblk[t] = c.causal ? min(kv_blocks, c.row0[t] / 128 + 1) : kv_blocks;
+    }
+    c.nblk_max = max(c.nblk[0], c.nblk[1]);
+}
 
 __device__ __forceinline__ void give_up(const Cta& c, int* err_word)
 {
-    *c.abort = 1;
+    st_volatile_shared(c.abort_flag, 1u);
     raise_device_error(err_word, HATTN_ETIMEOUT);
 }
 
@@ -161,113 +243,165 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
 
 // ---------------------------------------------------------------- TMA producers
 
-template <int D>
-__device__ void produce_qk(const Cta& c, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                           int* err_word)
+template <int D, bool kTable, class Sched>
+__device__ void produce_qk(Cta c, const TcParams& p, const Sched& sch, const CUtensorMap* tm_q,
+                           const CUtensorMap* tm_k)
 {
     using C = Cfg<D>;
-    const int n_tiles = c.nblk[1] > 0 ? 2 : 1;
-    mbar_arrive_expect_tx(c.bar(C::kBarQ), n_tiles * C::kTileBytes);
-    for (int t = 0; t < n_tiles; ++t)
-        for (int x = 0; x < C::kBoxes; ++x)
-            tma_load_4d(c.sbase + C::kOffQ + t * C::kTileBytes + x * kBoxBytes, tm_q,
-                        c.bar(C::kBarQ), x * 64, c.head, c.row0[t], c.b);
-    int issued = 0;
-    for (int j = 0; j < c.nblk_max; ++j) {
-        const int s = j % C::kKStages;
-        if (*c.abort || !mbar_wait(c.bar(C::kBarKEmpty + s), ((j / C::kKStages) & 1) ^ 1)) {
-            give_up(c, err_word);
-            break;
+    uint32_t kc = 0;    // K blocks issued so far (ring position)
+    int qn[2] = {0, 0};  // Q tiles issued so far, per tile
+    bool ok = true;
+    UnitIter<kTable> it;
+    for (int slot; ok && (slot = it.next(p, sch)) >= 0;) {
+        if (c.aborted()) break;
+        unit_setup(c, p, slot);
+        for (int t = 0; t < 2 && ok; ++t) {
+            if (c.nblk[t] == 0) continue;
+            // The previous unit's S MMAs of this tile must have finished reading Q_t.
+            if (qn[t] > 0 && !mbar_wait(c.bar(C::kBarQEmpty + t), (qn[t] - 1) & 1)) {
+                ok = false;
+                break;
+            }
+            mbar_arrive_expect_tx(c.bar(C::kBarQFull + t), C::kTileBytes);
+            for (int x = 0; x < C::kBoxes; ++x)
+                tma_load_4d(c.sbase + C::kOffQ + t * C::kTileBytes + x * kBoxBytes, tm_q,
+                            c.bar(C::kBarQFull + t), x * 64, c.head, c.row0[t], c.b);
+            ++qn[t];
         }
-        mbar_arrive_expect_tx(c.bar(C::kBarKFull + s), C::kTileBytes);
-        for (int x = 0; x < C::kBoxes; ++x)
-            tma_load_4d(c.sbase + C::kOffK + s * C::kTileBytes + x * kBoxBytes, tm_k,
-                        c.bar(C::kBarKFull + s), x * 64, c.head, j * 128, c.b);
-        ++issued;
+        for (int j = 0; ok && j < c.nblk_max; ++j) {
+            const uint32_t s = kc % C::kKStages;
+            if (c.aborted() || !mbar_wait(c.bar(C::kBarKEmpty + s), ((kc / C::kKStages) & 1) ^ 1)) {
+                ok = false;
+                break;
+            }
+            mbar_arrive_expect_tx(c.bar(C::kBarKFull + s), C::kTileBytes);
+            for (int x = 0; x < C::kBoxes; ++x)
+                tma_load_4d(c.sbase + C::kOffK + s * C::kTileBytes + x * kBoxBytes, tm_k,
+                            c.bar(C::kBarKFull + s), x * 64, c.head, j * 128, c.b);
+            ++kc;
+        }
     }
+    if (!ok) give_up(c, p.err_word);
     // Every copy this CTA started must land before the CTA may exit.
-    mbar_wait(c.bar(C::kBarQ), 0);
-    for (int j = max(0, issued - C::kKStages); j < issued; ++j)
-        mbar_wait(c.bar(C::kBarKFull + j % C::kKStages), (j / C::kKStages) & 1);
+    for (int t = 0; t < 2; ++t)
+        if (qn[t] > 0) mbar_wait(c.bar(C::kBarQFull + t), (qn[t] - 1) & 1);
+    for (uint32_t i = kc > (uint32_t)C::kKStages ? kc - C::kKStages : 0u; i < kc; ++i)
+        mbar_wait(c.bar(C::kBarKFull + i % C::kKStages), (i / C::kKStages) & 1);
 }
 
-template <int D>
-__device__ void produce_v(const Cta& c, const CUtensorMap* tm_v, int* err_word)
+template <int D, bool kTable, class Sched>
+__device__ void produce_v(Cta c, const TcParams& p, const Sched& sch, const CUtensorMap* tm_v)
 {
     using C = Cfg<D>;
-    int issued = 0;
-    for (int j = 0; j < c.nblk_max; ++j) {
-        const int s = j % C::kVStages;
-        if (*c.abort || !mbar_wait(c.bar(C::kBarVEmpty + s), ((j / C::kVStages) & 1) ^ 1)) {
-            give_up(c, err_word);
-            break;
+    uint32_t vc = 0;
+    bool ok = true;
+    UnitIter<kTable> it;
+    for (int slot; ok && (slot = it.next(p, sch)) >= 0;) {
+        if (c.aborted()) break;
+        unit_setup(c, p, slot);
+        for (int j = 0; ok && j < c.nblk_max; ++j) {
+            const uint32_t s = vc % C::kVStages;
+            if (c.aborted() || !mbar_wait(c.bar(C::kBarVEmpty + s), ((vc / C::kVStages) & 1) ^ 1)) {
+                ok = false;
+                break;
+            }
+            mbar_arrive_expect_tx(c.bar(C::kBarVFull + s), C::kTileBytes);
+            for (int x = 0; x < C::kBoxes; ++x)
+                tma_load_4d(c.sbase + C::kOffV + s * C::kTileBytes + x * kBoxBytes, tm_v,
+                            c.bar(C::kBarVFull + s), x * 64, c.head, j * 128, c.b);
+            ++vc;
         }
-        mbar_arrive_expect_tx(c.bar(C::kBarVFull + s), C::kTileBytes);
-        for (int x = 0; x < C::kBoxes; ++x)
-            tma_load_4d(c.sbase + C::kOffV + s * C::kTileBytes + x * kBoxBytes, tm_v,
-                        c.bar(C::kBarVFull + s), x * 64, c.head, j * 128, c.b);
-        ++issued;
     }
-    for (int j = max(0, issued - C::kVStages); j < issued; ++j)
-        mbar_wait(c.bar(C::kBarVFull + j % C::kVStages), (j / C::kVStages) & 1);
+    if (!ok) give_up(c, p.err_word);
+    for (uint32_t i = vc > (uint32_t)C::kVStages ? vc - C::kVStages : 0u; i < vc; ++i)
+        mbar_wait(c.bar(C::kBarVFull + i % C::kVStages), (i / C::kVStages) & 1);
 }
 
 // ---------------------------------------------------------------- MMA issuers
 
-// Issues every MMA of tile t (one thread). The K/V "empty" barriers expect one
-// arrival per issuer and block: a block this tile does not multiply is
-// released by a plain arrive once its copy has landed (so the arrival belongs
-// to the phase of that block).
-template <int D>
-__device__ void issue_tile_mmas(const Cta& c, int t, int nb, uint32_t sQ, int* err_word)
+// Issues every MMA of tile t (one thread), unit after unit. The K/V "empty"
+// barriers expect one arrival per issuer and block: a block this tile does not
+// multiply is released by a plain arrive once its copy has landed (so the
+// arrival belongs to the phase of that block). After the unit's last S MMA of
+// the tile, a commit onto the tile's Q-empty barrier lets the producer load
+// the next unit's Q tile.
+template <int D, bool kTable, class Sched>
+__device__ void issue_tile_mmas(Cta c, const TcParams& p, const Sched& sch, int t)
 {
     using C = Cfg<D>;
     const uint32_t tS = c.tmem + 256u * t, tO = tS + 128u;
     // K-major Q/K tiles: SBO = 1024 (8-row groups); MN-major V: LBO = one 64-column box.
-    const uint64_t q_desc = sdesc_sw128(sQ, 16, 1024);
+    const uint64_t q_desc = sdesc_sw128(c.sbase + C::kOffQ + t * C::kTileBytes, 16, 1024);
     const uint64_t k_desc0 = sdesc_sw128(c.sbase + C::kOffK, 16, 1024);
     const uint64_t v_desc0 = sdesc_sw128(c.sbase + C::kOffV, kBoxBytes, 1024);
-    auto kdesc = [&](int s) { return k_desc0 + static_cast<uint64_t>((s * C::kTileBytes) >> 4); };
-    auto vdesc = [&](int s) { return v_desc0 + static_cast<uint64_t>((s * C::kTileBytes) >> 4); };
+    auto kdesc = [&](uint32_t s) { return k_desc0 + static_cast<uint64_t>((s * C::kTileBytes) >> 4); };
+    auto vdesc = [&](uint32_t s) { return v_desc0 + static_cast<uint64_t>((s * C::kTileBytes) >> 4); };
 
-    bool ok = mbar_wait(c.bar(C::kBarQ), 0) && mbar_wait(c.bar(C::kBarKFull), 0);
-    if (ok) {
-        tc_fence_after();
-        issue_qk<D>(tS, q_desc, kdesc(0));
-        mma_commit(c.bar(C::kBarS + t));
-        mma_commit(c.bar(C::kBarKEmpty));
-    }
-    for (int j = 0; ok && j < c.nblk_max; ++j) {
-        const int sv = j % C::kVStages, sk1 = (j + 1) % C::kKStages;
-        const uint32_t phv = (j / C::kVStages) & 1, phk1 = ((j + 1) / C::kKStages) & 1;
-        const bool has_next = j + 1 < c.nblk_max;
-        if (!mbar_wait(c.bar(C::kBarVFull + sv), phv)) { ok = false; break; }
-        if (j < nb) {
-            if (*c.abort || !mbar_wait(c.bar(C::kBarP + t), j & 1)) { ok = false; break; }
-            tc_fence_after();
-            issue_pv<D>(tO, tS, vdesc(sv), j > 0);
-            if (j == nb - 1) mma_commit(c.bar(C::kBarO + t));
-            mma_commit(c.bar(C::kBarVEmpty + sv));
-            if (has_next) {
-                if (!mbar_wait(c.bar(C::kBarKFull + sk1), phk1)) { ok = false; break; }
-                if (j + 1 < nb) {
-                    tc_fence_after();
-                    issue_qk<D>(tS, q_desc, kdesc(sk1));
-                    mma_commit(c.bar(C::kBarS + t));
-                    mma_commit(c.bar(C::kBarKEmpty + sk1));
-                } else {
+    uint32_t kc = 0, vc = 0, pc = 0, qn = 0;  // K / V blocks, P handoffs, Q tiles so far
+    bool ok = true;
+    UnitIter<kTable> it;
+    for (int slot; ok && (slot = it.next(p, sch)) >= 0;) {
+        if (c.aborted()) {
+            ok = false;
+            break;
+        }
+        unit_setup(c, p, slot);
+        const int nb = t ? c.nblk[1] : c.nblk[0], R = c.nblk_max;
+        if (R == 0) continue;
+        if (nb > 0) {
+            if (!mbar_wait(c.bar(C::kBarQFull + t), qn & 1)) { ok = false; break; }
+            ++qn;
+        }
+        {
+            const uint32_t s = kc % C::kKStages;
+            if (!mbar_wait(c.bar(C::kBarKFull + s), (kc / C::kKStages) & 1)) { ok = false; break; }
+            if (nb > 0) {
+                tc_fence_after();
+                issue_qk<D>(tS, q_desc, kdesc(s));
+                mma_commit(c.bar(C::kBarS + t));
+                mma_commit(c.bar(C::kBarKEmpty + s));
+                if (nb == 1) mma_commit(c.bar(C::kBarQEmpty + t));
+            } else {
+                mbar_arrive(c.bar(C::kBarKEmpty + s));
+            }
+        }
+        for (int j = 0; ok && j < R; ++j) {
+            const uint32_t vi = vc + j, ki = kc + j + 1;
+            const uint32_t sv = vi % C::kVStages, phv = (vi / C::kVStages) & 1;
+            const uint32_t sk1 = ki % C::kKStages, phk1 = (ki / C::kKStages) & 1;
+            const bool has_next = j + 1 < R;
+            if (!mbar_wait(c.bar(C::kBarVFull + sv), phv)) { ok = false; break; }
+            if (j < nb) {
+                if (c.aborted() || !mbar_wait(c.bar(C::kBarP + t), pc & 1)) { ok = false; break; }
+                ++pc;
+                tc_fence_after();
+                issue_pv<D>(tO, tS, vdesc(sv), j > 0);
+                if (j == nb - 1) mma_commit(c.bar(C::kBarO + t));
+                mma_commit(c.bar(C::kBarVEmpty + sv));
+                if (has_next) {
+                    if (!mbar_wait(c.bar(C::kBarKFull + sk1), phk1)) { ok = false; break; }
+                    if (j + 1 < nb) {
+                        tc_fence_after();
+                        issue_qk<D>(tS, q_desc, kdesc(sk1));
+                        mma_commit(c.bar(C::kBarS + t));
+                        mma_commit(c.bar(C::kBarKEmpty + sk1));
+                        if (j + 1 == nb - 1) mma_commit(c.bar(C::kBarQEmpty + t));
+                    } else {
+                        mbar_arrive(c.bar(C::kBarKEmpty + sk1));
+                    }
+                }
+            } else {
+                mbar_arrive(c.bar(C::kBarVEmpty + sv));
+                if (has_next) {
+                    if (!mbar_wait(c.bar(C::kBarKFull + sk1), phk1)) { ok = false; break; }
                     mbar_arrive(c.bar(C::kBarKEmpty + sk1));
                 }
             }
-        } else {
-            mbar_arrive(c.bar(C::kBarVEmpty + sv));
-            if (has_next) {
-                if (!mbar_wait(c.bar(C::kBarKFull + sk1), phk1)) { ok = false; break; }
-                mbar_arrive(c.bar(C::kBarKEmpty + sk1));
-            }
         }
+        kc += R;
+        vc += R;
     }
-    if (!ok) give_up(c, err_word);
+    if (!ok) give_up(c, p.err_word);
     // All issued MMAs must complete before TMEM is released.
     mma_commit(c.bar(C::kBarDrain + t));
     mbar_wait(c.bar(C::kBarDrain + t), 0);
@@ -331,124 +465,143 @@ __device__ __forceinline__ float row_max(const uint32_t (&sr)[128])
     return max3f(max3f(part[0], part[1], part[2]), part[3], fmaxf(part[4], part[15]));
 }
 
-template <int D>
-__device__ void softmax_tile(const Cta& c, const TcParams& p, int t, int wq, int lane)
+template <int D, bool kTable, class Sched>
+__device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, int wq, int lane)
 {
     using C = Cfg<D>;
     const int r = wq * 32 + lane;
-    const int my_row0 = c.row0[t];
-    const int row = my_row0 + r;
     const uint32_t lane_base = c.tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t cS = 256u * t, cO = 256u * t + 128u;
-    const int nb = c.nblk[t];
     const uint32_t my_turn = t ? kTurn1 : kTurn0, other_turn = t ? kTurn0 : kTurn1;
-    float m_used = -INFINITY, l = 0.0f;
+    uint32_t sc = 0, oc = 0;  // S blocks and O results waited for so far
     bool ok = true;
-    // Turn protocol over nblk_max rounds (every round is taken, with or without
-    // work, so both warpgroups pass the named barriers the same number of times):
-    // tile 0 waits for its turn, works, hands the turn over; tile 1 hands tile 0
-    // the first turn, then waits, works, and hands it back (except after the last).
-    if (kPingPong && t == 1) named_arrive(kTurn0, 256);
-    for (int j = 0; j < c.nblk_max; ++j) {
-        const bool work = ok && j < nb;
-        uint32_t sr[128];  // raw scores q.k of this row for keys kbase .. kbase + 127
-        if (work) {
-            const bool got = mbar_wait(c.bar(C::kBarS + t), j & 1);
+    UnitIter<kTable> it;
+    for (int slot; (slot = it.next(p, sch)) >= 0;) {
+        unit_setup(c, p, slot);
+        // Selects, not indexing by the runtime tile number (keeps Cta in registers).
+        const int my_row0 = t ? c.row0[1] : c.row0[0];
+        const int row = my_row0 + r;
+        if (!c.valid) {
+            // Key length outside [1, n_k]: this unit's rows are zero and the error is raised.
+            __nv_bfloat16* orow = p.out + (((size_t)c.b * p.n_q + row) * p.h + c.head) * D;
+            if (row < p.n_q)
+                for (int k = 0; k < D; k += 8) st_global_v4(orow + k, 0u, 0u, 0u, 0u);
+            if (t == 0 && r == 0) raise_device_error(p.err_word, HATTN_EKEYLEN);
+            continue;
+        }
+        const int nb = t ? c.nblk[1] : c.nblk[0], R = c.nblk_max;
+        float m_used = -INFINITY, l = 0.0f;
+        // Turn protocol over the unit's R rounds (every round is taken, with or
+        // without work, so both warpgroups pass the named barriers the same number
+        // of times): tile 0 waits for its turn, works, hands the turn over; tile 1
+        // hands tile 0 the first turn, then waits, works, and hands it back
+        // (except after the last round).
+        if (kPingPong && t == 1 && R > 0) named_arrive(kTurn0, 256);
+        for (int j = 0; j < R; ++j) {
+            ok = __all_sync(0xffffffffu, ok && !c.aborted());
+            const bool work = ok && j < nb;
+            uint32_t sr[128];  // raw scores q.k of this row for keys kbase .. kbase + 127
+            if (work) {
+                const bool got = mbar_wait(c.bar(C::kBarS + t), sc & 1);
+                ++sc;
+                ok = __all_sync(0xffffffffu, got);
+            }
+            if (work && ok) {
+                tc_fence_after();
+                tmem_ld_x128(lane_base + cS, sr);
+                const int kbase = j * 128;
+                const bool need_mask = (kbase + 128 > c.kv_len) || (c.causal && kbase + 127 > my_row0);
+                if (need_mask) {
+#pragma unroll
+                    for (int i = 0; i < 128; ++i) {
+                        const int kj = kbase + i;
+                        const bool visible = (kj < c.kv_len) && !(c.causal && kj > row);
+                        if (!visible) sr[i] = __float_as_uint(-INFINITY);
+                    }
+                }
+                // The first block sets the running max before its exponentials.
+                if (j == 0) m_used = row_max(sr) * p.scale_log2;
+            }
+            if (kPingPong) named_sync(my_turn, 256);
+            if (work && ok) {
+                // p = 2^(s * scale * log2(e) - m) with the running max m (scale > 0, so
+                // the max of scale * s is scale * max s). After the first block the
+                // block's own max is found alongside the exponentials; a row whose max
+                // grows by more than 2^8 (rare) rescales O and l and redoes the block.
+                const uint64_t c2 = f32x2(p.scale_log2, p.scale_log2);
+                uint64_t acc[4] = {0, 0, 0, 0};
+                const float mx = exp_block<true>(sr, c2, f32x2(-m_used, -m_used), acc, lane_base + cS) *
+                                 p.scale_log2;
+                const bool grow = j > 0 && mx > m_used + kRescaleLog2;
+                if (__any_sync(0xffffffffu, grow)) {
+                    const float m_new = grow ? mx : m_used;
+                    const float alpha = ex2_approx(m_used - m_new);  // 1 where the max is kept
+#pragma unroll
+                    for (int q = 0; q < D / 16; ++q) {
+                        uint32_t o[16];
+                        tmem_ld_x16(lane_base + cO + 16 * q, o);  // PV up to block j-1 is complete
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st_x16(lane_base + cO + 16 * q, o);
+                    }
+                    l *= alpha;
+                    m_used = m_new;
+                    acc[0] = acc[1] = acc[2] = acc[3] = 0;
+                    exp_block<false>(sr, c2, f32x2(-m_used, -m_used), acc, lane_base + cS);
+                }
+                if (kPingPong && (t == 0 || j + 1 < R)) named_arrive(other_turn, 256);
+                float a0, a1;
+                f32x2_split(add_f32x2(add_f32x2(acc[0], acc[1]), add_f32x2(acc[2], acc[3])), a0, a1);
+                l += a0 + a1;
+                // Each thread's TMEM stores are complete and fenced before the warp
+                // synchronises; one arrival per warp (128 single-thread arrivals on one
+                // barrier word would serialise).
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(c.bar(C::kBarP + t));
+            } else if (kPingPong && (t == 0 || j + 1 < R)) {
+                named_arrive(other_turn, 256);
+            }
+        }
+        if (nb == 0 || !ok) continue;
+        {
+            const bool got = mbar_wait(c.bar(C::kBarO + t), oc & 1);
+            ++oc;
             ok = __all_sync(0xffffffffu, got);
         }
-        if (work && ok) {
-            tc_fence_after();
-            tmem_ld_x128(lane_base + cS, sr);
-            const int kbase = j * 128;
-            const bool need_mask = (kbase + 128 > c.kv_len) || (c.causal && kbase + 127 > my_row0);
-            if (need_mask) {
+        if (!ok) continue;
+        tc_fence_after();
+        // O is in registers after the loads below; the next unit's first PV of this
+        // tile (which overwrites O) waits for this warpgroup's next P handoff.
+        const float inv = 1.0f / l;
+        __nv_bfloat16* orow = p.out + (((size_t)c.b * p.n_q + row) * p.h + c.head) * D;
 #pragma unroll
-                for (int i = 0; i < 128; ++i) {
-                    const int kj = kbase + i;
-                    const bool visible = (kj < c.kv_len) && !(c.causal && kj > row);
-                    if (!visible) sr[i] = __float_as_uint(-INFINITY);
-                }
+        for (int q = 0; q < D / 32; ++q) {
+            uint32_t o[32];
+            tmem_ld_x32(lane_base + cO + 32 * q, o);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+            if (row < p.n_q) {
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4)
+                    st_global_v4(orow + 32 * q + 8 * v4, pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
+                                 pk[4 * v4 + 3]);
             }
-            // The first block sets the running max before its exponentials.
-            if (j == 0) m_used = row_max(sr) * p.scale_log2;
-        }
-        if (kPingPong) named_sync(my_turn, 256);
-        if (work && ok) {
-            // p = 2^(s * scale * log2(e) - m) with the running max m (scale > 0, so
-            // the max of scale * s is scale * max s). After the first block the
-            // block's own max is found alongside the exponentials; a row whose max
-            // grows by more than 2^8 (rare) rescales O and l and redoes the block.
-            const uint64_t c2 = f32x2(p.scale_log2, p.scale_log2);
-            uint64_t acc[4] = {0, 0, 0, 0};
-            const float mx = exp_block<true>(sr, c2, f32x2(-m_used, -m_used), acc, lane_base + cS) *
-                             p.scale_log2;
-            const bool grow = j > 0 && mx > m_used + kRescaleLog2;
-            if (__any_sync(0xffffffffu, grow)) {
-                const float m_new = grow ? mx : m_used;
-                const float alpha = ex2_approx(m_used - m_new);  // 1 where the max is kept
-#pragma unroll
-                for (int q = 0; q < D / 16; ++q) {
-                    uint32_t o[16];
-                    tmem_ld_x16(lane_base + cO + 16 * q, o);  // PV up to block j-1 is complete
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st_x16(lane_base + cO + 16 * q, o);
-                }
-                l *= alpha;
-                m_used = m_new;
-                acc[0] = acc[1] = acc[2] = acc[3] = 0;
-                exp_block<false>(sr, c2, f32x2(-m_used, -m_used), acc, lane_base + cS);
-            }
-            if (kPingPong && (t == 0 || j + 1 < c.nblk_max)) named_arrive(other_turn, 256);
-            float a0, a1;
-            f32x2_split(add_f32x2(add_f32x2(acc[0], acc[1]), add_f32x2(acc[2], acc[3])), a0, a1);
-            l += a0 + a1;
-            // Each thread's TMEM stores are complete and fenced before the warp
-            // synchronises; one arrival per warp (128 single-thread arrivals on one
-            // barrier word would serialise).
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(c.bar(C::kBarP + t));
-        } else if (kPingPong && (t == 0 || j + 1 < c.nblk_max)) {
-            named_arrive(other_turn, 256);
         }
     }
-    if (nb > 0 && ok) {
-        const bool got = mbar_wait(c.bar(C::kBarO + t), 0);
-        ok = __all_sync(0xffffffffu, got);
-    }
-    if (!ok) {
-        give_up(c, p.err_word);
-        return;
-    }
-    if (nb == 0) return;
-    tc_fence_after();
-    const float inv = 1.0f / l;
-    __nv_bfloat16* orow = p.out + (((size_t)c.b * p.n_q + row) * p.h + c.head) * D;
-#pragma unroll
-    for (int q = 0; q < D / 32; ++q) {
-        uint32_t o[32];
-        tmem_ld_x32(lane_base + cO + 32 * q, o);
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-        if (row < p.n_q) {
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-                st_global_v4(orow + 32 * q + 8 * v4, pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
-                             pk[4 * v4 + 3]);
-        }
-    }
+    if (!ok) give_up(c, p.err_word);
 }
 
 // ---------------------------------------------------------------- kernel
 
-template <int D>
+template <int D, bool kTable, class Sched>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const TcParams p)
+                   const __grid_constant__ CUtensorMap tm_v, const TcParams p,
+                   const __grid_constant__ Sched sch)
 {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -460,49 +613,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     Cta c;
     c.sbase = smem_u32(smem);
     c.bar0 = c.sbase + C::kOffBar;
-    c.abort = reinterpret_cast<volatile int*>(smem + C::kOffSlot + 4);
+    c.abort_flag = c.sbase + C::kOffSlot + 4;
     c.causal = (p.mask_kind & HATTN_MASK_CAUSAL) != 0;
-    // Work unit: (batch, head)-major so that the CTAs resident at one time share
-    // K/V in L2; within a head, the heaviest causal rows first.
-    const int bh = blockIdx.x / p.n_pairs;
-    int pair = blockIdx.x % p.n_pairs;
-    if (c.causal) pair = p.n_pairs - 1 - pair;
-    c.b = bh / p.h;
-    c.head = bh % p.h;
-    c.row0[0] = pair * kRowsPerCta;
-    c.row0[1] = c.row0[0] + 128;
-
-    c.kv_len = p.n_k;
-    if (p.mask_kind & HATTN_MASK_KEY_PADDING) c.kv_len = p.key_lens[c.b];
-    if (c.kv_len < 1 || c.kv_len > p.n_k) {
-        if (threadIdx.x < 256) {
-            const int row = c.row0[threadIdx.x / 128] + threadIdx.x % 128;
-            if (row < p.n_q) {
-                __nv_bfloat16* orow = p.out + (((size_t)c.b * p.n_q + row) * p.h + c.head) * D;
-                for (int k = 0; k < D; k += 8) st_global_v4(orow + k, 0u, 0u, 0u, 0u);
-            }
-        }
-        if (threadIdx.x == 0) raise_device_error(p.err_word, HATTN_EKEYLEN);
-        return;
-    }
-    const int kv_blocks = (c.kv_len + 127) / 128;
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        if (c.row0[t] >= p.n_q) c.nblk[t] = 0;
-        else c.nblk[t] = c.causal ? min(kv_blocks, c.row0[t] / 128 + 1) : kv_blocks;
-    }
-    c.nblk_max = max(c.nblk[0], c.nblk[1]);
 
     if (threadIdx.x == 0) {
-        mbar_init(c.bar(C::kBarQ), 1);
-        const int issuers = c.nblk[1] > 0 ? 2 : 1;
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(c.bar(C::kBarQFull + t), 1);
+            mbar_init(c.bar(C::kBarQEmpty + t), 1);
+        }
         for (int s = 0; s < C::kKStages; ++s) {
             mbar_init(c.bar(C::kBarKFull + s), 1);
-            mbar_init(c.bar(C::kBarKEmpty + s), issuers);
+            mbar_init(c.bar(C::kBarKEmpty + s), p.issuers);
         }
         for (int s = 0; s < C::kVStages; ++s) {
             mbar_init(c.bar(C::kBarVFull + s), 1);
-            mbar_init(c.bar(C::kBarVEmpty + s), issuers);
+            mbar_init(c.bar(C::kBarVEmpty + s), p.issuers);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(c.bar(C::kBarS + t), 1);
@@ -511,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(c.bar(C::kBarDrain), 1);
         mbar_init(c.bar(C::kBarDrain + 1), 1);
-        *c.abort = 0;
+        st_volatile_shared(c.abort_flag, 0u);
         fence_barrier_init();
     }
     if (warp == kWarpMma0) {
@@ -531,17 +656,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp >= 8) {
         regs_dec<kRegsControl>();
         if (lane == 0) {
-            if (warp == kWarpLoadK) produce_qk<D>(c, &tm_q, &tm_k, p.err_word);
-            else if (warp == kWarpLoadV) produce_v<D>(c, &tm_v, p.err_word);
-            else if (warp == kWarpMma0)
-                issue_tile_mmas<D>(c, 0, c.nblk[0], c.sbase + C::kOffQ, p.err_word);
-            else if (warp == kWarpMma1 && c.nblk[1] > 0)
-                issue_tile_mmas<D>(c, 1, c.nblk[1], c.sbase + C::kOffQ + C::kTileBytes, p.err_word);
+            if (warp == kWarpLoadK) produce_qk<D, kTable>(c, p, sch, &tm_q, &tm_k);
+            else if (warp == kWarpLoadV) produce_v<D, kTable>(c, p, sch, &tm_v);
+            else if (warp == kWarpMma0) issue_tile_mmas<D, kTable>(c, p, sch, 0);
+            else if (warp == kWarpMma1 && p.issuers == 2) issue_tile_mmas<D, kTable>(c, p, sch, 1);
         }
         __syncwarp();
     } else {
         regs_inc<kRegsSoftmax>();
-        softmax_tile<D>(c, p, warp / 4, warp % 4, lane);
+        softmax_tile<D, kTable>(c, p, sch, warp / 4, warp % 4, lane);
     }
 
     tc_fence_before();
@@ -552,14 +675,88 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D>
-cudaError_t launch_d(const AttnArgs& a, const AttnMaps& m)
+int sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 152;
+    return n;
+}
+
+// Greedy list scheduling of the unit slots (in their order) onto `grid` CTAs,
+// each unit costing its key-block count per tile plus a fixed per-unit
+// overhead; the owner table is cached per shape.
+std::shared_ptr<const SchedTable> greedy_table(const TcParams& p, int grid)
+{
+    struct Key {
+        int B, h, n_q, n_k, mask, grid, group;
+        bool operator==(const Key& o) const
+        {
+            return B == o.B && h == o.h && n_q == o.n_q && n_k == o.n_k && mask == o.mask &&
+                   grid == o.grid && group == o.group;
+        }
+    };
+    static std::mutex mu;
+    static std::vector<std::pair<Key, std::shared_ptr<const SchedTable>>> cache;
+    const Key key{p.B, p.h, p.n_q, p.n_k, p.mask_kind, grid, p.group_heads};
+    std::lock_guard<std::mutex> lock(mu);
+    for (auto& e : cache)
+        if (e.first == key) return e.second;
+    std::vector<int> owner(p.units);
+    using Load = std::pair<long long, int>;  // (accumulated cost, cta)
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (int i = 0; i < grid; ++i) heap.push({0, i});
+    const int kv_blocks = (p.n_k + 127) / 128;
+    const bool causal = (p.mask_kind & HATTN_MASK_CAUSAL) != 0;
+    const int per_group = p.group_heads * p.n_pairs;
+    const int BH = p.B * p.h;
+    constexpr long long kUnitOverhead = 2;  // in key blocks
+    for (int slot = 0; slot < p.units; ++slot) {
+        const int g = slot / per_group;
+        const int w = slot - g * per_group;
+        const int heads_here = std::min(p.group_heads, BH - g * p.group_heads);
+        const int pi = w / heads_here;
+        const int pair = causal ? p.n_pairs - 1 - pi : pi;
+        long long cost = kUnitOverhead;
+        for (int t = 0; t < 2; ++t) {
+            const int row0 = pair * kRowsPerCta + 128 * t;
+            if (row0 < p.n_q) cost += causal ? std::min(kv_blocks, row0 / 128 + 1) : kv_blocks;
+        }
+        Load top = heap.top();
+        heap.pop();
+        owner[slot] = top.second;
+        heap.push({top.first + cost, top.second});
+    }
+    auto tab = std::make_shared<SchedTable>();
+    std::memset(tab.get(), 0, sizeof(SchedTable));
+    std::vector<int> count(grid + 1, 0);
+    for (int slot = 0; slot < p.units; ++slot) ++count[owner[slot] + 1];
+    for (int i = 0; i < grid; ++i) count[i + 1] += count[i];
+    for (int i = 0; i <= kTableCtas; ++i) tab->first[i] = static_cast<uint16_t>(count[std::min(i, grid)]);
+    std::vector<int> fill(count.begin(), count.end() - 1);
+    for (int slot = 0; slot < p.units; ++slot) tab->list[fill[owner[slot]]++] = static_cast<uint16_t>(slot);
+    if (cache.size() >= 64) cache.clear();
+    cache.emplace_back(key, tab);
+    return tab;
+}
+
+template <int D, bool kTable, class Sched>
+cudaError_t launch_kernel(const AttnArgs& a, const AttnMaps& m, const TcParams& p, int grid,
+                          const Sched& sch)
 {
     using C = Cfg<D>;
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, kTable, Sched>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
+    attn_tc_kernel<D, kTable, Sched><<<grid, kThreads, C::kSmemBytes, a.stream>>>(m.q, m.k, m.v, p, sch);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const AttnArgs& a, const AttnMaps& m)
+{
     TcParams p;
     p.B = a.B;
     p.h = a.h;
@@ -571,10 +768,22 @@ cudaError_t launch_d(const AttnArgs& a, const AttnMaps& m)
     p.key_lens = a.key_lens;
     p.out = static_cast<__nv_bfloat16*>(a.out);
     p.err_word = a.err_word;
+    p.issuers = a.n_q > 128 ? 2 : 1;
     const long long units = (long long)p.n_pairs * a.B * a.h;
     if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    attn_tc_kernel<D><<<dim3((unsigned)units), kThreads, C::kSmemBytes, a.stream>>>(m.q, m.k, m.v, p);
-    return cudaGetLastError();
+    p.units = static_cast<int>(units);
+    // Heads per group: their K and V together take at most ~64 MB of the 129 MB L2.
+    const long long kv_head_bytes = 4LL * a.n_k * D;
+    long long g = (64LL << 20) / kv_head_bytes;
+    g = std::max(1LL, std::min(g, (long long)a.B * a.h));
+    p.group_heads = static_cast<int>(g);
+    const int grid = static_cast<int>(std::min<long long>(units, std::min(sm_count(), kTableCtas)));
+    const bool causal = (a.mask_kind & HATTN_MASK_CAUSAL) != 0;
+    if (causal && units > grid && units <= kTableUnits) {
+        const std::shared_ptr<const SchedTable> tab = greedy_table(p, grid);
+        return launch_kernel<D, true>(a, m, p, grid, *tab);
+    }
+    return launch_kernel<D, false>(a, m, p, grid, SchedSnake{});
 }
 
 }  // namespace

@@ -16,6 +16,18 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Volatile 32-bit shared-memory word access through a 32-bit shared address.
+__device__ __forceinline__ uint32_t ld_volatile_shared(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_volatile_shared(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // Every pipeline wait gives up after this many SM clock cycles (about two
 // seconds at GB300 clocks; real waits last microseconds). The SM-local cycle
 // counter is read rather than %globaltimer because it costs a few cycles, and
