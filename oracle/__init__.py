@@ -1,7 +1,8 @@
 """ORACLE — test infrastructure, not product code.
 
 ctypes wrapper around ``attn_oracle.c``, the plain fp64 CPU restatement of
-multi-head scaled dot-product attention and of the post-norm MHA sublayer.
+multi-head scaled dot-product attention, of the post-norm MHA and feed-forward
+sublayers and of the sinusoidal positional encoding.
 Only the tests, the smoke check and the benchmark's CPU-baseline leg may use
 it; the CUDA path never imports it and shares no code with it.
 
@@ -78,6 +79,8 @@ def _load():
         lib.oracle_mha_rows.restype = c_int
         lib.oracle_pos_encoding.argtypes = [dp, dp, c_int, c_int, c_int, c_double, c_int]
         lib.oracle_pos_encoding.restype = c_int
+        lib.oracle_ffn.argtypes = [dp] * 7 + [c_double, dp, c_int, c_int, c_int, c_int]
+        lib.oracle_ffn.restype = c_int
         _lib = lib
         return lib
 
@@ -245,3 +248,21 @@ def pos_encoding(B, n, d_model, emb=None, emb_scale=1.0, pos0=0) -> np.ndarray:
                                  int(d_model), float(emb_scale), int(pos0))
     _check(rc, "oracle_pos_encoding")
     return out
+
+
+def ffn(x, w1, b1, w2, b2, gamma, beta, eps, nthreads=0) -> np.ndarray:
+    """Post-norm feed-forward sublayer y = LayerNorm(x + max(0, x W1 + b1) W2 + b2) on the
+    rows of x [..., d_model] (W1 [d_model, d_ff], W2 [d_ff, d_model])."""
+    lib = _load()
+    x = _f64(x)
+    shape = x.shape
+    d_model = shape[-1]
+    x2 = x.reshape(-1, d_model)
+    w1, b1, w2, b2 = _f64(w1), _f64(b1), _f64(w2), _f64(b2)
+    gamma, beta = _f64(gamma), _f64(beta)
+    d_ff = w1.shape[1]
+    y = np.empty_like(x2)
+    rc = lib.oracle_ffn(_dp(x2), _dp(w1), _dp(b1), _dp(w2), _dp(b2), _dp(gamma), _dp(beta),
+                        float(eps), _dp(y), x2.shape[0], d_model, d_ff, int(nthreads))
+    _check(rc, "oracle_ffn")
+    return y.reshape(shape)

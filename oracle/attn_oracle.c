@@ -398,3 +398,57 @@ int oracle_pos_encoding(const double* emb, double* out, int B, int n, int d_mode
             }
     return ORACLE_OK;
 }
+
+/*
+ * The post-norm position-wise feed-forward sublayer, row by row:
+ *   h = max(0, x W1 + b1)          (d_model -> d_ff, ReLU)
+ *   f = h W2 + b2                  (d_ff -> d_model)
+ *   y = LayerNorm(x + f)
+ * [devpress "【深度学习】Transformer（Attention Is All You Need）", §2.3]:
+ * x + FFN(x) = x + max(0, x W1 + b1) W2 + b2, followed by norm2(x + FFN(x));
+ * [hex4c59, §前馈网络为什么放在注意力后面？]: the same FFN is applied to every
+ * position independently (a row never reads another row), ReLU zeroes
+ * negatives, the base model widens 512 -> 2048 -> 512.
+ * W1 is [d_model, d_ff], W2 [d_ff, d_model], row-major; x and y are
+ * [rows, d_model]. Rows are independent, so any subset of rows may be passed.
+ */
+int oracle_ffn(const double* x, const double* W1, const double* b1, const double* W2,
+               const double* b2, const double* gamma, const double* beta, double eps, double* y,
+               int rows, int d_model, int d_ff, int nthreads)
+{
+    if (rows <= 0 || d_model <= 0 || d_ff <= 0) return ORACLE_EINVAL;
+    int rc = ORACLE_OK;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+#pragma omp parallel
+    {
+        double* hid = (double*)malloc(sizeof(double) * (size_t)d_ff);
+        double* z = (double*)malloc(sizeof(double) * (size_t)d_model);
+        if (!hid || !z) {
+#pragma omp atomic write
+            rc = ORACLE_ENOMEM;
+        } else {
+#pragma omp for schedule(static)
+            for (int r = 0; r < rows; ++r) {
+                const double* xr = x + (size_t)r * d_model;
+                for (int j = 0; j < d_ff; ++j) {
+                    double acc = b1[j];
+                    for (int c = 0; c < d_model; ++c) acc += xr[c] * W1[(size_t)c * d_ff + j];
+                    hid[j] = acc > 0.0 ? acc : 0.0;
+                }
+                for (int c = 0; c < d_model; ++c) {
+                    double acc = b2[c];
+                    for (int j = 0; j < d_ff; ++j) acc += hid[j] * W2[(size_t)j * d_model + c];
+                    z[c] = xr[c] + acc;
+                }
+                oracle_layernorm_row(z, gamma, beta, eps, d_model, y + (size_t)r * d_model);
+            }
+        }
+        free(hid);
+        free(z);
+    }
+    return rc;
+}

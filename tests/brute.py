@@ -40,3 +40,14 @@ def attention(q, k, v, scale, causal=False, key_lens=None):
             rows.append(heads)
         out.append(rows)
     return out
+
+
+def feed_forward_row(x, w1, b1, w2, b2, gamma, beta, eps):
+    """One row of LayerNorm(x + max(0, x W1 + b1) W2 + b2): x list[d_model],
+    w1 list of d_model lists of d_ff, w2 list of d_ff lists of d_model."""
+    d_model, d_ff = len(x), len(b1)
+    hid = [max(0.0, b1[j] + math.fsum(x[c] * w1[c][j] for c in range(d_model))) for j in range(d_ff)]
+    z = [x[c] + b2[c] + math.fsum(hid[j] * w2[j][c] for j in range(d_ff)) for c in range(d_model)]
+    mean = math.fsum(z) / d_model
+    var = math.fsum((v - mean) ** 2 for v in z) / d_model
+    return [gamma[c] * (z[c] - mean) / math.sqrt(var + eps) + beta[c] for c in range(d_model)]

@@ -395,3 +395,84 @@ def test_pos_encoding_embedding_scale_and_offset():
     np.testing.assert_allclose(full, emb * math.sqrt(8) + pe[3:9][None], atol=1e-14)
     # Position 0: sin(0) = 0 on even dimensions, cos(0) = 1 on odd ones.
     np.testing.assert_array_equal(oracle.pos_encoding(1, 1, 8)[0, 0], [0, 1] * 4)
+
+
+# ---------------------------------------------------------------- feed-forward sublayer
+
+def _ffn_case(rng, rows, dm, dff):
+    return dict(x=_rand(rng, rows, dm), w1=_rand(rng, dm, dff) / 2, b1=_rand(rng, dff) / 2,
+                w2=_rand(rng, dff, dm) / 2, b2=_rand(rng, dm), gamma=rng.uniform(0.5, 1.5, dm),
+                beta=rng.uniform(-0.5, 0.5, dm))
+
+
+def test_ffn_brute_force_tiny():
+    """Non-square W1 (d_ff != d_model) and non-trivial biases / gamma / beta: a
+    transposed operand, a dropped bias or a misplaced ReLU fails this."""
+    rng = np.random.default_rng(21)
+    c = _ffn_case(rng, 4, 5, 7)
+    y = oracle.ffn(c["x"], c["w1"], c["b1"], c["w2"], c["b2"], c["gamma"], c["beta"], 1e-6)
+    for r in range(4):
+        ref = brute.feed_forward_row(list(c["x"][r]), c["w1"].tolist(), list(c["b1"]),
+                                     c["w2"].tolist(), list(c["b2"]), list(c["gamma"]),
+                                     list(c["beta"]), 1e-6)
+        np.testing.assert_allclose(y[r], ref, rtol=0, atol=1e-12)
+    # Some pre-activations are negative here, so the ReLU is exercised.
+    pre = c["x"] @ c["w1"] + c["b1"]
+    assert (pre < 0).any() and (pre > 0).any()
+
+
+def test_ffn_against_torch_fp64():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(22)
+    c = _ffn_case(rng, 2 * 6, 16, 40)
+    y = oracle.ffn(c["x"].reshape(2, 6, 16), c["w1"], c["b1"], c["w2"], c["b2"], c["gamma"],
+                   c["beta"], 1e-6)
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    F = torch.nn.functional
+    hid = F.relu(T(c["x"]) @ T(c["w1"]) + T(c["b1"]))
+    ref = F.layer_norm(T(c["x"]) + hid @ T(c["w2"]) + T(c["b2"]), (16,), T(c["gamma"]),
+                       T(c["beta"]), 1e-6).numpy()
+    np.testing.assert_allclose(y.reshape(12, 16), ref, rtol=0, atol=1e-12)
+
+
+def test_ffn_closed_forms():
+    rng = np.random.default_rng(23)
+    dm = 6
+    x = _rand(rng, 5, dm)
+    g, b0 = np.ones(dm), np.zeros(dm)
+    # A very negative b1 switches every hidden unit off: y = LN(x + b2).
+    b2 = _rand(rng, dm)
+    y = oracle.ffn(x, _rand(rng, dm, 9), np.full(9, -1e6), _rand(rng, 9, dm), b2, g, b0, 1e-6)
+    np.testing.assert_allclose(y, oracle.layernorm(x + b2, g, b0, 1e-6), atol=1e-13)
+    # W1 = W2 = I, no biases: y = LN(x + max(0, x)).
+    eye = np.eye(dm)
+    y = oracle.ffn(x, eye, np.zeros(dm), eye, np.zeros(dm), g, b0, 1e-6)
+    np.testing.assert_allclose(y, oracle.layernorm(x + np.maximum(x, 0.0), g, b0, 1e-6), atol=1e-13)
+
+
+def test_ffn_is_position_wise():
+    """[hex4c59] §前馈网络为什么放在注意力后面？: a row never reads another row."""
+    rng = np.random.default_rng(24)
+    c = _ffn_case(rng, 6, 8, 12)
+    args = (c["w1"], c["b1"], c["w2"], c["b2"], c["gamma"], c["beta"], 1e-6)
+    y = oracle.ffn(c["x"], *args)
+    x2 = c["x"].copy()
+    x2[[0, 5]] = _rand(rng, 2, 8) * 10
+    y2 = oracle.ffn(x2, *args)
+    np.testing.assert_array_equal(y[1:5], y2[1:5])
+    perm = rng.permutation(6)
+    np.testing.assert_array_equal(oracle.ffn(c["x"][perm], *args), y[perm])
+
+
+def test_encoder_layer_reduction():
+    """With W^O = 0 and W2 = 0, b2 = 0, both sublayers reduce to LayerNorm, so the
+    layer gives LN(LN(x)) = LN(x) up to the epsilon (gamma = 1, beta = 0)."""
+    rng = np.random.default_rng(25)
+    B, n, dm, h = 2, 5, 8, 2
+    x = _rand(rng, B, n, dm)
+    g, b0 = np.ones(dm), np.zeros(dm)
+    ws = [_rand(rng, dm, dm) for _ in range(3)]
+    y1 = oracle.mha(x, x, *ws, np.zeros((dm, dm)), g, b0, 1e-6, h)
+    y = oracle.ffn(y1, _rand(rng, dm, 16), _rand(rng, 16), np.zeros((16, dm)), np.zeros(dm), g, b0,
+                   1e-6)
+    np.testing.assert_allclose(y, oracle.layernorm(x, g, b0, 1e-6), atol=1e-5)
