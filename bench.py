@@ -322,6 +322,46 @@ def oracle_pe_sample_rate(w, inp, budget_s: float, sample_index: int = 0):
     return nbytes / elapsed / 1e9, 1, desc
 
 
+def oracle_layer_sample_rate(w, inp, budget_s: float, sample_index: int = 0):
+    """Times the oracle's encoder / decoder layer (its sublayers composed, each
+    output rounded to bf16 as the API passes it on) on whole batch elements until
+    about budget_s seconds of work; returns (TFLOP/s of the layer's defined FLOPs,
+    threads, description)."""
+    import oracle
+    from synth import inputs as synth
+    threads = os.cpu_count() or 1
+    wd = lambda a: synth.widen(a, "bf16")
+    rb = lambda a: synth.bf16_bits_to_f64(synth.round_to_bf16_bits(a))
+
+    def mha(xq, xkv, m, mask, kl):
+        return oracle.mha(xq, xkv, wd(m["wq"]), wd(m["wk"]), wd(m["wv"]), wd(m["wo"]),
+                          m["gamma"].astype("float64"), m["beta"].astype("float64"), inp["eps"],
+                          w.h, mask, kl, nthreads=threads)
+
+    f = inp["ffn"]
+    fw = (wd(f["w1"]), f["b1"].astype("float64"), wd(f["w2"]), f["b2"].astype("float64"),
+          f["gamma"], f["beta"], f["eps"])
+    per_elem = w.layer_flops() / w.B
+    done, elapsed = 0, 0.0
+    while elapsed < budget_s and done < w.B:
+        b = (sample_index + done) % w.B
+        kl = None if inp["key_lens"] is None else inp["key_lens"][b:b + 1]
+        x = wd(inp["x"][b:b + 1].copy())
+        t0 = time.perf_counter()
+        if w.kind == "encoder":
+            y1 = rb(mha(x, x, inp["self_attn"], 2 if kl is not None else 0, kl))
+        else:
+            y0 = rb(mha(x, x, inp["self_attn"], 1, None))
+            y1 = rb(mha(y0, wd(inp["memory"][b:b + 1].copy()), inp["cross_attn"],
+                        2 if kl is not None else 0, kl))
+        oracle.ffn(y1, *fw, nthreads=threads)
+        elapsed += time.perf_counter() - t0
+        done += 1
+    desc = (f"{done} of {w.B} batch elements (the whole layer for each); "
+            f"{done * per_elem / 1e9:.2f} GFLOP in {elapsed:.2f} s")
+    return done * per_elem / elapsed / 1e12, threads, desc
+
+
 def pe_inputs(w):
     from synth import inputs as synth
     return {"emb": synth.round_to_bf16_bits(synth.draw_normal(w.seed, 0, (w.B, w.n_q, w.d_model)))}
@@ -331,6 +371,8 @@ def workload_inputs(w):
     from synth import inputs as synth
     if w.kind == "pe":
         return pe_inputs(w)
+    if w.kind in ("encoder", "decoder"):
+        return synth.layer_inputs(w)
     return synth.mha_inputs(w) if w.kind == "mha" else synth.attn_inputs(w)
 
 
@@ -345,6 +387,8 @@ def load_workload(args):
 def sample_rate(w, inp, budget_s: float, sample_index: int = 0):
     if w.kind == "pe":
         return oracle_pe_sample_rate(w, inp, budget_s, sample_index)
+    if w.kind in ("encoder", "decoder"):
+        return oracle_layer_sample_rate(w, inp, budget_s, sample_index)
     if w.is_mha:
         return oracle_mha_sample_rate(w, inp, budget_s, sample_index)
     return oracle_sample_rate(w, inp, budget_s, sample_index)
@@ -431,6 +475,50 @@ def _setup_pe(w, inp):
     return step, host, 1
 
 
+def _setup_layer(w, inp):
+    """Device tensors, workspace and a step closure for one encoder_layer_fwd /
+    decoder_layer_fwd call (five or eight kernel launches)."""
+    import torch
+
+    import head_attention_gb300 as hattn
+    dev = lambda a: _device_array(a, "bf16")
+    f32 = lambda a: torch.from_numpy(a).cuda()
+
+    def mha_w(m):
+        return {**{k: dev(m[k]) for k in ("wq", "wk", "wv", "wo")},
+                "gamma": f32(m["gamma"]), "beta": f32(m["beta"])}
+
+    f = inp["ffn"]
+    ffn = {"w1": dev(f["w1"]), "w2": dev(f["w2"]), "b1": f32(f["b1"]), "b2": f32(f["b2"]),
+           "gamma": f32(f["gamma"]), "beta": f32(f["beta"])}
+    x = dev(inp["x"])
+    y = torch.empty_like(x)
+    kl = None if inp["key_lens"] is None else f32(inp["key_lens"])
+    host_inputs = {"x": (inp["x"], x)}
+    if w.kind == "encoder":
+        sa = mha_w(inp["self_attn"])
+        ws = torch.empty(hattn.encoder_layer_workspace_bytes(hattn.HATTN_BF16, w.B, w.n_q,
+                                                             w.d_model, w.h, w.d_k, w.d_ff),
+                         dtype=torch.uint8, device="cuda")
+
+        def step():
+            hattn.encoder_layer_fwd(x, sa, ffn, inp["eps"], w.h, key_lens=kl, y=y, workspace=ws)
+        launches = 5
+    else:
+        sa, ca = mha_w(inp["self_attn"]), mha_w(inp["cross_attn"])
+        mem = dev(inp["memory"])
+        host_inputs["memory"] = (inp["memory"], mem)
+        ws = torch.empty(hattn.decoder_layer_workspace_bytes(hattn.HATTN_BF16, w.B, w.n_q, w.n_k,
+                                                             w.d_model, w.h, w.d_k, w.d_ff),
+                         dtype=torch.uint8, device="cuda")
+
+        def step():
+            hattn.decoder_layer_fwd(x, mem, sa, ca, ffn, inp["eps"], w.h, src_lens=kl, y=y,
+                                    workspace=ws)
+        launches = 8
+    return step, {"inputs": host_inputs, "output": y}, launches
+
+
 def run_gpu(args, rank, world, local):
     import torch
 
@@ -452,6 +540,10 @@ def run_gpu(args, rank, world, local):
         inp = synth.attn_inputs(w)
         step, host, launches_per_step = _setup_decode(w, inp)
         flops = 4.0 * w.h * w.d_k * float(inp["key_lens"].sum())  # visible (query, key) pairs
+    elif w.kind in ("encoder", "decoder"):
+        inp = synth.layer_inputs(w)
+        step, host, launches_per_step = _setup_layer(w, inp)
+        flops = w.layer_flops()
     elif w.kind == "pe":
         inp = pe_inputs(w)
         step, host, launches_per_step = _setup_pe(w, inp)
@@ -507,6 +599,12 @@ def run_gpu(args, rank, world, local):
     if w.kind == "mha":
         bytes_in = (2 * w.B * w.n_q * w.d_model + 4 * w.d_model * w.h * w.d_k) * esize
         bytes_alg = bytes_in + w.B * w.n_q * w.d_model * esize
+    elif w.kind in ("encoder", "decoder"):
+        n_mha = 1 if w.kind == "encoder" else 2
+        weights = n_mha * 4 * w.d_model * w.h * w.d_k + 2 * w.d_model * w.d_ff
+        acts = w.B * w.n_q * w.d_model + (w.B * w.n_k * w.d_model if w.kind == "decoder" else 0)
+        bytes_in = (acts + weights) * esize
+        bytes_alg = bytes_in + w.B * w.n_q * w.d_model * esize
     elif w.kind == "decode":
         bytes_in = (float(inp["key_lens"].sum()) * w.h * (w.d_k + w.d_v) + w.B * w.h * w.d_k) * esize
         bytes_alg = bytes_in + w.B * w.h * w.d_v * esize
@@ -518,6 +616,9 @@ def run_gpu(args, rank, world, local):
         bytes_alg = bytes_in + w.B * w.n_q * w.h * w.d_v * esize
     tc_attn = w.dtype == "bf16" and w.d_k == w.d_v and w.d_k in (64, 128)
     kernel = {"mha": "mha sublayer: proj_gemm + attn_tc_kernel + outproj_ln (one step)",
+              "encoder": "encoder layer: MHA (proj_gemm, attn_tc_kernel, outproj_ln) + FFN "
+                         "(proj_gemm with bias+ReLU, outproj_ln with bias) (one step)",
+              "decoder": "decoder layer: two MHA sublayers + FFN (eight launches, one step)",
               "decode": f"decode_split_kernel<{w.d_k}> + decode_combine_kernel (one step)",
               "pe": "pos_encoding_kernel"}.get(
                   w.kind, f"attn_tc_kernel<{w.d_k}>" if tc_attn else "attn_simt_kernel")
@@ -570,8 +671,10 @@ def run_gpu(args, rank, world, local):
         "gpu_launches": args.steps * launches_per_step,
         "clocks": sampler.summary(),
     }
-    if w.is_mha:
+    if w.is_mha or w.kind in ("encoder", "decoder"):
         result["config"]["d_model"] = w.d_model
+    if w.kind in ("encoder", "decoder"):
+        result["config"]["d_ff"] = w.d_ff
 
     if not args.no_e2e and w.kind != "pe":
         result["e2e"] = e2e_leg(args, w, host, step, flops, world)

@@ -18,8 +18,19 @@ from ._binding import (  # noqa: F401
     attn_fwd,
     attn_fwd_raw,
     check_device_error,
+    decoder_layer_fwd,
+    decoder_layer_fwd_raw,
+    decoder_layer_workspace_bytes,
+    encoder_layer_fwd,
+    encoder_layer_fwd_raw,
+    encoder_layer_workspace_bytes,
+    ffn_fwd,
+    ffn_fwd_raw,
+    ffn_weights,
+    ffn_workspace_bytes,
     load,
     mha_fwd,
+    mha_weights,
     mha_fwd_noalloc_raw,
     mha_fwd_raw,
     mha_workspace_bytes,

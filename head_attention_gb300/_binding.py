@@ -21,8 +21,22 @@ NOALLOC_SCRATCH_BYTES = 32 << 20
 
 # Every symbol include/hattn.h declares.
 EXPORTED = ("attn_fwd", "attn_decode_fwd", "attn_decode_workspace_bytes", "mha_fwd",
-            "mha_fwd_noalloc", "mha_workspace_bytes", "pos_encoding_fwd", "hattn_status_str",
+            "mha_fwd_noalloc", "mha_workspace_bytes", "pos_encoding_fwd", "ffn_fwd",
+            "ffn_workspace_bytes", "encoder_layer_fwd", "encoder_layer_workspace_bytes",
+            "decoder_layer_fwd", "decoder_layer_workspace_bytes", "hattn_status_str",
             "hattn_check_device_error", "hattn_version")
+
+
+class MhaWeights(ctypes.Structure):
+    """hattn_mha_weights: device pointers of one MHA sublayer's weights."""
+    _fields_ = [("Wq", ctypes.c_void_p), ("Wk", ctypes.c_void_p), ("Wv", ctypes.c_void_p),
+                ("Wo", ctypes.c_void_p), ("gamma", ctypes.c_void_p), ("beta", ctypes.c_void_p)]
+
+
+class FfnWeights(ctypes.Structure):
+    """hattn_ffn_weights: device pointers of one feed-forward sublayer's weights."""
+    _fields_ = [("W1", ctypes.c_void_p), ("b1", ctypes.c_void_p), ("W2", ctypes.c_void_p),
+                ("b2", ctypes.c_void_p), ("gamma", ctypes.c_void_p), ("beta", ctypes.c_void_p)]
 
 _lock = threading.Lock()
 _lib = None
@@ -63,6 +77,20 @@ def load() -> ctypes.CDLL:
         lib.pos_encoding_fwd.restype = i
         lib.mha_workspace_bytes.argtypes = [i] * 8
         lib.mha_workspace_bytes.restype = sz
+        lib.ffn_fwd.argtypes = [vp] * 7 + [f, vp, i, i, i, i, vp, sz, vp]
+        lib.ffn_fwd.restype = i
+        lib.ffn_workspace_bytes.argtypes = [i] * 4
+        lib.ffn_workspace_bytes.restype = sz
+        mw, fw = ctypes.POINTER(MhaWeights), ctypes.POINTER(FfnWeights)
+        lib.encoder_layer_fwd.argtypes = [vp, mw, fw, f, vp, i, i, i, i, i, i, i, vp, vp, sz, vp]
+        lib.encoder_layer_fwd.restype = i
+        lib.encoder_layer_workspace_bytes.argtypes = [i] * 7
+        lib.encoder_layer_workspace_bytes.restype = sz
+        lib.decoder_layer_fwd.argtypes = ([vp, vp, mw, mw, fw, f, vp] + [i] * 8
+                                          + [vp, vp, sz, vp])
+        lib.decoder_layer_fwd.restype = i
+        lib.decoder_layer_workspace_bytes.argtypes = [i] * 8
+        lib.decoder_layer_workspace_bytes.restype = sz
         lib.hattn_status_str.argtypes = [i]
         lib.hattn_status_str.restype = ctypes.c_char_p
         lib.hattn_check_device_error.argtypes = [vp]
@@ -229,3 +257,119 @@ def check_device_error(stream=None) -> int:
 
 def version() -> int:
     return int(load().hattn_version())
+
+
+def ffn_workspace_bytes(dtype, M, d_model, d_ff) -> int:
+    return int(load().ffn_workspace_bytes(int(dtype), int(M), int(d_model), int(d_ff)))
+
+
+def ffn_fwd_raw(x, w1, b1, w2, b2, gamma, beta, eps, y, dtype, M, d_model, d_ff, workspace,
+                ws_bytes, stream) -> int:
+    return load().ffn_fwd(_ptr(x), _ptr(w1), _ptr(b1), _ptr(w2), _ptr(b2), _ptr(gamma),
+                          _ptr(beta), float(eps), _ptr(y), int(dtype), int(M), int(d_model),
+                          int(d_ff), _ptr(workspace), int(ws_bytes), _stream(stream))
+
+
+def ffn_fwd(x, w1, b1, w2, b2, gamma, beta, eps, y=None, workspace=None, stream=None):
+    """Post-norm feed-forward sublayer on bf16 CUDA tensors x [..., d_model]; b1, b2, gamma,
+    beta fp32 (b1/b2 may be None)."""
+    import torch
+    d_model = x.shape[-1]
+    M = x.numel() // d_model
+    d_ff = w1.shape[1]
+    if y is None:
+        y = torch.empty_like(x)
+    if workspace is None:
+        workspace = torch.empty(ffn_workspace_bytes(_dtype_code(x), M, d_model, d_ff),
+                                dtype=torch.uint8, device=x.device)
+    rc = ffn_fwd_raw(x, w1, b1, w2, b2, gamma, beta, eps, y, _dtype_code(x), M, d_model, d_ff,
+                     workspace, workspace.numel(), stream)
+    if rc != OK:
+        raise HattnError(rc, "ffn_fwd")
+    return y
+
+
+def mha_weights(wq, wk, wv, wo, gamma, beta) -> MhaWeights:
+    return MhaWeights(_ptr(wq), _ptr(wk), _ptr(wv), _ptr(wo), _ptr(gamma), _ptr(beta))
+
+
+def ffn_weights(w1, b1, w2, b2, gamma, beta) -> FfnWeights:
+    return FfnWeights(_ptr(w1), _ptr(b1), _ptr(w2), _ptr(b2), _ptr(gamma), _ptr(beta))
+
+
+def encoder_layer_workspace_bytes(dtype, B, n, d_model, h, d_k, d_ff) -> int:
+    return int(load().encoder_layer_workspace_bytes(int(dtype), int(B), int(n), int(d_model),
+                                                    int(h), int(d_k), int(d_ff)))
+
+
+def encoder_layer_fwd_raw(x, attn, ffn, eps, y, dtype, B, n, d_model, h, d_k, d_ff, key_lens,
+                          workspace, ws_bytes, stream) -> int:
+    return load().encoder_layer_fwd(_ptr(x), ctypes.byref(attn) if attn is not None else None,
+                                    ctypes.byref(ffn) if ffn is not None else None, float(eps),
+                                    _ptr(y), int(dtype), int(B), int(n), int(d_model), int(h),
+                                    int(d_k), int(d_ff), _ptr(key_lens), _ptr(workspace),
+                                    int(ws_bytes), _stream(stream))
+
+
+def encoder_layer_fwd(x, attn, ffn, eps, h, key_lens=None, y=None, workspace=None, stream=None):
+    """One post-norm encoder layer on x [B, n, d_model] (bf16 CUDA). attn / ffn are dicts of
+    CUDA tensors with keys wq, wk, wv, wo, gamma, beta / w1, b1, w2, b2, gamma, beta."""
+    import torch
+    B, n, d_model = x.shape
+    d_k = attn["wq"].shape[1] // h
+    d_ff = ffn["w1"].shape[1]
+    if y is None:
+        y = torch.empty_like(x)
+    if workspace is None:
+        workspace = torch.empty(encoder_layer_workspace_bytes(_dtype_code(x), B, n, d_model, h,
+                                                              d_k, d_ff),
+                                dtype=torch.uint8, device=x.device)
+    aw = mha_weights(*(attn[k] for k in ("wq", "wk", "wv", "wo", "gamma", "beta")))
+    fw = ffn_weights(*(ffn[k] for k in ("w1", "b1", "w2", "b2", "gamma", "beta")))
+    rc = encoder_layer_fwd_raw(x, aw, fw, eps, y, _dtype_code(x), B, n, d_model, h, d_k, d_ff,
+                               key_lens, workspace, workspace.numel(), stream)
+    if rc != OK:
+        raise HattnError(rc, "encoder_layer_fwd")
+    return y
+
+
+def decoder_layer_workspace_bytes(dtype, B, n_tgt, n_src, d_model, h, d_k, d_ff) -> int:
+    return int(load().decoder_layer_workspace_bytes(int(dtype), int(B), int(n_tgt), int(n_src),
+                                                    int(d_model), int(h), int(d_k), int(d_ff)))
+
+
+def decoder_layer_fwd_raw(x, memory, self_attn, cross_attn, ffn, eps, y, dtype, B, n_tgt, n_src,
+                          d_model, h, d_k, d_ff, src_lens, workspace, ws_bytes, stream) -> int:
+    ref = lambda s: ctypes.byref(s) if s is not None else None
+    return load().decoder_layer_fwd(_ptr(x), _ptr(memory), ref(self_attn), ref(cross_attn),
+                                    ref(ffn), float(eps), _ptr(y), int(dtype), int(B), int(n_tgt),
+                                    int(n_src), int(d_model), int(h), int(d_k), int(d_ff),
+                                    _ptr(src_lens), _ptr(workspace), int(ws_bytes),
+                                    _stream(stream))
+
+
+def decoder_layer_fwd(x, memory, self_attn, cross_attn, ffn, eps, h, src_lens=None, y=None,
+                      workspace=None, stream=None):
+    """One post-norm decoder layer: x [B, n_tgt, d_model], memory [B, n_src, d_model]
+    (bf16 CUDA); weight dicts as for encoder_layer_fwd."""
+    import torch
+    B, n_tgt, d_model = x.shape
+    n_src = memory.shape[1]
+    d_k = self_attn["wq"].shape[1] // h
+    d_ff = ffn["w1"].shape[1]
+    if y is None:
+        y = torch.empty_like(x)
+    if workspace is None:
+        workspace = torch.empty(decoder_layer_workspace_bytes(_dtype_code(x), B, n_tgt, n_src,
+                                                              d_model, h, d_k, d_ff),
+                                dtype=torch.uint8, device=x.device)
+    keys = ("wq", "wk", "wv", "wo", "gamma", "beta")
+    sw = mha_weights(*(self_attn[k] for k in keys))
+    cw = mha_weights(*(cross_attn[k] for k in keys))
+    fw = ffn_weights(*(ffn[k] for k in ("w1", "b1", "w2", "b2", "gamma", "beta")))
+    rc = decoder_layer_fwd_raw(x, memory, sw, cw, fw, eps, y, _dtype_code(x), B, n_tgt, n_src,
+                               d_model, h, d_k, d_ff, src_lens, workspace, workspace.numel(),
+                               stream)
+    if rc != OK:
+        raise HattnError(rc, "decoder_layer_fwd")
+    return y

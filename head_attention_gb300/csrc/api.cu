@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -404,6 +405,155 @@ int pos_encoding_fwd(const void* emb, void* out, int dtype, int B, int n, int d_
         return HATTN_EINVAL;
     return from_cuda(launch_pos_encoding(emb, out, dtype, B, n, d_model, emb_scale, pos0,
                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+namespace hattn {
+namespace {
+
+bool ffn_shapes_ok(int M, int d_model, int d_ff)
+{
+    return M > 0 && d_model > 0 && d_ff > 0;
+}
+
+int ffn_supported(int d_model, int d_ff)
+{
+    return (d_model % 64 == 0 && d_model <= 512 && d_ff % 64 == 0) ? HATTN_OK : HATTN_EUNSUPPORTED;
+}
+
+}  // namespace
+}  // namespace hattn
+
+extern "C" {
+
+size_t ffn_workspace_bytes(int dtype, int M, int d_model, int d_ff)
+{
+    if (dtype != HATTN_BF16 || !ffn_shapes_ok(M, d_model, d_ff)) return 0;
+    return align256((size_t)M * d_ff * 2);
+}
+
+int ffn_fwd(const void* x, const void* W1, const float* b1, const void* W2, const float* b2,
+            const float* gamma, const float* beta, float eps, void* y, int dtype, int M,
+            int d_model, int d_ff, void* workspace, size_t ws_bytes, hattn_stream_t stream)
+{
+    if (!x || !W1 || !W2 || !gamma || !beta || !y) return HATTN_EINVAL;
+    if (dtype != HATTN_BF16) return dtype == HATTN_F32 ? HATTN_EUNSUPPORTED : HATTN_EINVAL;
+    if (!ffn_shapes_ok(M, d_model, d_ff)) return HATTN_EINVAL;
+    if (!(eps > 0.0f) || !std::isfinite(eps)) return HATTN_EINVAL;
+    const void* ptrs[] = {x, W1, W2, gamma, beta, y};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return HATTN_EINVAL;
+    if ((b1 && !aligned16(b1)) || (b2 && !aligned16(b2))) return HATTN_EINVAL;
+    if (x == y) return HATTN_EINVAL;
+    int rc = ffn_supported(d_model, d_ff);
+    if (rc != HATTN_OK) return rc;
+    const size_t need = ffn_workspace_bytes(dtype, M, d_model, d_ff);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || ws_bytes < need)
+        return HATTN_EWORKSPACE;
+    int* err = device_error_ptr();
+    if (!err) return HATTN_ECUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    void* H = workspace;
+    // H = max(0, x W1 + b1)
+    ProjProblem pr;
+    if (!make_2d_map(&pr.a, x, M, d_model, 128) || !make_2d_map(&pr.w, W1, d_model, d_ff, 64))
+        return HATTN_ECUDA;
+    pr.c = H;
+    pr.M = M;
+    pr.N = d_ff;
+    pr.K = d_model;
+    pr.bias = b1;
+    pr.relu = true;
+    rc = from_cuda(launch_proj_gemm(&pr, 1, st, err));
+    if (rc != HATTN_OK) return rc;
+    // y = LN(x + H W2 + b2)
+    OutProjLnArgs o;
+    if (!make_2d_map(&o.a, H, M, d_ff, 128) || !make_2d_map(&o.wo, W2, d_ff, d_model, 64))
+        return HATTN_ECUDA;
+    o.x = x;
+    o.gamma = gamma;
+    o.beta = beta;
+    o.eps = eps;
+    o.y = y;
+    o.M = M;
+    o.N = d_model;
+    o.K = d_ff;
+    o.bias = b2;
+    return from_cuda(launch_outproj_ln(o, st, err));
+}
+
+size_t encoder_layer_workspace_bytes(int dtype, int B, int n, int d_model, int h, int d_k,
+                                     int d_ff)
+{
+    const size_t mha = mha_workspace_bytes(dtype, B, n, n, d_model, h, d_k, d_k);
+    const size_t ffn = ((long long)B * n > 0x7fffffffLL) ? 0 : ffn_workspace_bytes(dtype, B * n, d_model, d_ff);
+    if (mha == 0 || ffn == 0) return 0;
+    return std::max(mha, ffn) + align256((size_t)B * n * d_model * 2);
+}
+
+int encoder_layer_fwd(const void* x, const hattn_mha_weights* attn, const hattn_ffn_weights* ffn,
+                      float eps, void* y, int dtype, int B, int n, int d_model, int h, int d_k,
+                      int d_ff, const int32_t* key_lens, void* workspace, size_t ws_bytes,
+                      hattn_stream_t stream)
+{
+    if (!x || !attn || !ffn || !y) return HATTN_EINVAL;
+    if (B <= 0 || n <= 0 || (long long)B * n > 0x7fffffffLL) return HATTN_EINVAL;
+    const size_t need = encoder_layer_workspace_bytes(dtype, B, n, d_model, h, d_k, d_ff);
+    if (need == 0) return dtype == HATTN_F32 ? HATTN_EUNSUPPORTED : HATTN_EINVAL;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || ws_bytes < need)
+        return HATTN_EWORKSPACE;
+    const size_t scratch = need - align256((size_t)B * n * d_model * 2);
+    void* y1 = static_cast<char*>(workspace) + scratch;
+    const int mask = key_lens ? HATTN_MASK_KEY_PADDING : HATTN_MASK_NONE;
+    int rc = mha_fwd(x, x, attn->Wq, attn->Wk, attn->Wv, attn->Wo, attn->gamma, attn->beta, eps,
+                     y1, dtype, B, n, n, d_model, h, d_k, d_k, mask, key_lens, workspace, scratch,
+                     stream);
+    if (rc != HATTN_OK) return rc;
+    return ffn_fwd(y1, ffn->W1, ffn->b1, ffn->W2, ffn->b2, ffn->gamma, ffn->beta, eps, y, dtype,
+                   B * n, d_model, d_ff, workspace, scratch, stream);
+}
+
+size_t decoder_layer_workspace_bytes(int dtype, int B, int n_tgt, int n_src, int d_model, int h,
+                                     int d_k, int d_ff)
+{
+    const size_t self = mha_workspace_bytes(dtype, B, n_tgt, n_tgt, d_model, h, d_k, d_k);
+    const size_t cross = mha_workspace_bytes(dtype, B, n_tgt, n_src, d_model, h, d_k, d_k);
+    const size_t ffn =
+        ((long long)B * n_tgt > 0x7fffffffLL) ? 0 : ffn_workspace_bytes(dtype, B * n_tgt, d_model, d_ff);
+    if (self == 0 || cross == 0 || ffn == 0) return 0;
+    return std::max(std::max(self, cross), ffn) + 2 * align256((size_t)B * n_tgt * d_model * 2);
+}
+
+int decoder_layer_fwd(const void* x, const void* memory, const hattn_mha_weights* self_attn,
+                      const hattn_mha_weights* cross_attn, const hattn_ffn_weights* ffn, float eps,
+                      void* y, int dtype, int B, int n_tgt, int n_src, int d_model, int h,
+                      int d_k, int d_ff, const int32_t* src_lens, void* workspace,
+                      size_t ws_bytes, hattn_stream_t stream)
+{
+    if (!x || !memory || !self_attn || !cross_attn || !ffn || !y) return HATTN_EINVAL;
+    if (B <= 0 || n_tgt <= 0 || n_src <= 0 || (long long)B * n_tgt > 0x7fffffffLL)
+        return HATTN_EINVAL;
+    const size_t need =
+        decoder_layer_workspace_bytes(dtype, B, n_tgt, n_src, d_model, h, d_k, d_ff);
+    if (need == 0) return dtype == HATTN_F32 ? HATTN_EUNSUPPORTED : HATTN_EINVAL;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || ws_bytes < need)
+        return HATTN_EWORKSPACE;
+    const size_t act = align256((size_t)B * n_tgt * d_model * 2);
+    const size_t scratch = need - 2 * act;
+    void* y1 = static_cast<char*>(workspace) + scratch;
+    void* y2 = static_cast<char*>(y1) + act;
+    int rc = mha_fwd(x, x, self_attn->Wq, self_attn->Wk, self_attn->Wv, self_attn->Wo,
+                     self_attn->gamma, self_attn->beta, eps, y1, dtype, B, n_tgt, n_tgt, d_model,
+                     h, d_k, d_k, HATTN_MASK_CAUSAL, nullptr, workspace, scratch, stream);
+    if (rc != HATTN_OK) return rc;
+    rc = mha_fwd(y1, memory, cross_attn->Wq, cross_attn->Wk, cross_attn->Wv, cross_attn->Wo,
+                 cross_attn->gamma, cross_attn->beta, eps, y2, dtype, B, n_tgt, n_src, d_model, h,
+                 d_k, d_k, src_lens ? HATTN_MASK_KEY_PADDING : HATTN_MASK_NONE, src_lens,
+                 workspace, scratch, stream);
+    if (rc != HATTN_OK) return rc;
+    return ffn_fwd(y2, ffn->W1, ffn->b1, ffn->W2, ffn->b2, ffn->gamma, ffn->beta, eps, y, dtype,
+                   B * n_tgt, d_model, d_ff, workspace, scratch, stream);
 }
 
 const char* hattn_status_str(int status)

@@ -5,7 +5,9 @@
 //                 (Q = x_q Wq, K = x_kv Wk, V = x_kv Wv). C is row-major
 //                 [M, h*d], which is already the [B, n, h, d] layout the
 //                 attention kernel reads (heads concatenated along features).
-//   outproj_ln:   y = LayerNorm(x + A . Wo) * gamma + beta, one CTA per 128 rows
+//                 An optional per-column bias and ReLU make the same kernel the
+//                 first layer of the feed-forward sublayer, max(0, x W1 + b1).
+//   outproj_ln:   y = LayerNorm(x + A . Wo [+ b]) * gamma + beta, one CTA per 128 rows
 //                 holding the whole d_model-wide row in TMEM, so the residual
 //                 add, the mean/variance and the normalisation run in the
 //                 epilogue on fp32 values and y is rounded to bf16 once.
@@ -19,7 +21,8 @@
 // Sources: the projections Q = X W^Q etc. ([hex4c59 "读懂 Attention Is All You
 // Need", §Q、K、V 是三种计算角色]), W^O after the concatenated heads
 // (§多头注意力让一次读取有多组投影), LayerNorm(x + F(x)) (§Add & Norm 里究竟
-// 发生了什么？).
+// 发生了什么？); the feed-forward sublayer LayerNorm(x + max(0, x W1 + b1) W2 + b2)
+// ([devpress "【深度学习】Transformer（Attention Is All You Need）", §2.3]).
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -84,6 +87,8 @@ constexpr uint32_t kProjIdesc = idesc_bf16_f32(128, kProjBN, false, true);
 
 struct ProjParams {
     void* c[3];
+    const float* bias[3];
+    int relu[3];
     int M[3], N[3];
     int K;
     int tiles_n[3];
@@ -168,11 +173,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(p.c[prob]) + (size_t)row * p.N[prob];
             const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+            const float* bias = p.bias[prob];
+            const bool relu = p.relu[prob] != 0;
 #pragma unroll
             for (int c = 0; c < kProjBN / 32; ++c) {
                 uint32_t acc[32];
                 tmem_ld_x32(lane_base + 32 * c, acc);
                 const int col = tn * kProjBN + 32 * c;
+                if (bias && col < p.N[prob]) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        float v = __uint_as_float(acc[i]) + __ldg(bias + col + i);
+                        if (relu) v = fmaxf(v, 0.0f);
+                        acc[i] = __float_as_uint(v);
+                    }
+                } else if (relu) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[i] = __float_as_uint(fmaxf(__uint_as_float(acc[i]), 0.0f));
+                }
                 if (row < p.M[prob] && col < p.N[prob]) {
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4) {
@@ -202,6 +220,7 @@ constexpr int kLnSmem = kLnOffBar + 8 * (2 * kLnStages + 2) + 16 + 1024;
 
 struct LnParams {
     const __nv_bfloat16* x;
+    const float* bias;
     const float* gamma;
     const float* beta;
     float eps;
@@ -299,6 +318,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int v4 = 0; v4 < 4; ++v4) xv[v4] = src[v4];
                 }
                 const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(xv);
+                if (p.bias) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        z[i] = __float_as_uint(__uint_as_float(z[i]) + __ldg(p.bias + 32 * c + i));
+                }
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const float zi = __uint_as_float(z[i]) + __bfloat162float(xb[i]);
@@ -364,6 +388,8 @@ cudaError_t launch_proj_gemm(const ProjProblem* problems, int count, cudaStream_
         const ProjProblem& pr = problems[i < count ? i : count - 1];
         if (pr.K != p.K || pr.K % 64 != 0 || pr.N % 64 != 0) return cudaErrorInvalidValue;
         p.c[i] = pr.c;
+        p.bias[i] = pr.bias;
+        p.relu[i] = pr.relu ? 1 : 0;
         p.M[i] = pr.M;
         p.N[i] = pr.N;
         p.tiles_n[i] = (pr.N + kProjBN - 1) / kProjBN;
@@ -386,6 +412,7 @@ cudaError_t launch_outproj_ln(const OutProjLnArgs& a, cudaStream_t stream, int* 
     if (a.N % 64 != 0 || a.N > kLnMaxN || a.K % 64 != 0) return cudaErrorInvalidValue;
     LnParams p;
     p.x = static_cast<const __nv_bfloat16*>(a.x);
+    p.bias = a.bias;
     p.gamma = a.gamma;
     p.beta = a.beta;
     p.eps = a.eps;

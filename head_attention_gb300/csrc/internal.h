@@ -77,13 +77,15 @@ struct ProjProblem {
     CUtensorMap w;  // W [K][N], 64 x 64 boxes, N-major
     void* c;        // bf16 [M][N]
     int M, N, K;
+    const float* bias = nullptr;  // optional fp32 [N], added to every row
+    bool relu = false;            // max(0, .) after the bias
 };
 
 // Up to three independent projection GEMMs in one launch (Q, K, V).
 cudaError_t launch_proj_gemm(const ProjProblem* problems, int count, cudaStream_t stream,
                              int* err_word);
 
-// y = LayerNorm(x + A . Wo) * gamma + beta over rows of length N = d_model.
+// y = LayerNorm(x + A . Wo [+ bias]) * gamma + beta over rows of length N = d_model.
 struct OutProjLnArgs {
     CUtensorMap a;   // A [M][K] bf16, K-major boxes 64 x 128
     CUtensorMap wo;  // Wo [K][N] bf16, N-major boxes 64 x 64
@@ -93,6 +95,7 @@ struct OutProjLnArgs {
     float eps;
     void* y;  // bf16 [M][N]
     int M, N, K;
+    const float* bias = nullptr;  // optional fp32 [N], added before the residual
 };
 cudaError_t launch_outproj_ln(const OutProjLnArgs& args, cudaStream_t stream, int* err_word);
 

@@ -210,6 +210,98 @@ size_t attn_decode_workspace_bytes(int B, int h, int n_max, int d);
 size_t mha_workspace_bytes(int dtype, int B, int n_q, int n_k, int d_model, int h, int d_k,
                            int d_v);
 
+/*
+ * ffn_fwd — the post-norm position-wise feed-forward sublayer,
+ *     y = LayerNorm(x + max(0, x W1 + b1) W2 + b2) * gamma + beta   (row by row)
+ *
+ * Defined in [P4] §2.3 (x + FFN(x) = x + max(0, x W1 + b1) W2 + b2, then norm2) and
+ * [P1] §前馈网络为什么放在注意力后面？ (the same FFN for every position; ReLU;
+ * 512 -> 2048 -> 512 in the base model).
+ *
+ *   x      device [M, d_model] (M = B * n rows; rows are independent)
+ *   W1     device [d_model, d_ff] row-major;  b1 fp32 [d_ff] or NULL (zero bias)
+ *   W2     device [d_ff, d_model] row-major;  b2 fp32 [d_model] or NULL
+ *   gamma, beta  fp32 [d_model];  eps > 0
+ *   y      device [M, d_model] (must not alias x)
+ *   workspace  device scratch of ffn_workspace_bytes() bytes, 256-byte aligned,
+ *          caller-owned; holds the hidden activations max(0, x W1 + b1) in bf16
+ * Supported: dtype HATTN_BF16; d_model a multiple of 64 and <= 512; d_ff a
+ * multiple of 64; every pointer 16-byte aligned. fp32 accumulation; the
+ * hidden activations are rounded to bf16 once, y once.
+ * Returns HATTN_OK, HATTN_EINVAL, HATTN_EUNSUPPORTED, HATTN_EWORKSPACE or
+ * HATTN_ECUDA; asynchronous on `stream`.
+ */
+int ffn_fwd(const void* x, const void* W1, const float* b1, const void* W2, const float* b2,
+            const float* gamma, const float* beta, float eps, void* y, int dtype, int M,
+            int d_model, int d_ff, void* workspace, size_t ws_bytes, hattn_stream_t stream);
+
+/* Bytes of caller-owned workspace ffn_fwd needs for these sizes (0 on bad sizes). */
+size_t ffn_workspace_bytes(int dtype, int M, int d_model, int d_ff);
+
+/* Weights of one post-norm MHA sublayer (see mha_fwd): W^Q, W^K, W^V [d_model, h*d_k],
+ * W^O [h*d_k, d_model] (dtype elements), LayerNorm gamma/beta fp32 [d_model]. */
+typedef struct hattn_mha_weights {
+    const void* Wq;
+    const void* Wk;
+    const void* Wv;
+    const void* Wo;
+    const float* gamma;
+    const float* beta;
+} hattn_mha_weights;
+
+/* Weights of one feed-forward sublayer (see ffn_fwd). */
+typedef struct hattn_ffn_weights {
+    const void* W1;
+    const float* b1;
+    const void* W2;
+    const float* b2;
+    const float* gamma;
+    const float* beta;
+} hattn_ffn_weights;
+
+/*
+ * encoder_layer_fwd — one encoder layer: the MHA sublayer (self-attention) then
+ * the feed-forward sublayer, each post-norm,
+ *     y1 = LayerNorm1(x + MHA(x, x));  y = LayerNorm2(y1 + FFN(y1)).
+ * Defined in [P1] §编码器：交互之后，还要逐位置处理信息 (two sublayers, each with
+ * residual and LayerNorm) and [P4] §2.3 (the order self-attention -> norm1 ->
+ * FFN -> norm2). key_lens (device int32 [B]) masks padded source positions as
+ * keys (mask_kind HATTN_MASK_KEY_PADDING of mha_fwd), or NULL for none.
+ * x, y: device [B, n, d_model]; the sublayer output y1 is rounded to bf16 (it is
+ * the bf16 input of the second sublayer). workspace: encoder_layer_workspace_bytes()
+ * bytes, 256-byte aligned. Constraints: those of mha_fwd (d_k in {64, 128}) and
+ * ffn_fwd. Returns as mha_fwd / ffn_fwd.
+ */
+int encoder_layer_fwd(const void* x, const hattn_mha_weights* attn, const hattn_ffn_weights* ffn,
+                      float eps, void* y, int dtype, int B, int n, int d_model, int h, int d_k,
+                      int d_ff, const int32_t* key_lens, void* workspace, size_t ws_bytes,
+                      hattn_stream_t stream);
+
+size_t encoder_layer_workspace_bytes(int dtype, int B, int n, int d_model, int h, int d_k,
+                                     int d_ff);
+
+/*
+ * decoder_layer_fwd — one decoder layer: masked self-attention, encoder-decoder
+ * (cross) attention over the encoder output `memory`, then the feed-forward
+ * sublayer, each post-norm:
+ *     y1 = LN1(x + MHA_causal(x, x));  y2 = LN2(y1 + MHA(y1, memory));  y = LN3(y2 + FFN(y2)).
+ * Defined in [P1] §解码器有两种读取：看前缀，以及看源句 (three sublayers, each with
+ * its own Add & Norm; queries from the decoder, keys and values from the encoder
+ * output) and the causal mask of §右移目标，是为了让输入与标签错开一位.
+ *   x, y     device [B, n_tgt, d_model];  memory device [B, n_src, d_model]
+ *   src_lens device int32 [B] (cross-attention key lengths) or NULL for none
+ * workspace: decoder_layer_workspace_bytes() bytes, 256-byte aligned.
+ * Returns as mha_fwd / ffn_fwd.
+ */
+int decoder_layer_fwd(const void* x, const void* memory, const hattn_mha_weights* self_attn,
+                      const hattn_mha_weights* cross_attn, const hattn_ffn_weights* ffn, float eps,
+                      void* y, int dtype, int B, int n_tgt, int n_src, int d_model, int h,
+                      int d_k, int d_ff, const int32_t* src_lens, void* workspace,
+                      size_t ws_bytes, hattn_stream_t stream);
+
+size_t decoder_layer_workspace_bytes(int dtype, int B, int n_tgt, int n_src, int d_model, int h,
+                                     int d_k, int d_ff);
+
 /* Static text for a status code. */
 const char* hattn_status_str(int status);
 

@@ -25,6 +25,10 @@ STREAM_Q, STREAM_K, STREAM_V = 0, 1, 2
 STREAM_XQ, STREAM_XKV = 3, 4
 STREAM_WQ, STREAM_WK, STREAM_WV, STREAM_WO = 5, 6, 7, 8
 STREAM_KEYLEN = 9
+STREAM_W1, STREAM_B1, STREAM_W2, STREAM_B2 = 10, 11, 12, 13
+# A second set of sublayer weights (the decoder layer's cross-attention) draws
+# from the MHA streams offset by this much.
+STREAM_CROSS_OFFSET = 100
 
 MASK_NONE = 0
 MASK_CAUSAL = 1
@@ -134,7 +138,8 @@ class Workload:
     key_len_range: tuple | None = None  # inclusive (lo, hi) when KEY_PADDING
     d_model: int = 0  # > 0 for the MHA sublayer (and the embedding width for "pe")
     description: str = ""
-    kind: str = "attn"  # "attn", "mha", "decode" (n_q = 1 over a K/V prefix) or "pe"
+    kind: str = "attn"  # "attn", "mha", "decode" (n_q = 1 over a K/V prefix), "pe", "encoder", "decoder"
+    d_ff: int = 0  # feed-forward width of the encoder / decoder layer
 
     @property
     def scale(self) -> float:
@@ -156,6 +161,22 @@ class Workload:
         hd = self.h * self.d_k
         return 2.0 * self.B * (self.n_q * self.d_model * hd + 2 * self.n_k * self.d_model * hd
                                + self.n_q * self.h * self.d_v * self.d_model)
+
+    def layer_flops(self) -> float:
+        """Defined FLOPs of one encoder / decoder layer: every attention at the metric's
+        count (causal halved), every projection and both FFN GEMMs (2 per multiply-add)."""
+        if self.kind not in ("encoder", "decoder"):
+            return 0.0
+        dm, hd = self.d_model, self.h * self.d_k
+        Mq, Mk = self.B * self.n_q, self.B * self.n_k
+        ffn = 2.0 * 2.0 * Mq * dm * self.d_ff
+        self_proj = 2.0 * Mq * dm * hd * 4  # Q, K, V, O over the target rows
+        self_attn = 4.0 * self.B * self.h * self.n_q * self.n_q * self.d_k
+        if self.kind == "encoder":
+            return ffn + self_proj + self_attn
+        cross_proj = 2.0 * dm * hd * (2 * Mq + 2 * Mk)  # Q, O over the target; K, V over the source
+        cross_attn = 4.0 * self.B * self.h * self.n_q * self.n_k * self.d_k
+        return ffn + self_proj + 0.5 * self_attn + cross_proj + cross_attn
 
     def tokens(self) -> int:
         return self.B * self.n_q
@@ -181,6 +202,18 @@ WORKLOADS = {
         "mha_bf16", "bf16", B=16, h=8, n_q=512, n_k=512, d_k=64, d_v=64,
         mask_kind=MASK_NONE, seed=3, d_model=512, kind="mha",
         description="post-norm MHA sublayer, bf16, B=16 n=512 d_model=512 h=8 d=64"),
+    "encoder_layer_bf16": Workload(
+        "encoder_layer_bf16", "bf16", B=16, h=8, n_q=512, n_k=512, d_k=64, d_v=64,
+        mask_kind=MASK_NONE, seed=8, d_model=512, d_ff=2048, kind="encoder",
+        description="post-norm encoder layer (MHA + FFN sublayers), bf16, B=16 n=512 d_model=512 "
+                    "h=8 d=64 d_ff=2048"),
+    "decoder_layer_bf16": Workload(
+        "decoder_layer_bf16", "bf16", B=16, h=8, n_q=512, n_k=512, d_k=64, d_v=64,
+        mask_kind=MASK_KEY_PADDING, seed=9, d_model=512, d_ff=2048, kind="decoder",
+        key_len_range=(256, 512),
+        description="post-norm decoder layer (causal self-attention, cross-attention over "
+                    "source lengths U[256,512], FFN), bf16, B=16 n_tgt=n_src=512 d_model=512 h=8 "
+                    "d=64 d_ff=2048"),
     "long_causal_d128": Workload(
         "long_causal_d128", "bf16", B=4, h=16, n_q=8192, n_k=8192, d_k=128, d_v=128,
         mask_kind=MASK_CAUSAL, seed=4,
@@ -256,6 +289,56 @@ def mha_inputs(w: Workload, self_attention: bool = True) -> dict:
         "eps": 1e-6,
         "key_lens": None,
     }
+    if w.mask_kind & MASK_KEY_PADDING:
+        lo, hi = w.key_len_range if w.key_len_range else (1, w.n_k)
+        out["key_lens"] = draw_key_lens(w.seed, STREAM_KEYLEN, w.B, lo, hi)
+    return out
+
+
+def ffn_inputs(w: Workload, seed_offset: int = 0) -> dict:
+    """Feed-forward sublayer weights: W1 ~ N(0, 1/d_model), W2 ~ N(0, 1/d_ff) in the
+    kernel dtype, biases b1, b2 ~ N(0, 0.1^2) in fp32, gamma = 1, beta = 0."""
+    dm, dff = w.d_model, w.d_ff
+    s = w.seed + seed_offset
+    return {
+        "w1": _to_kernel_dtype(draw_normal(s, STREAM_W1, (dm, dff), 1.0 / math.sqrt(dm)), w.dtype),
+        "b1": draw_normal(s, STREAM_B1, (dff,), 0.1).astype(np.float32),
+        "w2": _to_kernel_dtype(draw_normal(s, STREAM_W2, (dff, dm), 1.0 / math.sqrt(dff)), w.dtype),
+        "b2": draw_normal(s, STREAM_B2, (dm,), 0.1).astype(np.float32),
+        "gamma": np.ones(dm, dtype=np.float32),
+        "beta": np.zeros(dm, dtype=np.float32),
+        "eps": 1e-6,
+    }
+
+
+def _mha_weights(w: Workload, offset: int) -> dict:
+    dm, hdk, hdv = w.d_model, w.h * w.d_k, w.h * w.d_v
+    wstd = 1.0 / math.sqrt(dm)
+    return {
+        "wq": _to_kernel_dtype(draw_normal(w.seed, offset + STREAM_WQ, (dm, hdk), wstd), w.dtype),
+        "wk": _to_kernel_dtype(draw_normal(w.seed, offset + STREAM_WK, (dm, hdk), wstd), w.dtype),
+        "wv": _to_kernel_dtype(draw_normal(w.seed, offset + STREAM_WV, (dm, hdv), wstd), w.dtype),
+        "wo": _to_kernel_dtype(draw_normal(w.seed, offset + STREAM_WO, (hdv, dm), wstd), w.dtype),
+        "gamma": np.ones(dm, dtype=np.float32),
+        "beta": np.zeros(dm, dtype=np.float32),
+    }
+
+
+def layer_inputs(w: Workload) -> dict:
+    """Inputs of one encoder layer (kind "encoder": x [B, n_q, d_model], self-attention
+    weights, FFN weights, optional key lengths) or decoder layer (kind "decoder": also the
+    encoder output ("memory") [B, n_k, d_model], cross-attention weights, source lengths)."""
+    out = {
+        "x": _to_kernel_dtype(draw_normal(w.seed, STREAM_XQ, (w.B, w.n_q, w.d_model)), w.dtype),
+        "self_attn": _mha_weights(w, 0),
+        "ffn": ffn_inputs(w),
+        "eps": 1e-6,
+        "key_lens": None,
+    }
+    if w.kind == "decoder":
+        out["memory"] = _to_kernel_dtype(draw_normal(w.seed, STREAM_XKV, (w.B, w.n_k, w.d_model)),
+                                         w.dtype)
+        out["cross_attn"] = _mha_weights(w, STREAM_CROSS_OFFSET)
     if w.mask_kind & MASK_KEY_PADDING:
         lo, hi = w.key_len_range if w.key_len_range else (1, w.n_k)
         out["key_lens"] = draw_key_lens(w.seed, STREAM_KEYLEN, w.B, lo, hi)

@@ -43,14 +43,25 @@ def errors(got, ref):
     return float(d.max()), float(d.mean())
 
 
-def assert_close(got, ref, dtype, what=""):
-    max_tol, mean_tol = TOL[dtype]
+def assert_close(got, ref, dtype, what="", tol=None):
+    max_tol, mean_tol = tol if tol is not None else TOL[dtype]
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     mx, mn = errors(got, ref)
-    assert mx <= max_tol, f"{what}: max |err| {mx:.3g} > {max_tol}"
+    assert mx <= max_tol, f"{what}: max |err| {mx:.3g} > {max_tol} (mean {mn:.3g})"
     if mean_tol is not None:
-        assert mn <= mean_tol, f"{what}: mean |err| {mn:.3g} > {mean_tol}"
+        assert mn <= mean_tol, f"{what}: mean |err| {mn:.3g} > {mean_tol} (max {mx:.3g})"
     return mx, mn
+
+
+def chained_tol(sublayers: int):
+    """bf16 tolerance of k chained sublayers. Each sublayer's bf16 output is the next
+    one's input and reaches the next output through the residual with a gain of at
+    most about 1 (LayerNorm divides by sigma(x + F(x)) >= ~1 for unit-variance x), so
+    a sublayer's own error (its bf16 roundings, up to a flipped rounding of its
+    input, 2^-8 |y|) adds to those before it: the per-sublayer max and mean
+    tolerances add up once per sublayer (triangle inequality)."""
+    max_tol, mean_tol = TOL["bf16"]
+    return (sublayers * max_tol, sublayers * mean_tol)
 
 
 def sample_rows(B, n_q, h, count, seed=0, n_tile=128):

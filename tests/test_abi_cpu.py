@@ -166,3 +166,78 @@ def test_decode_workspace_size():
     assert n > 0 and n % (4 * 130) == 0
     assert hattn.attn_decode_workspace_bytes(1, 1, 1, 128) == 4 * 130
     assert hattn.attn_decode_workspace_bytes(1, 1, 1, 100) == 0
+
+
+FFN_GOOD = dict(x=A, w1=2 * A, b1=3 * A, w2=4 * A, b2=5 * A, gamma=6 * A, beta=7 * A, eps=1e-6,
+                y=8 * A, dtype=1, M=256, d_model=512, d_ff=2048, workspace=0x100000,
+                ws_bytes=256 * 2048 * 2, stream=0)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=None), hattn._binding.EINVAL),
+    (dict(w2=None), hattn._binding.EINVAL),
+    (dict(gamma=None), hattn._binding.EINVAL),
+    (dict(dtype=0), hattn._binding.EUNSUPPORTED),
+    (dict(dtype=7), hattn._binding.EINVAL),
+    (dict(M=0), hattn._binding.EINVAL),
+    (dict(eps=0.0), hattn._binding.EINVAL),
+    (dict(y=A), hattn._binding.EINVAL),            # y aliases x
+    (dict(x=A + 8), hattn._binding.EINVAL),        # misaligned
+    (dict(b1=3 * A + 4), hattn._binding.EINVAL),
+    (dict(d_model=576), hattn._binding.EUNSUPPORTED),
+    (dict(d_model=96), hattn._binding.EUNSUPPORTED),
+    (dict(d_ff=100), hattn._binding.EUNSUPPORTED),
+    (dict(workspace=None), hattn._binding.EWORKSPACE),
+    (dict(workspace=0x100010), hattn._binding.EWORKSPACE),
+    (dict(ws_bytes=256 * 2048 * 2 - 1), hattn._binding.EWORKSPACE),
+])
+def test_ffn_rejects_bad_arguments(lib, kw, code):
+    args = dict(FFN_GOOD)
+    args.update(kw)
+    assert hattn.ffn_fwd_raw(**args) == code
+
+
+def test_ffn_and_layer_workspace_sizes(lib):
+    assert hattn.ffn_workspace_bytes(1, 8192, 512, 2048) == 8192 * 2048 * 2
+    assert hattn.ffn_workspace_bytes(1, 3, 64, 64) == 512  # rounded up to 256 bytes
+    assert hattn.ffn_workspace_bytes(0, 8192, 512, 2048) == 0
+    mha = hattn.mha_workspace_bytes(1, 16, 512, 512, 512, 8, 64, 64)
+    act = 16 * 512 * 512 * 2
+    assert hattn.encoder_layer_workspace_bytes(1, 16, 512, 512, 8, 64, 2048) == max(
+        mha, 8192 * 2048 * 2) + act
+    cross = hattn.mha_workspace_bytes(1, 16, 512, 300, 512, 8, 64, 64)
+    assert hattn.decoder_layer_workspace_bytes(1, 16, 512, 300, 512, 8, 64, 2048) == max(
+        mha, cross, 8192 * 2048 * 2) + 2 * act
+    assert hattn.encoder_layer_workspace_bytes(1, 0, 512, 512, 8, 64, 2048) == 0
+
+
+def _weights():
+    aw = hattn.mha_weights(2 * A, 3 * A, 4 * A, 5 * A, 6 * A, 7 * A)
+    fw = hattn.ffn_weights(8 * A, 9 * A, 10 * A, 11 * A, 12 * A, 13 * A)
+    return aw, fw
+
+
+def test_layers_reject_bad_arguments(lib):
+    aw, fw = _weights()
+    ws = hattn.encoder_layer_workspace_bytes(1, 2, 128, 512, 8, 64, 2048)
+    enc = dict(x=A, attn=aw, ffn=fw, eps=1e-6, y=20 * A, dtype=1, B=2, n=128, d_model=512, h=8,
+               d_k=64, d_ff=2048, key_lens=None, workspace=0x1000000, ws_bytes=ws, stream=0)
+    for kw, code in [(dict(x=None), hattn._binding.EINVAL), (dict(attn=None), hattn._binding.EINVAL),
+                     (dict(ffn=None), hattn._binding.EINVAL), (dict(B=0), hattn._binding.EINVAL),
+                     (dict(dtype=0), hattn._binding.EUNSUPPORTED),
+                     (dict(ws_bytes=ws - 1), hattn._binding.EWORKSPACE),
+                     (dict(workspace=0x1000010), hattn._binding.EWORKSPACE)]:
+        args = dict(enc)
+        args.update(kw)
+        assert hattn.encoder_layer_fwd_raw(**args) == code, kw
+    ws = hattn.decoder_layer_workspace_bytes(1, 2, 128, 96, 512, 8, 64, 2048)
+    dec = dict(x=A, memory=30 * A, self_attn=aw, cross_attn=aw, ffn=fw, eps=1e-6, y=20 * A,
+               dtype=1, B=2, n_tgt=128, n_src=96, d_model=512, h=8, d_k=64, d_ff=2048,
+               src_lens=None, workspace=0x1000000, ws_bytes=ws, stream=0)
+    for kw, code in [(dict(memory=None), hattn._binding.EINVAL),
+                     (dict(cross_attn=None), hattn._binding.EINVAL),
+                     (dict(n_src=0), hattn._binding.EINVAL),
+                     (dict(ws_bytes=ws - 1), hattn._binding.EWORKSPACE)]:
+        args = dict(dec)
+        args.update(kw)
+        assert hattn.decoder_layer_fwd_raw(**args) == code, kw
