@@ -1,22 +1,26 @@
-// Tensor-core GEMMs of the post-norm MHA sublayer (bf16 operands, fp32
-// accumulation in TMEM), for sm_103a.
+// Tensor-core GEMMs of the MHA and feed-forward sublayers (bf16 operands, fp32
+// accumulation in TMEM), for sm_103a. One persistent, warp-specialised kernel
+// template with two epilogues:
 //
-//   proj_gemm:    C = A . W for up to three independent problems in one launch
-//                 (Q = x_q Wq, K = x_kv Wk, V = x_kv Wv). C is row-major
-//                 [M, h*d], which is already the [B, n, h, d] layout the
-//                 attention kernel reads (heads concatenated along features).
-//                 An optional per-column bias and ReLU make the same kernel the
-//                 first layer of the feed-forward sublayer, max(0, x W1 + b1).
-//   outproj_ln:   y = LayerNorm(x + A . Wo [+ b]) * gamma + beta, one CTA per 128 rows
-//                 holding the whole d_model-wide row in TMEM, so the residual
-//                 add, the mean/variance and the normalisation run in the
-//                 epilogue on fp32 values and y is rounded to bf16 once.
+//   store:  C = A . W [+ bias][, max(0, .)] for up to three independent
+//           problems in one launch (Q = x_q W^Q, K = x_kv W^K, V = x_kv W^V;
+//           or the first feed-forward layer max(0, x W1 + b1)). C is
+//           row-major [M, N]; for the projections that is already the
+//           [B, n, h, d] layout the attention kernel reads.
+//   norm:   y = LayerNorm(x + A . W [+ b]) * gamma + beta (the out-projection
+//           W^O, or the second feed-forward layer W2, with the residual and
+//           the post-norm). The mean and biased variance need whole rows: a
+//           row of up to 256 columns stays in one CTA; wider rows (d_model up
+//           to 512) are split over the two CTAs of a cluster, which exchange
+//           their per-row partial sums through distributed shared memory.
 //
-// Operands arrive by TMA with 128-byte swizzle: A as 128-row x 64-column
-// K-major boxes, W ([K][N] row-major, i.e. N-major) as 64-row x 64-column
-// boxes. Warp 0 issues the copies, warp 1 (one thread) the tcgen05 MMAs, and
-// warps 2-5 run the epilogue; thread r of the epilogue owns output row r (TMEM
-// lane r). All mbarrier waits are bounded.
+// Tiles are 128 rows x up to 256 columns. Warp 0 streams A (128 x 64 boxes,
+// K-major) and W ([K][N] row-major, i.e. N-major, 64 x 64 boxes) through a
+// 4-stage shared-memory ring by TMA; warp 1 (one thread) issues the tcgen05
+// MMAs into one of two TMEM accumulators (256 columns each), so the epilogue
+// of one tile overlaps the MMAs of the next; warps 2-5 run the epilogue, thread
+// r of a warp quadrant owning output row r (TMEM lane r). CTAs loop over tiles
+// (persistent grid of at most one CTA per SM). All mbarrier waits are bounded.
 //
 // Sources: the projections Q = X W^Q etc. ([hex4c59 "读懂 Attention Is All You
 // Need", §Q、K、V 是三种计算角色]), W^O after the concatenated heads
@@ -25,6 +29,7 @@
 // ([devpress "【深度学习】Transformer（Attention Is All You Need）", §2.3]).
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cmath>
 
 #include "internal.h"
@@ -35,343 +40,413 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kWarpLoad = 0;
-constexpr int kWarpMma = 1;
-constexpr uint32_t kABoxBytes = 128 * 64 * 2;  // A box: 128 rows x 64 columns
-constexpr uint32_t kWBoxBytes = 64 * 64 * 2;   // W box: 64 rows x 64 columns
+constexpr int kWarpMma = 1;  // also owns the TMEM allocation
+constexpr int kBM = 128, kBN = 256, kBK = 64;
+constexpr int kStages = 4;
+constexpr uint32_t kABoxBytes = kBM * kBK * 2;  // A box: 128 rows x 64 columns
+constexpr uint32_t kWBoxBytes = 64 * kBK * 2;   // W box: 64 K-rows x 64 N-columns
+constexpr uint32_t kStageBytes = kABoxBytes + (kBN / 64) * kWBoxBytes;
+// Barrier indices.
+constexpr int kBarFull = 0;
+constexpr int kBarEmpty = kStages;
+constexpr int kBarAccFull = 2 * kStages;       // 2: accumulator b holds a finished tile
+constexpr int kBarAccEmpty = 2 * kStages + 2;  // 2: the epilogue has read accumulator b
+constexpr int kBarSum = 2 * kStages + 4;       // the peer's per-row partial sums arrived
+constexpr int kBarSq = 2 * kStages + 5;        // the peer's per-row squared deviations arrived
+constexpr int kBarDrain = 2 * kStages + 6;
+constexpr int kNumBars = 2 * kStages + 7;
+constexpr int kOffBar = kStages * kStageBytes;
+constexpr int kOffStat = kOffBar + 8 * kNumBars;  // float recv_sum[128], recv_sq[128]
+constexpr int kOffSlot = kOffStat + 2 * kBM * 4;  // TMEM base address
+constexpr int kSmemBytes = kOffSlot + 16 + 1024;  // + slack to align the base to 1024 B
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+constexpr int kEpiThreads = 128;
 
-// ------------------------------------------------------------------ shared pieces
-
-struct Ring {
-    uint32_t full0, empty0, acc, slot;
+struct GemmProblem {
+    void* c;            // bf16 [M][N] (store epilogue) or y (norm epilogue)
+    const float* bias;  // fp32 [N] or null
+    int relu;
+    int M, N, K;
+    int tiles_n;
+    int tile_begin;
 };
 
-__device__ __forceinline__ void gemm_setup(uint32_t sbar, int stages, uint32_t* tmem_slot,
-                                           uint32_t tmem_cols, int warp)
-{
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < stages; ++s) {
-            mbar_init(sbar + 8u * s, 1);             // full
-            mbar_init(sbar + 8u * (stages + s), 1);  // empty
-        }
-        mbar_init(sbar + 8u * (2 * stages), 1);  // accumulator ready
-        mbar_init(sbar + 8u * (2 * stages + 1), 1);  // drain
-        fence_barrier_init();
-    }
-    if (warp == kWarpMma) {
-        tmem_alloc(smem_u32(tmem_slot), tmem_cols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-}
-
-__device__ __forceinline__ void gemm_teardown(uint32_t tmem, uint32_t cols, int warp)
-{
-    tc_fence_before();
-    __syncthreads();
-    if (warp == kWarpMma) {
-        tc_fence_after();
-        tmem_dealloc(tmem, cols);
-    }
-}
-
-// ------------------------------------------------------------------ projection GEMM
-
-constexpr int kProjBN = 128;
-constexpr int kProjStages = 3;
-constexpr uint32_t kProjStageBytes = kABoxBytes + 2 * kWBoxBytes;
-constexpr int kProjOffBar = kProjStages * kProjStageBytes;
-constexpr int kProjSmem = kProjOffBar + 8 * (2 * kProjStages + 2) + 16 + 1024;
-constexpr uint32_t kProjIdesc = idesc_bf16_f32(128, kProjBN, false, true);
-
-struct ProjParams {
-    void* c[3];
-    const float* bias[3];
-    int relu[3];
-    int M[3], N[3];
-    int K;
-    int tiles_n[3];
-    int tile_start[4];
-    int* err_word;
-};
-
-__global__ void __launch_bounds__(kThreads, 1)
-    proj_gemm_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant__ CUtensorMap a1,
-                     const __grid_constant__ CUtensorMap a2, const __grid_constant__ CUtensorMap w0,
-                     const __grid_constant__ CUtensorMap w1, const __grid_constant__ CUtensorMap w2,
-                     const ProjParams p)
-{
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const uint32_t sbase = smem_u32(smem);
-    const uint32_t sbar = sbase + kProjOffBar;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kProjOffBar + 8 * (2 * kProjStages + 2));
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-
-    const int tile = blockIdx.x;
-    const int prob = tile < p.tile_start[1] ? 0 : (tile < p.tile_start[2] ? 1 : 2);
-    const int local = tile - p.tile_start[prob];
-    const int tm = local / p.tiles_n[prob], tn = local % p.tiles_n[prob];
-    const CUtensorMap* am = prob == 0 ? &a0 : (prob == 1 ? &a1 : &a2);
-    const CUtensorMap* wm = prob == 0 ? &w0 : (prob == 1 ? &w1 : &w2);
-    const int kblocks = p.K / 64;
-
-    gemm_setup(sbar, kProjStages, tmem_slot, kProjBN, warp);
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t bar_acc = sbar + 8u * (2 * kProjStages);
-    const uint32_t bar_drain = bar_acc + 8u;
-
-    if (warp == kWarpLoad) {
-        if (lane == 0) {
-            int issued = 0;
-            bool ok = true;
-            for (int kb = 0; kb < kblocks; ++kb) {
-                const int s = kb % kProjStages;
-                const uint32_t ph = (kb / kProjStages) & 1;
-                if (!mbar_wait(sbar + 8u * (kProjStages + s), ph ^ 1)) { ok = false; break; }
-                const uint32_t full = sbar + 8u * s;
-                const uint32_t st = sbase + s * kProjStageBytes;
-                mbar_arrive_expect_tx(full, kProjStageBytes);
-                tma_load_2d(st, am, full, kb * 64, tm * 128);
-                tma_load_2d(st + kABoxBytes, wm, full, tn * kProjBN, kb * 64);
-                tma_load_2d(st + kABoxBytes + kWBoxBytes, wm, full, tn * kProjBN + 64, kb * 64);
-                ++issued;
-            }
-            if (!ok) raise_device_error(p.err_word, HATTN_ETIMEOUT);
-            for (int kb = max(0, issued - kProjStages); kb < issued; ++kb)
-                mbar_wait(sbar + 8u * (kb % kProjStages), (kb / kProjStages) & 1);
-        }
-    } else if (warp == kWarpMma) {
-        if (lane == 0) {
-            bool ok = true;
-            for (int kb = 0; kb < kblocks; ++kb) {
-                const int s = kb % kProjStages;
-                const uint32_t ph = (kb / kProjStages) & 1;
-                if (!mbar_wait(sbar + 8u * s, ph)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t st = sbase + s * kProjStageBytes;
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_ss(tmem, sdesc_sw128(st + ks * 32, 16, 1024),
-                           sdesc_sw128(st + kABoxBytes + ks * 2048, kWBoxBytes, 1024), kProjIdesc,
-                           (kb > 0 || ks > 0) ? 1u : 0u);
-                mma_commit(sbar + 8u * (kProjStages + s));
-            }
-            if (ok) mma_commit(bar_acc);
-            else raise_device_error(p.err_word, HATTN_ETIMEOUT);
-            mma_commit(bar_drain);
-            mbar_wait(bar_drain, 0);
-        }
-        __syncwarp();
-    } else {
-        const int wq = warp % 4;
-        const int row = tm * 128 + wq * 32 + lane;
-        bool got = mbar_wait(bar_acc, 0);
-        if (__all_sync(0xffffffffu, got)) {
-            tc_fence_after();
-            __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(p.c[prob]) + (size_t)row * p.N[prob];
-            const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-            const float* bias = p.bias[prob];
-            const bool relu = p.relu[prob] != 0;
-#pragma unroll
-            for (int c = 0; c < kProjBN / 32; ++c) {
-                uint32_t acc[32];
-                tmem_ld_x32(lane_base + 32 * c, acc);
-                const int col = tn * kProjBN + 32 * c;
-                if (bias && col < p.N[prob]) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        float v = __uint_as_float(acc[i]) + __ldg(bias + col + i);
-                        if (relu) v = fmaxf(v, 0.0f);
-                        acc[i] = __float_as_uint(v);
-                    }
-                } else if (relu) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[i] = __float_as_uint(fmaxf(__uint_as_float(acc[i]), 0.0f));
-                }
-                if (row < p.M[prob] && col < p.N[prob]) {
-#pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            w[i] = pack_bf16x2(__uint_as_float(acc[8 * v4 + 2 * i]),
-                                               __uint_as_float(acc[8 * v4 + 2 * i + 1]));
-                        st_global_v4(crow + col + 8 * v4, w[0], w[1], w[2], w[3]);
-                    }
-                }
-            }
-        } else {
-            raise_device_error(p.err_word, HATTN_ETIMEOUT);
-        }
-    }
-    gemm_teardown(tmem, kProjBN, warp);
-}
-
-// ------------------------------------------------------------------ out-projection + LayerNorm
-
-constexpr int kLnMaxN = 512;
-constexpr int kLnStages = 2;
-constexpr uint32_t kLnStageBytes = kABoxBytes + (kLnMaxN / 64) * kWBoxBytes;
-constexpr int kLnOffBar = kLnStages * kLnStageBytes;
-constexpr int kLnSmem = kLnOffBar + 8 * (2 * kLnStages + 2) + 16 + 1024;
-
-struct LnParams {
-    const __nv_bfloat16* x;
-    const float* bias;
+struct GemmParams {
+    GemmProblem prob[3];
+    int nprob;
+    int tiles;  // store: all (m, n) tiles of all problems; norm: row tiles
+    // norm epilogue
+    const __nv_bfloat16* x;  // residual [M][N]
     const float* gamma;
     const float* beta;
     float eps;
-    __nv_bfloat16* y;
-    int M, N, K;
+    int split;   // CTAs per row: 1, or 2 (a cluster pair, columns [0, n_half) and [n_half, N))
+    int n_half;
     int* err_word;
 };
 
+// Rows and columns one CTA covers for a tile.
+struct TileGeom {
+    int p;       // problem
+    int m0, n0;  // first row, first column
+    int bn;      // columns (a multiple of 64, <= 256)
+};
+
+template <bool kNorm>
+__device__ __forceinline__ TileGeom tile_geom(const GemmParams& p, int tile, uint32_t rank)
+{
+    TileGeom g;
+    if constexpr (kNorm) {
+        g.p = 0;
+        g.m0 = tile * kBM;
+        const int N = p.prob[0].N;
+        if (p.split == 2) {
+            g.n0 = rank ? p.n_half : 0;
+            g.bn = rank ? N - p.n_half : p.n_half;
+        } else {
+            g.n0 = 0;
+            g.bn = N;
+        }
+    } else {
+        int q = 0;
+        while (q + 1 < p.nprob && tile >= p.prob[q + 1].tile_begin) ++q;
+        const int local = tile - p.prob[q].tile_begin;
+        const int tm = local / p.prob[q].tiles_n, tn = local % p.prob[q].tiles_n;
+        g.p = q;
+        g.m0 = tm * kBM;
+        g.n0 = tn * kBN;
+        g.bn = min(kBN, p.prob[q].N - g.n0);
+    }
+    return g;
+}
+
+// This CTA's tiles: first, first + stride, ... (for a cluster pair both CTAs
+// take the same row tiles).
+struct TileRange {
+    int first, stride;
+};
+
+__device__ __forceinline__ TileRange tile_range(const GemmParams& p)
+{
+    if (p.split == 2) return {static_cast<int>(blockIdx.x / 2), static_cast<int>(gridDim.x / 2)};
+    return {static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x)};
+}
+
+__device__ __forceinline__ const CUtensorMap* pick(int i, const CUtensorMap* m0,
+                                                   const CUtensorMap* m1, const CUtensorMap* m2)
+{
+    return i == 0 ? m0 : (i == 1 ? m1 : m2);
+}
+
+__device__ __forceinline__ float ld_volatile_shared_f32(uint32_t addr)
+{
+    return __uint_as_float(ld_volatile_shared(addr));
+}
+
+// Sends this row's partial `v` to the peer CTA of the pair and returns the
+// peer's partial for the same row. Each exchange barrier completes once per
+// tile: the peer's next arrival on it needs this CTA's next exchange, which
+// happens only after this one has been read.
+__device__ __forceinline__ bool exchange_partial(float v, float& peer_v, uint32_t sbase,
+                                                 int stat_off, int bar_index, uint32_t parity,
+                                                 int r, uint32_t peer)
+{
+    const uint32_t slot = sbase + kOffStat + stat_off + 4u * r;
+    const uint32_t bar = sbase + kOffBar + 8u * bar_index;
+    st_cluster_f32(mapa_shared(slot, peer), v);
+    mbar_arrive_cluster(mapa_shared(bar, peer));
+    if (!mbar_wait_cluster(bar, parity)) return false;
+    peer_v = ld_volatile_shared_f32(slot);
+    return true;
+}
+
+template <bool kNorm>
 __global__ void __launch_bounds__(kThreads, 1)
-    outproj_ln_kernel(const __grid_constant__ CUtensorMap am, const __grid_constant__ CUtensorMap wm,
-                      const LnParams p)
+    gemm_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant__ CUtensorMap a1,
+                const __grid_constant__ CUtensorMap a2, const __grid_constant__ CUtensorMap w0,
+                const __grid_constant__ CUtensorMap w1, const __grid_constant__ CUtensorMap w2,
+                const __grid_constant__ GemmParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sbar = sbase + kLnOffBar;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kLnOffBar + 8 * (2 * kLnStages + 2));
+    const uint32_t sbar = sbase + kOffBar;
+    auto bar = [&](int i) { return sbar + 8u * i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffSlot);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int tm = blockIdx.x;
-    const int kblocks = p.K / 64;
-    const int nboxes = p.N / 64;
-    const uint32_t stage_tx = kABoxBytes + nboxes * kWBoxBytes;
+    const uint32_t rank = p.split == 2 ? cluster_ctarank() : 0u;
 
-    gemm_setup(sbar, kLnStages, tmem_slot, 512, warp);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar(kBarFull + s), 1);
+            mbar_init(bar(kBarEmpty + s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(kBarAccFull + b), 1);
+            mbar_init(bar(kBarAccEmpty + b), kEpiThreads / 32);
+        }
+        mbar_init(bar(kBarSum), kEpiThreads);
+        mbar_init(bar(kBarSq), kEpiThreads);
+        mbar_init(bar(kBarDrain), 1);
+        fence_barrier_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    if (warp == kWarpLoad && lane == 0) {
+        for (int i = 0; i < p.nprob; ++i) {
+            prefetch_tmap(pick(i, &a0, &a1, &a2));
+            prefetch_tmap(pick(i, &w0, &w1, &w2));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    // The peer's barriers must be initialised before any remote arrival.
+    if (p.split == 2) cluster_sync_all();
+    tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t bar_acc = sbar + 8u * (2 * kLnStages);
-    const uint32_t bar_drain = bar_acc + 8u;
+    const TileRange tr = tile_range(p);
 
     if (warp == kWarpLoad) {
         if (lane == 0) {
-            int issued = 0;
+            uint32_t it = 0;
             bool ok = true;
-            for (int kb = 0; kb < kblocks; ++kb) {
-                const int s = kb % kLnStages;
-                const uint32_t ph = (kb / kLnStages) & 1;
-                if (!mbar_wait(sbar + 8u * (kLnStages + s), ph ^ 1)) { ok = false; break; }
-                const uint32_t full = sbar + 8u * s;
-                const uint32_t st = sbase + s * kLnStageBytes;
-                mbar_arrive_expect_tx(full, stage_tx);
-                tma_load_2d(st, &am, full, kb * 64, tm * 128);
-                for (int x = 0; x < nboxes; ++x)
-                    tma_load_2d(st + kABoxBytes + x * kWBoxBytes, &wm, full, x * 64, kb * 64);
-                ++issued;
+            for (int t = tr.first; ok && t < p.tiles; t += tr.stride) {
+                const TileGeom g = tile_geom<kNorm>(p, t, rank);
+                const CUtensorMap* am = pick(g.p, &a0, &a1, &a2);
+                const CUtensorMap* wm = pick(g.p, &w0, &w1, &w2);
+                const int kblocks = p.prob[g.p].K / kBK;
+                const int nbox = g.bn / 64;
+                const uint32_t tx = kABoxBytes + nbox * kWBoxBytes;
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    const uint32_t s = it % kStages;
+                    if (!mbar_wait(bar(kBarEmpty + s), ((it / kStages) & 1) ^ 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t st = sbase + s * kStageBytes;
+                    mbar_arrive_expect_tx(bar(kBarFull + s), tx);
+                    tma_load_2d(st, am, bar(kBarFull + s), kb * kBK, g.m0);
+                    for (int j = 0; j < nbox; ++j)
+                        tma_load_2d(st + kABoxBytes + j * kWBoxBytes, wm, bar(kBarFull + s),
+                                    g.n0 + 64 * j, kb * kBK);
+                    ++it;
+                }
             }
             if (!ok) raise_device_error(p.err_word, HATTN_ETIMEOUT);
-            for (int kb = max(0, issued - kLnStages); kb < issued; ++kb)
-                mbar_wait(sbar + 8u * (kb % kLnStages), (kb / kLnStages) & 1);
+            // Every copy this CTA started must land before the CTA may exit.
+            for (uint32_t i = it > (uint32_t)kStages ? it - kStages : 0u; i < it; ++i)
+                mbar_wait(bar(kBarFull + i % kStages), (i / kStages) & 1);
         }
+        __syncwarp();
     } else if (warp == kWarpMma) {
         if (lane == 0) {
+            uint32_t it = 0, i = 0;
             bool ok = true;
-            for (int kb = 0; kb < kblocks; ++kb) {
-                const int s = kb % kLnStages;
-                const uint32_t ph = (kb / kLnStages) & 1;
-                if (!mbar_wait(sbar + 8u * s, ph)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t st = sbase + s * kLnStageBytes;
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint64_t a_desc = sdesc_sw128(st + ks * 32, 16, 1024);
-                    for (int n0 = 0; n0 < p.N; n0 += 256) {
-                        const int nn = min(256, p.N - n0);
-                        const uint32_t b_addr = st + kABoxBytes + (n0 / 64) * kWBoxBytes + ks * 2048;
-                        mma_ss(tmem + n0, a_desc, sdesc_sw128(b_addr, kWBoxBytes, 1024),
-                               idesc_bf16_f32(128, nn, false, true), (kb > 0 || ks > 0) ? 1u : 0u);
-                    }
+            for (int t = tr.first; ok && t < p.tiles; t += tr.stride, ++i) {
+                const TileGeom g = tile_geom<kNorm>(p, t, rank);
+                const int kblocks = p.prob[g.p].K / kBK;
+                const uint32_t b = i & 1;
+                if (!mbar_wait(bar(kBarAccEmpty + b), ((i >> 1) & 1) ^ 1)) {
+                    ok = false;
+                    break;
                 }
-                mma_commit(sbar + 8u * (kLnStages + s));
+                tc_fence_after();
+                const uint32_t d = tmem + 256u * b;
+                const uint32_t idesc = idesc_bf16_f32(128, g.bn, false, true);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    const uint32_t s = it % kStages;
+                    if (!mbar_wait(bar(kBarFull + s), (it / kStages) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t st = sbase + s * kStageBytes;
+#pragma unroll
+                    for (int ks = 0; ks < kBK / 16; ++ks)
+                        mma_ss(d, sdesc_sw128(st + ks * 32, 16, 1024),
+                               sdesc_sw128(st + kABoxBytes + ks * 2048, kWBoxBytes, 1024), idesc,
+                               (kb > 0 || ks > 0) ? 1u : 0u);
+                    mma_commit(bar(kBarEmpty + s));
+                    ++it;
+                }
+                if (ok) mma_commit(bar(kBarAccFull + b));
             }
-            if (ok) mma_commit(bar_acc);
-            else raise_device_error(p.err_word, HATTN_ETIMEOUT);
-            mma_commit(bar_drain);
-            mbar_wait(bar_drain, 0);
+            if (!ok) raise_device_error(p.err_word, HATTN_ETIMEOUT);
+            // All issued MMAs must complete before TMEM is released.
+            mma_commit(bar(kBarDrain));
+            mbar_wait(bar(kBarDrain), 0);
         }
         __syncwarp();
     } else {
-        const int wq = warp % 4;
-        const int row = tm * 128 + wq * 32 + lane;
-        const bool valid = row < p.M;
-        bool got = mbar_wait(bar_acc, 0);
-        if (__all_sync(0xffffffffu, got)) {
+        const int q = warp % 4;  // TMEM lane quadrant this warp may access
+        const int r = q * 32 + lane;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        const uint32_t peer = rank ^ 1u;
+        uint32_t i = 0;
+        bool ok = true;
+        for (int t = tr.first; ok && t < p.tiles; t += tr.stride, ++i) {
+            const TileGeom g = tile_geom<kNorm>(p, t, rank);
+            const GemmProblem& pr = p.prob[g.p];
+            const uint32_t b = i & 1;
+            {
+                const bool got = mbar_wait(bar(kBarAccFull + b), (i >> 1) & 1);
+                ok = __all_sync(0xffffffffu, got);
+            }
+            if (!ok) break;
             tc_fence_after();
-            const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-            const __nv_bfloat16* xrow = p.x + (size_t)row * p.N;
-            const int nchunks = p.N / 32;
-            // Pass 1: z = acc + x (kept in TMEM), row sum.
-            float sum = 0.0f;
-            for (int c = 0; c < nchunks; ++c) {
-                uint32_t z[32];
-                tmem_ld_x32(lane_base + 32 * c, z);
-                uint4 xv[4] = {};
-                if (valid) {
-                    const uint4* src = reinterpret_cast<const uint4*>(xrow + 32 * c);
+            const uint32_t acc = lane_base + 256u * b;
+            const int row = g.m0 + r;
+            const bool valid = row < pr.M;
+            const int nchunks = g.bn / 32;
+            if constexpr (!kNorm) {
+                __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(pr.c) + (size_t)row * pr.N + g.n0;
+                const bool relu = pr.relu != 0;
+                for (int c = 0; c < nchunks; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_x32(acc + 32 * c, v);
+                    if (pr.bias) {
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) xv[v4] = src[v4];
-                }
-                const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(xv);
-                if (p.bias) {
+                        for (int e = 0; e < 32; ++e)
+                            v[e] = __float_as_uint(__uint_as_float(v[e]) + __ldg(pr.bias + g.n0 + 32 * c + e));
+                    }
+                    if (relu) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        z[i] = __float_as_uint(__uint_as_float(z[i]) + __ldg(p.bias + 32 * c + i));
-                }
+                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(fmaxf(__uint_as_float(v[e]), 0.0f));
+                    }
+                    if (valid) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float zi = __uint_as_float(z[i]) + __bfloat162float(xb[i]);
-                    sum += zi;
-                    z[i] = __float_as_uint(zi);
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            st_global_v4(crow + 32 * c + 8 * v4,
+                                         pack_bf16x2(__uint_as_float(v[8 * v4]), __uint_as_float(v[8 * v4 + 1])),
+                                         pack_bf16x2(__uint_as_float(v[8 * v4 + 2]), __uint_as_float(v[8 * v4 + 3])),
+                                         pack_bf16x2(__uint_as_float(v[8 * v4 + 4]), __uint_as_float(v[8 * v4 + 5])),
+                                         pack_bf16x2(__uint_as_float(v[8 * v4 + 6]), __uint_as_float(v[8 * v4 + 7])));
+                    }
                 }
-                tmem_st_x32(lane_base + 32 * c, z);
+            } else {
+                const int N = pr.N;
+                const __nv_bfloat16* xrow = p.x + (size_t)row * N + g.n0;
+                // Pass 1: z = acc [+ bias] + x, kept in TMEM; partial row sum.
+                float sum = 0.0f;
+                for (int c = 0; c < nchunks; ++c) {
+                    uint32_t z[32];
+                    tmem_ld_x32(acc + 32 * c, z);
+                    uint4 xv[4] = {};
+                    if (valid) {
+                        const uint4* src = reinterpret_cast<const uint4*>(xrow + 32 * c);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4) xv[v4] = src[v4];
+                    }
+                    const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(xv);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        float zi = __uint_as_float(z[e]) + __bfloat162float(xb[e]);
+                        if (pr.bias) zi += __ldg(pr.bias + g.n0 + 32 * c + e);
+                        sum += zi;
+                        z[e] = __float_as_uint(zi);
+                    }
+                    tmem_st_x32(acc + 32 * c, z);
+                }
+                tmem_st_wait();
+                if (p.split == 2) {
+                    float other = 0.0f;
+                    const bool got = exchange_partial(sum, other, sbase, 0, kBarSum, i & 1, r, peer);
+                    ok = __all_sync(0xffffffffu, got);
+                    sum += other;
+                }
+                const float mean = sum / static_cast<float>(N);
+                // Pass 2: biased variance about the mean.
+                float sq = 0.0f;
+                for (int c = 0; ok && c < nchunks; ++c) {
+                    uint32_t z[32];
+                    tmem_ld_x32(acc + 32 * c, z);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float dz = __uint_as_float(z[e]) - mean;
+                        sq = fmaf(dz, dz, sq);
+                    }
+                }
+                if (ok && p.split == 2) {
+                    float other = 0.0f;
+                    const bool got = exchange_partial(sq, other, sbase, 4 * kBM, kBarSq, i & 1, r, peer);
+                    ok = __all_sync(0xffffffffu, got);
+                    sq += other;
+                }
+                const float rstd = 1.0f / sqrtf(sq / static_cast<float>(N) + p.eps);
+                // Pass 3: normalise, scale, shift, round once to bf16.
+                __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(pr.c) + (size_t)row * N + g.n0;
+                for (int c = 0; ok && c < nchunks; ++c) {
+                    uint32_t z[32];
+                    tmem_ld_x32(acc + 32 * c, z);
+                    uint32_t w[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int col = g.n0 + 32 * c + 2 * e;
+                        const float y0 = (__uint_as_float(z[2 * e]) - mean) * rstd * __ldg(p.gamma + col) +
+                                         __ldg(p.beta + col);
+                        const float y1 = (__uint_as_float(z[2 * e + 1]) - mean) * rstd *
+                                             __ldg(p.gamma + col + 1) + __ldg(p.beta + col + 1);
+                        w[e] = pack_bf16x2(y0, y1);
+                    }
+                    if (valid) {
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            st_global_v4(yrow + 32 * c + 8 * v4, w[4 * v4], w[4 * v4 + 1],
+                                         w[4 * v4 + 2], w[4 * v4 + 3]);
+                    }
+                }
+                if (!ok) break;
             }
-            tmem_st_wait();
-            const float mean = sum / static_cast<float>(p.N);
-            // Pass 2: biased variance about the mean.
-            float var = 0.0f;
-            for (int c = 0; c < nchunks; ++c) {
-                uint32_t z[32];
-                tmem_ld_x32(lane_base + 32 * c, z);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float dz = __uint_as_float(z[i]) - mean;
-                    var = fmaf(dz, dz, var);
-                }
-            }
-            const float rstd = 1.0f / sqrtf(var / static_cast<float>(p.N) + p.eps);
-            // Pass 3: normalise, scale, shift, round once to bf16.
-            __nv_bfloat16* yrow = p.y + (size_t)row * p.N;
-            for (int c = 0; c < nchunks; ++c) {
-                uint32_t z[32];
-                tmem_ld_x32(lane_base + 32 * c, z);
-                uint32_t w[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int col = 32 * c + 2 * i;
-                    const float y0 = (__uint_as_float(z[2 * i]) - mean) * rstd * __ldg(p.gamma + col) +
-                                     __ldg(p.beta + col);
-                    const float y1 = (__uint_as_float(z[2 * i + 1]) - mean) * rstd *
-                                         __ldg(p.gamma + col + 1) + __ldg(p.beta + col + 1);
-                    w[i] = pack_bf16x2(y0, y1);
-                }
-                if (valid) {
-#pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4)
-                        st_global_v4(yrow + 32 * c + 8 * v4, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
-                                     w[4 * v4 + 3]);
-                }
-            }
-        } else {
-            raise_device_error(p.err_word, HATTN_ETIMEOUT);
+            // The accumulator has been read: the MMA warp may reuse it.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarAccEmpty + b));
         }
+        if (!ok) raise_device_error(p.err_word, HATTN_ETIMEOUT);
     }
-    gemm_teardown(tmem, 512, warp);
+
+    tc_fence_before();
+    __syncthreads();
+    // No CTA of a pair may exit while its peer can still reach its shared memory.
+    if (p.split == 2) cluster_sync_all();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+int sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 152;
+    return n;
+}
+
+template <bool kNorm>
+cudaError_t launch(const CUtensorMap* a, const CUtensorMap* w, const GemmParams& p, int grid,
+                   int cluster, cudaStream_t stream)
+{
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<kNorm>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<kNorm>, a[0], a[1], a[2], w[0], w[1], w[2], p);
 }
 
 }  // namespace
@@ -380,52 +455,61 @@ cudaError_t launch_proj_gemm(const ProjProblem* problems, int count, cudaStream_
                              int* err_word)
 {
     if (count < 1 || count > 3) return cudaErrorInvalidValue;
-    ProjParams p{};
-    p.K = problems[0].K;
+    GemmParams p{};
+    p.nprob = count;
+    p.split = 1;
     p.err_word = err_word;
-    p.tile_start[0] = 0;
+    CUtensorMap a[3], w[3];
+    int tiles = 0;
     for (int i = 0; i < 3; ++i) {
         const ProjProblem& pr = problems[i < count ? i : count - 1];
-        if (pr.K != p.K || pr.K % 64 != 0 || pr.N % 64 != 0) return cudaErrorInvalidValue;
-        p.c[i] = pr.c;
-        p.bias[i] = pr.bias;
-        p.relu[i] = pr.relu ? 1 : 0;
-        p.M[i] = pr.M;
-        p.N[i] = pr.N;
-        p.tiles_n[i] = (pr.N + kProjBN - 1) / kProjBN;
-        const int tiles = i < count ? ((pr.M + 127) / 128) * p.tiles_n[i] : 0;
-        p.tile_start[i + 1] = p.tile_start[i] + tiles;
+        if (i < count && (pr.K % kBK != 0 || pr.N % 64 != 0 || pr.M <= 0 || pr.K <= 0))
+            return cudaErrorInvalidValue;
+        a[i] = pr.a;
+        w[i] = pr.w;
+        GemmProblem& g = p.prob[i];
+        g.c = pr.c;
+        g.bias = pr.bias;
+        g.relu = pr.relu ? 1 : 0;
+        g.M = pr.M;
+        g.N = pr.N;
+        g.K = pr.K;
+        g.tiles_n = (pr.N + kBN - 1) / kBN;
+        g.tile_begin = tiles;
+        if (i < count) tiles += ((pr.M + kBM - 1) / kBM) * g.tiles_n;
     }
-    cudaError_t e = cudaFuncSetAttribute(proj_gemm_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kProjSmem);
-    if (e != cudaSuccess) return e;
-    const ProjProblem& q0 = problems[0];
-    const ProjProblem& q1 = problems[count > 1 ? 1 : 0];
-    const ProjProblem& q2 = problems[count > 2 ? 2 : 0];
-    proj_gemm_kernel<<<p.tile_start[3], kThreads, kProjSmem, stream>>>(q0.a, q1.a, q2.a, q0.w,
-                                                                      q1.w, q2.w, p);
-    return cudaGetLastError();
+    p.tiles = tiles;
+    const int grid = std::min(tiles, sm_count());
+    return launch<false>(a, w, p, grid, 1, stream);
 }
 
-cudaError_t launch_outproj_ln(const OutProjLnArgs& a, cudaStream_t stream, int* err_word)
+cudaError_t launch_outproj_ln(const OutProjLnArgs& args, cudaStream_t stream, int* err_word)
 {
-    if (a.N % 64 != 0 || a.N > kLnMaxN || a.K % 64 != 0) return cudaErrorInvalidValue;
-    LnParams p;
-    p.x = static_cast<const __nv_bfloat16*>(a.x);
-    p.bias = a.bias;
-    p.gamma = a.gamma;
-    p.beta = a.beta;
-    p.eps = a.eps;
-    p.y = static_cast<__nv_bfloat16*>(a.y);
-    p.M = a.M;
-    p.N = a.N;
-    p.K = a.K;
+    const int N = args.N;
+    if (N % 64 != 0 || N > 2 * kBN || args.K % kBK != 0 || args.M <= 0 || args.K <= 0)
+        return cudaErrorInvalidValue;
+    GemmParams p{};
+    p.nprob = 1;
     p.err_word = err_word;
-    cudaError_t e = cudaFuncSetAttribute(outproj_ln_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kLnSmem);
-    if (e != cudaSuccess) return e;
-    outproj_ln_kernel<<<(a.M + 127) / 128, kThreads, kLnSmem, stream>>>(a.a, a.wo, p);
-    return cudaGetLastError();
+    GemmProblem& g = p.prob[0];
+    g.c = args.y;
+    g.bias = args.bias;
+    g.M = args.M;
+    g.N = N;
+    g.K = args.K;
+    p.x = static_cast<const __nv_bfloat16*>(args.x);
+    p.gamma = args.gamma;
+    p.beta = args.beta;
+    p.eps = args.eps;
+    p.split = N > kBN ? 2 : 1;
+    p.n_half = ((N / 2 + 63) / 64) * 64;
+    p.tiles = (args.M + kBM - 1) / kBM;
+    const CUtensorMap a[3] = {args.a, args.a, args.a};
+    const CUtensorMap w[3] = {args.wo, args.wo, args.wo};
+    int grid;
+    if (p.split == 2) grid = 2 * std::min(p.tiles, sm_count() / 2);
+    else grid = std::min(p.tiles, sm_count());
+    return launch<true>(a, w, p, grid, p.split, stream);
 }
 
 }  // namespace hattn
