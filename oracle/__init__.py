@@ -81,6 +81,8 @@ def _load():
         lib.oracle_pos_encoding.restype = c_int
         lib.oracle_ffn.argtypes = [dp] * 7 + [c_double, dp, c_int, c_int, c_int, c_int]
         lib.oracle_ffn.restype = c_int
+        lib.oracle_attn_bwd.argtypes = [dp] * 4 + [c_int] * 6 + [c_double, c_int, ip] + [dp] * 4
+        lib.oracle_attn_bwd.restype = c_int
         _lib = lib
         return lib
 
@@ -266,3 +268,20 @@ def ffn(x, w1, b1, w2, b2, gamma, beta, eps, nthreads=0) -> np.ndarray:
                         float(eps), _dp(y), x2.shape[0], d_model, d_ff, int(nthreads))
     _check(rc, "oracle_ffn")
     return y.reshape(shape)
+
+
+def attn_bwd(q, k, v, dout, scale, mask_kind=MASK_NONE, key_lens=None):
+    """Gradients (dq, dk, dv) of sum(dout * attn(q, k, v)) and the forward's per-row
+    log-sum-exp lse [B, h, n_q] (natural log of sum_j exp(scale q.k_j) over visible keys)."""
+    lib = _load()
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, n_q, h, d_k = q.shape
+    n_k, d_v = k.shape[1], v.shape[3]
+    dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    lse = np.empty((B, h, n_q), dtype=np.float64)
+    kl = _keylens(key_lens, mask_kind)
+    rc = lib.oracle_attn_bwd(_dp(q), _dp(k), _dp(v), _dp(dout), B, h, n_q, n_k, d_k, d_v,
+                             float(scale), int(mask_kind), _ip(kl), _dp(dq), _dp(dk), _dp(dv),
+                             _dp(lse))
+    _check(rc, "oracle_attn_bwd")
+    return dq, dk, dv, lse

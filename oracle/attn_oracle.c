@@ -452,3 +452,98 @@ int oracle_ffn(const double* x, const double* W1, const double* b1, const double
     }
     return rc;
 }
+
+/*
+ * Gradients of multi-head attention, and the per-row log-sum-exp of the
+ * forward pass.
+ *
+ * Training sends the loss gradient back through the attention weights and the
+ * projections ([hex4c59, §参数是怎样学出来的？]; all target positions are trained
+ * at once under the causal mask, §训练能并行，不意味着一次生成整句话). The pages
+ * print no backward formulas; these are the chain rule applied to the forward
+ * definition above, per (batch, head) and query row i:
+ *   s_ij  = scale * q_i . k_j            (visible keys only)
+ *   P_ij  = softmax_j(s_ij)              (0 for invisible keys)
+ *   O_i   = sum_j P_ij v_j
+ * with upstream gradient dO:
+ *   dV_j  = sum_i P_ij dO_i
+ *   dP_ij = dO_i . v_j
+ *   dS_ij = P_ij (dP_ij - sum_k P_ik dP_ik)      (softmax Jacobian)
+ *   dQ_i  = scale * sum_j dS_ij k_j
+ *   dK_j  = scale * sum_i dS_ij q_i
+ * lse (optional, [B, h, n_q]) receives ln sum_j exp(s_ij) over visible keys.
+ * Layouts as oracle_attn; dq/dk/dv have the shapes of q/k/v.
+ */
+int oracle_attn_bwd(const double* q, const double* k, const double* v, const double* dout,
+                    int B, int h, int n_q, int n_k, int d_k, int d_v, double scale, int mask_kind,
+                    const int32_t* key_lens, double* dq, double* dk, double* dv, double* lse)
+{
+    int rc = check_attn_args(B, h, n_q, n_k, d_k, d_v, mask_kind, key_lens);
+    if (rc != ORACLE_OK) return rc;
+    const int causal = (mask_kind & ORACLE_MASK_CAUSAL) != 0;
+    memset(dq, 0, sizeof(double) * (size_t)B * n_q * h * d_k);
+    memset(dk, 0, sizeof(double) * (size_t)B * n_k * h * d_k);
+    memset(dv, 0, sizeof(double) * (size_t)B * n_k * h * d_v);
+    double* s = (double*)malloc(sizeof(double) * (size_t)n_k);
+    double* w = (double*)malloc(sizeof(double) * (size_t)n_k);
+    double* dp = (double*)malloc(sizeof(double) * (size_t)n_k);
+    unsigned char* vis = (unsigned char*)malloc((size_t)n_k);
+    if (!s || !w || !dp || !vis) {
+        rc = ORACLE_ENOMEM;
+        goto done;
+    }
+    for (int b = 0; b < B; ++b) {
+        const int kv_len = (mask_kind & ORACLE_MASK_KEY_PADDING) ? key_lens[b] : n_k;
+        for (int i = 0; i < h; ++i) {
+            for (int t = 0; t < n_q; ++t) {
+                const double* q_row = q + (((size_t)b * n_q + t) * h + i) * d_k;
+                const double* do_row = dout + (((size_t)b * n_q + t) * h + i) * d_v;
+                for (int j = 0; j < n_k; ++j) {
+                    const double* k_row = k + (((size_t)b * n_k + j) * h + i) * d_k;
+                    double dot = 0.0;
+                    for (int c = 0; c < d_k; ++c) dot += q_row[c] * k_row[c];
+                    s[j] = scale * dot;
+                    vis[j] = (unsigned char)(!(causal && j > t) && j < kv_len);
+                }
+                rc = oracle_softmax(s, vis, n_k, w);
+                if (rc != ORACLE_OK) goto done;
+                if (lse) {
+                    double m = -INFINITY;
+                    for (int j = 0; j < n_k; ++j)
+                        if (vis[j] && s[j] > m) m = s[j];
+                    double sum = 0.0;
+                    for (int j = 0; j < n_k; ++j)
+                        if (vis[j]) sum += exp(s[j] - m);
+                    lse[((size_t)b * h + i) * n_q + t] = m + log(sum);
+                }
+                double pdp = 0.0;
+                for (int j = 0; j < n_k; ++j) {
+                    dp[j] = 0.0;
+                    if (!vis[j]) continue;
+                    const double* v_row = v + (((size_t)b * n_k + j) * h + i) * d_v;
+                    for (int c = 0; c < d_v; ++c) dp[j] += do_row[c] * v_row[c];
+                    pdp += w[j] * dp[j];
+                }
+                double* dq_row = dq + (((size_t)b * n_q + t) * h + i) * d_k;
+                for (int j = 0; j < n_k; ++j) {
+                    if (!vis[j]) continue;
+                    const double ds = w[j] * (dp[j] - pdp);
+                    const double* k_row = k + (((size_t)b * n_k + j) * h + i) * d_k;
+                    double* dk_row = dk + (((size_t)b * n_k + j) * h + i) * d_k;
+                    double* dv_row = dv + (((size_t)b * n_k + j) * h + i) * d_v;
+                    for (int c = 0; c < d_k; ++c) {
+                        dq_row[c] += scale * ds * k_row[c];
+                        dk_row[c] += scale * ds * q_row[c];
+                    }
+                    for (int c = 0; c < d_v; ++c) dv_row[c] += w[j] * do_row[c];
+                }
+            }
+        }
+    }
+done:
+    free(s);
+    free(w);
+    free(dp);
+    free(vis);
+    return rc;
+}

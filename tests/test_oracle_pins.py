@@ -476,3 +476,108 @@ def test_encoder_layer_reduction():
     y = oracle.ffn(y1, _rand(rng, dm, 16), _rand(rng, 16), np.zeros((16, dm)), np.zeros(dm), g, b0,
                    1e-6)
     np.testing.assert_allclose(y, oracle.layernorm(x, g, b0, 1e-6), atol=1e-5)
+
+
+# ---------------------------------------------------------------- attention backward
+
+def _fwd_objective(q, k, v, dout, scale, mask_kind, kl):
+    return float(np.sum(dout * oracle.attn(q, k, v, scale, mask_kind, kl)))
+
+
+@pytest.mark.parametrize("mask_kind", [0, 1, 2, 3])
+def test_attn_bwd_matches_finite_differences(mask_kind):
+    """Central differences of <dO, Attention(Q, K, V)> through the pinned forward
+    oracle: an independent check of every term of the chain rule (a dropped
+    softmax-Jacobian term, a sign or a transposed operand fails it)."""
+    rng = np.random.default_rng(31 + mask_kind)
+    B, n, h, dk_, dv_ = 2, 5, 2, 3, 4
+    q, k = _rand(rng, B, n, h, dk_), _rand(rng, B, n, h, dk_)
+    v, dout = _rand(rng, B, n, h, dv_), _rand(rng, B, n, h, dv_)
+    kl = np.array([3, 5], dtype=np.int32) if mask_kind & 2 else None
+    scale = 0.7
+    dq, dk, dv, _ = oracle.attn_bwd(q, k, v, dout, scale, mask_kind, kl)
+    eps = 1e-6
+    for name, arr, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        fd = np.zeros_like(arr)
+        it = np.nditer(arr, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            plus, minus = arr.copy(), arr.copy()
+            plus[idx] += eps
+            minus[idx] -= eps
+            args = {"q": q, "k": k, "v": v}
+            args[name] = plus
+            fp = _fwd_objective(args["q"], args["k"], args["v"], dout, scale, mask_kind, kl)
+            args[name] = minus
+            fm = _fwd_objective(args["q"], args["k"], args["v"], dout, scale, mask_kind, kl)
+            fd[idx] = (fp - fm) / (2 * eps)
+        np.testing.assert_allclose(grad, fd, rtol=0, atol=2e-8, err_msg=name)
+
+
+@pytest.mark.parametrize("mask_kind", [0, 1, 2])
+def test_attn_bwd_against_torch_autograd(mask_kind):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(41)
+    B, n_q, n_k, h, d = 2, 6, 6 if mask_kind & 1 else 9, 3, 4
+    q, k, v = _rand(rng, B, n_q, h, d), _rand(rng, B, n_k, h, d), _rand(rng, B, n_k, h, d)
+    dout = _rand(rng, B, n_q, h, d)
+    kl = np.array([4, n_k], dtype=np.int32) if mask_kind & 2 else None
+    scale = 0.5
+    dq, dk, dv, lse = oracle.attn_bwd(q, k, v, dout, scale, mask_kind, kl)
+    Q, K, V = (torch.from_numpy(a.transpose(0, 2, 1, 3).copy()).requires_grad_() for a in (q, k, v))
+    s = Q @ K.transpose(-1, -2) * scale
+    bias = torch.zeros(B, 1, n_q, n_k, dtype=torch.float64)
+    if mask_kind & 1:
+        bias = bias + torch.triu(torch.full((n_q, n_k), float("-inf"), dtype=torch.float64), 1)
+    if mask_kind & 2:
+        for b in range(B):
+            bias[b, :, :, int(kl[b]):] = float("-inf")
+    O = torch.softmax(s + bias, -1) @ V
+    O.backward(torch.from_numpy(dout.transpose(0, 2, 1, 3).copy()))
+    back = lambda t: t.grad.numpy().transpose(0, 2, 1, 3)
+    np.testing.assert_allclose(dq, back(Q), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk, back(K), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv, back(V), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, torch.logsumexp(s + bias, -1).detach().numpy(), rtol=0, atol=1e-12)
+
+
+def test_attn_bwd_invariants_and_closed_forms():
+    rng = np.random.default_rng(42)
+    B, n, h, d = 2, 7, 2, 5
+    q, k, v, dout = (_rand(rng, B, n, h, d) for _ in range(4))
+    kl = np.array([4, 7], dtype=np.int32)
+    dq, dk, dv, lse = oracle.attn_bwd(q, k, v, dout, 0.4, 2, kl)
+    # Shifting every key of a head by one vector shifts each score row by a constant:
+    # the softmax ignores it, so the key gradients of a head sum to zero.
+    np.testing.assert_allclose(dk.sum(axis=1), 0.0, atol=1e-12)
+    # Each weight row sums to 1, so the value gradients sum to the output gradients.
+    np.testing.assert_allclose(dv.sum(axis=1), dout.sum(axis=1), atol=1e-12)
+    # Padded keys receive no gradient.
+    assert np.all(dk[0, 4:] == 0.0) and np.all(dv[0, 4:] == 0.0)
+    # One key: O = v_1 whatever q and k are, so dQ = dK = 0 and dV = sum of dO.
+    dq1, dk1, dv1, lse1 = oracle.attn_bwd(q, k[:, :1], v[:, :1], dout, 0.4)
+    assert np.all(dq1 == 0.0) and np.all(dk1 == 0.0)
+    np.testing.assert_allclose(dv1[:, 0], dout.sum(axis=1), atol=1e-12)
+    np.testing.assert_allclose(lse1, 0.4 * np.einsum("bthc,bhc->bht", q, k[:, 0]), atol=1e-12)
+    # Causal: key j only receives gradient from queries t >= j (the last key only from the last query).
+    dqc, dkc, dvc, _ = oracle.attn_bwd(q, k, v, dout, 0.4, 1)
+    # ...so dV of the last key is the last query's weight on it times that query's dO.
+    sel = [(b, n - 1, i) for b in range(B) for i in range(h)]
+    _, wts = oracle.attn_rows(q, k, v, 0.4, sel, 1, weights=True)
+    for r, (b, t, i) in enumerate(sel):
+        np.testing.assert_allclose(dvc[b, n - 1, i], wts[r, n - 1] * dout[b, n - 1, i], atol=1e-13)
+    dout2 = dout.copy()
+    dout2[:, n - 1] = 0.0
+    _, dk2, dv2, _ = oracle.attn_bwd(q, k, v, dout2, 0.4, 1)
+    assert np.all(dv2[:, n - 1] == 0.0) and np.all(dk2[:, n - 1] == 0.0)
+
+
+def test_attn_lse_brute_force():
+    rng = np.random.default_rng(43)
+    q, k, v = (_rand(rng, 1, 4, 1, 3) for _ in range(3))
+    _, _, _, lse = oracle.attn_bwd(q, k, v, np.zeros_like(v), 0.9, 1)
+    for t in range(4):
+        scores = [0.9 * math.fsum(q[0, t, 0] * k[0, j, 0]) for j in range(t + 1)]
+        top = max(scores)
+        ref = top + math.log(math.fsum(math.exp(s - top) for s in scores))
+        assert abs(lse[0, 0, t] - ref) < 1e-13
