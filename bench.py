@@ -51,11 +51,16 @@ if ROOT not in sys.path:
 
 METRIC = "attention fwd TFLOP/s and % of GB300 BF16 tensor peak (1 GPU); tokens/s"
 PE_METRIC = "positional encoding GB/s (HBM-bound elementwise)"
+BWD_METRIC = "attention backward TFLOP/s (2.5x the forward's FLOPs; 1 GPU)"
 
 
 def metric_of(w):
     """(metric, unit) of a workload's bench line."""
-    return (PE_METRIC, "GB/s") if w.kind == "pe" else (METRIC, "TFLOP/s")
+    if w.kind == "pe":
+        return (PE_METRIC, "GB/s")
+    if w.kind == "bwd":
+        return (BWD_METRIC, "TFLOP/s")
+    return (METRIC, "TFLOP/s")
 DEFAULT_WORKLOAD = "long_causal_d128"
 NOMINAL_BF16_TFLOPS = 2250.0
 NOMINAL_HBM_GBS = 8000.0
@@ -362,6 +367,31 @@ def oracle_layer_sample_rate(w, inp, budget_s: float, sample_index: int = 0):
     return done * per_elem / elapsed / 1e12, threads, desc
 
 
+def oracle_bwd_sample_rate(w, inp, budget_s: float, sample_index: int = 0):
+    """Times the oracle's attention backward on whole (batch, head) units until about
+    budget_s seconds of work; returns (TFLOP/s at the backward's defined count of 2.5x
+    the forward's visible-pair FLOPs, threads, description). The oracle runs one thread."""
+    import oracle
+    from synth import inputs as synth
+    n_units = w.B * w.h
+    done, flops, elapsed = 0, 0.0, 0.0
+    while elapsed < budget_s and done < n_units:
+        u = (sample_index + done) % n_units
+        b, i = u % w.B, u // w.B
+        q, k, v = _head_arrays(inp, w, b, i)
+        g = synth.widen(inp["dout"][b:b + 1, :, i:i + 1].copy(), w.dtype)
+        kl = None if inp.get("key_lens") is None else inp["key_lens"][b:b + 1]
+        kv_len = int(kl[0]) if kl is not None else w.n_k
+        t0 = time.perf_counter()
+        oracle.attn_bwd(q, k, v, g, w.scale, w.mask_kind, kl)
+        elapsed += time.perf_counter() - t0
+        flops += 2.5 * _rows_flops(w, range(w.n_q), kv_len)
+        done += 1
+    desc = (f"{done} of {n_units} (batch, head) units, single-threaded; {flops / 1e9:.2f} GFLOP "
+            f"(2.5x the forward's visible pairs) in {elapsed:.2f} s")
+    return flops / elapsed / 1e12, 1, desc
+
+
 def pe_inputs(w):
     from synth import inputs as synth
     return {"emb": synth.round_to_bf16_bits(synth.draw_normal(w.seed, 0, (w.B, w.n_q, w.d_model)))}
@@ -373,6 +403,8 @@ def workload_inputs(w):
         return pe_inputs(w)
     if w.kind in ("encoder", "decoder"):
         return synth.layer_inputs(w)
+    if w.kind == "bwd":
+        return synth.attn_bwd_inputs(w)
     return synth.mha_inputs(w) if w.kind == "mha" else synth.attn_inputs(w)
 
 
@@ -389,6 +421,8 @@ def sample_rate(w, inp, budget_s: float, sample_index: int = 0):
         return oracle_pe_sample_rate(w, inp, budget_s, sample_index)
     if w.kind in ("encoder", "decoder"):
         return oracle_layer_sample_rate(w, inp, budget_s, sample_index)
+    if w.kind == "bwd":
+        return oracle_bwd_sample_rate(w, inp, budget_s, sample_index)
     if w.is_mha:
         return oracle_mha_sample_rate(w, inp, budget_s, sample_index)
     return oracle_sample_rate(w, inp, budget_s, sample_index)
@@ -519,6 +553,27 @@ def _setup_layer(w, inp):
     return step, {"inputs": host_inputs, "output": y}, launches
 
 
+def _setup_bwd(w, inp):
+    """Device tensors, the forward's output and log-sum-exp, workspace and a step closure
+    for one attn_bwd call (three kernel launches)."""
+    import torch
+
+    import head_attention_gb300 as hattn
+    q, k, v, g = (_device_array(inp[n], w.dtype) for n in ("q", "k", "v", "dout"))
+    kl = None if inp["key_lens"] is None else torch.from_numpy(inp["key_lens"]).cuda()
+    out, lse = hattn.attn_fwd_lse(q, k, v, scale=w.scale, mask_kind=w.mask_kind, key_lens=kl)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(hattn.attn_bwd_workspace_bytes(w.B, w.h, w.n_q), dtype=torch.uint8,
+                     device="cuda")
+
+    def step():
+        hattn.attn_bwd(q, k, v, out, g, lse, scale=w.scale, mask_kind=w.mask_kind, key_lens=kl,
+                       dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    host = {"inputs": {"dout": (inp["dout"], g)}, "output": dq}
+    return step, host, 3
+
+
 def run_gpu(args, rank, world, local):
     import torch
 
@@ -540,6 +595,10 @@ def run_gpu(args, rank, world, local):
         inp = synth.attn_inputs(w)
         step, host, launches_per_step = _setup_decode(w, inp)
         flops = 4.0 * w.h * w.d_k * float(inp["key_lens"].sum())  # visible (query, key) pairs
+    elif w.kind == "bwd":
+        inp = synth.attn_bwd_inputs(w)
+        step, host, launches_per_step = _setup_bwd(w, inp)
+        flops = 2.5 * w.attn_flops()  # five n_q x n_k x d contractions against the forward's two
     elif w.kind in ("encoder", "decoder"):
         inp = synth.layer_inputs(w)
         step, host, launches_per_step = _setup_layer(w, inp)
@@ -605,6 +664,10 @@ def run_gpu(args, rank, world, local):
         acts = w.B * w.n_q * w.d_model + (w.B * w.n_k * w.d_model if w.kind == "decoder" else 0)
         bytes_in = (acts + weights) * esize
         bytes_alg = bytes_in + w.B * w.n_q * w.d_model * esize
+    elif w.kind == "bwd":
+        qkv = w.B * (w.n_q * w.h * w.d_k + w.n_k * w.h * (w.d_k + w.d_v))
+        bytes_in = (qkv + 2 * w.B * w.n_q * w.h * w.d_v) * esize + 4 * w.B * w.h * w.n_q
+        bytes_alg = bytes_in + qkv * esize
     elif w.kind == "decode":
         bytes_in = (float(inp["key_lens"].sum()) * w.h * (w.d_k + w.d_v) + w.B * w.h * w.d_k) * esize
         bytes_alg = bytes_in + w.B * w.h * w.d_v * esize
@@ -619,28 +682,47 @@ def run_gpu(args, rank, world, local):
               "encoder": "encoder layer: MHA (proj_gemm, attn_tc_kernel, outproj_ln) + FFN "
                          "(proj_gemm with bias+ReLU, outproj_ln with bias) (one step)",
               "decoder": "decoder layer: two MHA sublayers + FFN (eight launches, one step)",
+              "bwd": "attention backward on CUDA cores: row_dot + key_grads + query_grads (one step)",
               "decode": f"decode_split_kernel<{w.d_k}> + decode_combine_kernel (one step)",
               "pe": "pos_encoding_kernel"}.get(
                   w.kind, f"attn_tc_kernel<{w.d_k}>" if tc_attn else "attn_simt_kernel")
     hbm_bound = w.kind in ("decode", "pe")
     gbs = bytes_alg / (step_ms * 1e-3) / 1e9
-    roofline = {
-        "kernel": kernel,
-        "bound": "hbm" if hbm_bound else "tensor",
-        "achieved": round(gbs if hbm_bound else achieved, 2),
-        "peak": peaks["hbm_gbs"] if hbm_bound else peaks["bf16_tflops"],
-        "unit": "GB/s" if hbm_bound else "TFLOP/s",
-        "frac": round(gbs / peaks["hbm_gbs"] if hbm_bound else achieved / peaks["bf16_tflops"], 4),
-        "peak_source": (f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if hbm_bound else
-                        f"{peak_src} (burst, MEASURED_PEAKS.json bf16_tflops)"),
-        "frac_of_sustained": None if hbm_bound else round(achieved / peaks["bf16_tflops_sustained"], 4),
-        "frac_of_nominal_2250": None if hbm_bound else round(achieved / NOMINAL_BF16_TFLOPS, 4),
-        "algorithmic_flops_per_launch": flops,
-        "algorithmic_bytes_per_launch": bytes_alg,
-        "hbm_gbs_at_algorithmic_bytes": round(bytes_alg / (step_ms * 1e-3) / 1e9, 1),
-        "hbm_frac_at_algorithmic_bytes": round(bytes_alg / (step_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-        "traffic": profiled_traffic(w.name),
-    }
+    if w.kind == "bwd":
+        # CUDA-core kernels: fp32 FMA peak = SMs x 128 lanes x 2 FLOP x max SM clock.
+        alu_peak = 152 * 128 * 2 * 2.07e9 / 1e12
+        roofline = {
+            "kernel": "attention backward on CUDA cores (row_dot, key_grads, query_grads)",
+            "bound": "alu",
+            "achieved": round(achieved, 2),
+            "peak": round(alu_peak, 1),
+            "unit": "TFLOP/s",
+            "frac": round(achieved / alu_peak, 4),
+            "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2070 MHz (fp32 FMA)",
+            "frac_of_bf16_tensor_peak": round(achieved / peaks["bf16_tflops"], 4),
+            "algorithmic_flops_per_launch": flops,
+            "algorithmic_bytes_per_launch": bytes_alg,
+            "hbm_gbs_at_algorithmic_bytes": round(gbs, 1),
+            "traffic": None,
+        }
+    else:
+        roofline = {
+            "kernel": kernel,
+            "bound": "hbm" if hbm_bound else "tensor",
+            "achieved": round(gbs if hbm_bound else achieved, 2),
+            "peak": peaks["hbm_gbs"] if hbm_bound else peaks["bf16_tflops"],
+            "unit": "GB/s" if hbm_bound else "TFLOP/s",
+            "frac": round(gbs / peaks["hbm_gbs"] if hbm_bound else achieved / peaks["bf16_tflops"], 4),
+            "peak_source": (f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if hbm_bound else
+                            f"{peak_src} (burst, MEASURED_PEAKS.json bf16_tflops)"),
+            "frac_of_sustained": None if hbm_bound else round(achieved / peaks["bf16_tflops_sustained"], 4),
+            "frac_of_nominal_2250": None if hbm_bound else round(achieved / NOMINAL_BF16_TFLOPS, 4),
+            "algorithmic_flops_per_launch": flops,
+            "algorithmic_bytes_per_launch": bytes_alg,
+            "hbm_gbs_at_algorithmic_bytes": round(bytes_alg / (step_ms * 1e-3) / 1e9, 1),
+            "hbm_frac_at_algorithmic_bytes": round(bytes_alg / (step_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "traffic": profiled_traffic(w.name),
+        }
 
     result = {
         "metric": metric_of(w)[0],

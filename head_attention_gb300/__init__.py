@@ -12,10 +12,15 @@ from ._binding import (  # noqa: F401
     MASK_KEY_PADDING,
     MASK_NONE,
     HattnError,
+    attn_bwd,
+    attn_bwd_raw,
+    attn_bwd_workspace_bytes,
     attn_decode_fwd,
     attn_decode_fwd_raw,
     attn_decode_workspace_bytes,
     attn_fwd,
+    attn_fwd_lse,
+    attn_fwd_lse_raw,
     attn_fwd_raw,
     check_device_error,
     decoder_layer_fwd,

@@ -20,7 +20,7 @@ OK, EINVAL, EUNSUPPORTED, ECUDA, ETIMEOUT, EKEYLEN, EWORKSPACE, ESCRATCH = 0, -1
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 # Every symbol include/hattn.h declares.
-EXPORTED = ("attn_fwd", "attn_decode_fwd", "attn_decode_workspace_bytes", "mha_fwd",
+EXPORTED = ("attn_fwd", "attn_fwd_lse", "attn_bwd", "attn_bwd_workspace_bytes", "attn_decode_fwd", "attn_decode_workspace_bytes", "mha_fwd",
             "mha_fwd_noalloc", "mha_workspace_bytes", "pos_encoding_fwd", "ffn_fwd",
             "ffn_workspace_bytes", "encoder_layer_fwd", "encoder_layer_workspace_bytes",
             "decoder_layer_fwd", "decoder_layer_workspace_bytes", "hattn_status_str",
@@ -75,6 +75,12 @@ def load() -> ctypes.CDLL:
         lib.attn_decode_workspace_bytes.restype = sz
         lib.pos_encoding_fwd.argtypes = [vp, vp, i, i, i, i, f, i, vp]
         lib.pos_encoding_fwd.restype = i
+        lib.attn_fwd_lse.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, vp]
+        lib.attn_fwd_lse.restype = i
+        lib.attn_bwd.argtypes = [vp] * 9 + [i] * 7 + [f, i, vp, vp, sz, vp]
+        lib.attn_bwd.restype = i
+        lib.attn_bwd_workspace_bytes.argtypes = [i, i, i]
+        lib.attn_bwd_workspace_bytes.restype = sz
         lib.mha_workspace_bytes.argtypes = [i] * 8
         lib.mha_workspace_bytes.restype = sz
         lib.ffn_fwd.argtypes = [vp] * 7 + [f, vp, i, i, i, i, vp, sz, vp]
@@ -373,3 +379,62 @@ def decoder_layer_fwd(x, memory, self_attn, cross_attn, ffn, eps, h, src_lens=No
     if rc != OK:
         raise HattnError(rc, "decoder_layer_fwd")
     return y
+
+
+def attn_fwd_lse_raw(q, k, v, out, lse, dtype, B, h, n_q, n_k, d_k, d_v, scale, mask_kind, key_lens,
+                     stream) -> int:
+    return load().attn_fwd_lse(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(dtype), int(B),
+                               int(h), int(n_q), int(n_k), int(d_k), int(d_v), float(scale),
+                               int(mask_kind), _ptr(key_lens), _stream(stream))
+
+
+def attn_fwd_lse(q, k, v, out=None, lse=None, scale=None, mask_kind=MASK_NONE, key_lens=None,
+                 stream=None):
+    """attn_fwd that also returns the per-row log-sum-exp lse [B, h, n_q] (fp32)."""
+    import torch
+    B, n_q, h, d_k = q.shape
+    n_k, d_v = k.shape[1], v.shape[3]
+    if out is None:
+        out = torch.empty((B, n_q, h, d_v), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, h, n_q), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = d_k ** -0.5
+    rc = attn_fwd_lse_raw(q, k, v, out, lse, _dtype_code(q), B, h, n_q, n_k, d_k, d_v, scale,
+                          mask_kind, key_lens, stream)
+    if rc != OK:
+        raise HattnError(rc, "attn_fwd_lse")
+    return out, lse
+
+
+def attn_bwd_workspace_bytes(B, h, n_q) -> int:
+    return int(load().attn_bwd_workspace_bytes(int(B), int(h), int(n_q)))
+
+
+def attn_bwd_raw(q, k, v, out, dout, lse, dq, dk, dv, dtype, B, h, n_q, n_k, d_k, d_v, scale,
+                 mask_kind, key_lens, workspace, ws_bytes, stream) -> int:
+    return load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq),
+                           _ptr(dk), _ptr(dv), int(dtype), int(B), int(h), int(n_q), int(n_k),
+                           int(d_k), int(d_v), float(scale), int(mask_kind), _ptr(key_lens),
+                           _ptr(workspace), int(ws_bytes), _stream(stream))
+
+
+def attn_bwd(q, k, v, out, dout, lse, scale=None, mask_kind=MASK_NONE, key_lens=None, dq=None,
+             dk=None, dv=None, workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of attention given dout; out and lse from attn_fwd_lse."""
+    import torch
+    B, n_q, h, d_k = q.shape
+    n_k, d_v = k.shape[1], v.shape[3]
+    if scale is None:
+        scale = d_k ** -0.5
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(attn_bwd_workspace_bytes(B, h, n_q), dtype=torch.uint8,
+                                device=q.device)
+    rc = attn_bwd_raw(q, k, v, out, dout, lse, dq, dk, dv, _dtype_code(q), B, h, n_q, n_k, d_k, d_v,
+                      scale, mask_kind, key_lens, workspace, workspace.numel(), stream)
+    if rc != OK:
+        raise HattnError(rc, "attn_bwd")
+    return dq, dk, dv

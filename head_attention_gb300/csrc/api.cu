@@ -366,6 +366,52 @@ int mha_fwd_noalloc(const void* x_q, const void* x_kv, const void* Wq, const voi
                    h, d_k, d_v, mask_kind, key_lens, scratch, HATTN_NOALLOC_SCRATCH_BYTES, stream);
 }
 
+int attn_fwd_lse(const void* q, const void* k, const void* v, void* out, float* lse, int dtype,
+                 int B, int h, int n_q, int n_k, int d_k, int d_v, float scale, int mask_kind,
+                 const int32_t* key_lens, hattn_stream_t stream)
+{
+    if (!lse || !aligned16(lse)) return HATTN_EINVAL;
+    int rc = validate_attn(q, k, v, out, dtype, B, h, n_q, n_k, d_k, d_v, scale, mask_kind,
+                           key_lens);
+    if (rc != HATTN_OK) return rc;
+    AttnArgs a{q, k, v, out, dtype, B, h, n_q, n_k, d_k, d_v, scale, mask_kind,
+               (mask_kind & HATTN_MASK_KEY_PADDING) ? key_lens : nullptr,
+               reinterpret_cast<cudaStream_t>(stream), device_error_ptr(), lse};
+    if (!a.err_word) return HATTN_ECUDA;
+    return run_attn(a);
+}
+
+size_t attn_bwd_workspace_bytes(int B, int h, int n_q)
+{
+    if (B <= 0 || h <= 0 || n_q <= 0) return 0;
+    return align256(sizeof(float) * (size_t)B * h * n_q);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, int dtype, int B, int h, int n_q,
+             int n_k, int d_k, int d_v, float scale, int mask_kind, const int32_t* key_lens,
+             void* workspace, size_t ws_bytes, hattn_stream_t stream)
+{
+    if (!dout || !lse || !dq || !dk || !dv) return HATTN_EINVAL;
+    const void* ptrs[] = {dout, lse, dq, dk, dv};
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return HATTN_EINVAL;
+    int rc = validate_attn(q, k, v, const_cast<void*>(out), dtype, B, h, n_q, n_k, d_k, d_v,
+                           scale, mask_kind, key_lens);
+    if (rc != HATTN_OK) return rc;
+    if (h > 65535 || B > 65535) return HATTN_EUNSUPPORTED;
+    const size_t need = attn_bwd_workspace_bytes(B, h, n_q);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || ws_bytes < need)
+        return HATTN_EWORKSPACE;
+    int* err = device_error_ptr();
+    if (!err) return HATTN_ECUDA;
+    AttnBwdArgs a{q, k, v, out, dout, lse, dq, dk, dv, static_cast<float*>(workspace), dtype,
+                  B, h, n_q, n_k, d_k, d_v, scale, mask_kind,
+                  (mask_kind & HATTN_MASK_KEY_PADDING) ? key_lens : nullptr,
+                  reinterpret_cast<cudaStream_t>(stream), err};
+    return from_cuda(launch_attn_bwd(a));
+}
+
 size_t attn_decode_workspace_bytes(int B, int h, int n_max, int d)
 {
     if (B <= 0 || h <= 0 || n_max <= 0 || (d != 64 && d != 128 && d != 256)) return 0;

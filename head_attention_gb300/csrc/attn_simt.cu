@@ -99,7 +99,8 @@ template <typename T, int kCols>  // kCols = output columns per lane (d_v <= 32 
 __global__ void __launch_bounds__(kThreads)
     attn_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                      T* __restrict__ out, int n_q, int n_k, int h, int d_k, int d_v, float scale,
-                     int mask_kind, const int32_t* __restrict__ key_lens, int* err_word)
+                     int mask_kind, const int32_t* __restrict__ key_lens, int* err_word,
+                     float* __restrict__ lse)
 {
     extern __shared__ float smem[];
     const int dkp = d_k + 1;  // padded stride: lane j reads row j without bank conflicts
@@ -126,6 +127,9 @@ __global__ void __launch_bounds__(kThreads)
                 const int t = row0 + idx / d_v;
                 if (t < n_q) store_f32(o_bh + (size_t)t * v_row_stride + idx % d_v, 0.0f);
             }
+            if (lse)
+                for (int r = threadIdx.x; r < kRows; r += kThreads)
+                    if (row0 + r < n_q) lse[((size_t)b * h + head) * n_q + row0 + r] = -INFINITY;
             if (threadIdx.x == 0) raise_device_error(err_word, HATTN_EKEYLEN);
             return;
         }
@@ -195,6 +199,7 @@ __global__ void __launch_bounds__(kThreads)
         const int t = row0 + warp * kRowsPerWarp + rr;
         if (t >= n_q) continue;
         const float inv = l[rr] > 0.0f ? 1.0f / l[rr] : 0.0f;
+        if (lse && lane == 0) lse[((size_t)b * h + head) * n_q + t] = m[rr] + logf(l[rr]);
 #pragma unroll
         for (int i = 0; i < kCols; ++i) {
             const int cc = lane + 32 * i;
@@ -215,7 +220,7 @@ cudaError_t launch_typed(const AttnArgs& a)
     attn_simt_kernel<T, kCols><<<grid, kThreads, smem, a.stream>>>(
         static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v),
         static_cast<T*>(a.out), a.n_q, a.n_k, a.h, a.d_k, a.d_v, a.scale, a.mask_kind,
-        a.key_lens, a.err_word);
+        a.key_lens, a.err_word, a.lse);
     return cudaGetLastError();
 }
 

@@ -124,6 +124,7 @@ struct TcParams {
     int issuers;      // 2 when any unit has a second tile (n_q > 128), else 1
     const int32_t* key_lens;
     __nv_bfloat16* out;
+    float* lse;  // optional [B, h, n_q]
     int* err_word;
 };
 
@@ -484,8 +485,10 @@ __device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, 
         if (!c.valid) {
             // Key length outside [1, n_k]: this unit's rows are zero and the error is raised.
             __nv_bfloat16* orow = p.out + (((size_t)c.b * p.n_q + row) * p.h + c.head) * D;
-            if (row < p.n_q)
+            if (row < p.n_q) {
                 for (int k = 0; k < D; k += 8) st_global_v4(orow + k, 0u, 0u, 0u, 0u);
+                if (p.lse) p.lse[((size_t)c.b * p.h + c.head) * p.n_q + row] = -INFINITY;
+            }
             if (t == 0 && r == 0) raise_device_error(p.err_word, HATTN_EKEYLEN);
             continue;
         }
@@ -576,6 +579,10 @@ __device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, 
         // tile (which overwrites O) waits for this warpgroup's next P handoff.
         const float inv = 1.0f / l;
         __nv_bfloat16* orow = p.out + (((size_t)c.b * p.n_q + row) * p.h + c.head) * D;
+        // Natural-log log-sum-exp of the scaled scores: the exponentials ran in base 2
+        // on s * scale * log2(e) with the running max m, so ln sum = (m + log2 l) ln 2.
+        if (p.lse && row < p.n_q)
+            p.lse[((size_t)c.b * p.h + c.head) * p.n_q + row] = (m_used + log2f(l)) * 0.6931471805599453f;
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) {
             uint32_t o[32];
@@ -767,6 +774,7 @@ cudaError_t launch_d(const AttnArgs& a, const AttnMaps& m)
     p.n_pairs = (a.n_q + kRowsPerCta - 1) / kRowsPerCta;
     p.key_lens = a.key_lens;
     p.out = static_cast<__nv_bfloat16*>(a.out);
+    p.lse = a.lse;
     p.err_word = a.err_word;
     p.issuers = a.n_q > 128 ? 2 : 1;
     const long long units = (long long)p.n_pairs * a.B * a.h;

@@ -24,7 +24,8 @@ struct AttnArgs {
     int mask_kind;
     const int32_t* key_lens;
     cudaStream_t stream;
-    int* err_word;  // device error word of the current device
+    int* err_word;     // device error word of the current device
+    float* lse = nullptr;  // optional fp32 [B, h, n_q]: ln sum_j exp(scale q.k_j)
 };
 
 // Tensor maps of one attention call on the tensor-core path: Q, K, V viewed as
@@ -48,6 +49,29 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const vo
 // [B][n][h][d] bf16 tensor as a 4-D map with 64-element x `box_rows` boxes,
 // 128-byte swizzle, zero fill past n within each batch element.
 bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int n, int h, int d, int box_rows);
+
+// Attention backward (CUDA cores): dQ, dK, dV from Q, K, V, O, dO and the
+// forward's row log-sum-exp; dsum is fp32 scratch [B, h, n_q] for D = dO . O.
+struct AttnBwdArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* out;
+    const void* dout;
+    const float* lse;
+    void* dq;
+    void* dk;
+    void* dv;
+    float* dsum;
+    int dtype;
+    int B, h, n_q, n_k, d_k, d_v;
+    float scale;
+    int mask_kind;
+    const int32_t* key_lens;
+    cudaStream_t stream;
+    int* err_word;
+};
+cudaError_t launch_attn_bwd(const AttnBwdArgs& a);
 
 // Sinusoidal positional encoding added to scaled embeddings (emb may be NULL).
 cudaError_t launch_pos_encoding(const void* emb, void* out, int dtype, int B, int n, int d_model,

@@ -206,6 +206,41 @@ int attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, voi
 /* Bytes of workspace attn_decode_fwd needs for these sizes (0 on bad sizes). */
 size_t attn_decode_workspace_bytes(int B, int h, int n_max, int d);
 
+/*
+ * attn_fwd_lse — attn_fwd that also writes, for every (b, i, t), the natural
+ * log-sum-exp of the scaled scores over the visible keys,
+ *     lse[(b*h + i)*n_q + t] = ln sum_j exp(scale * q_t . k_j)    (fp32 [B, h, n_q]),
+ * which the backward pass uses to recompute the attention weights
+ * exp(scale q.k - lse). Same arguments, constraints and returns as attn_fwd;
+ * lse must be 16-byte aligned. A batch element with an invalid key length gets
+ * lse = -inf (and zero output) and HATTN_EKEYLEN.
+ */
+int attn_fwd_lse(const void* q, const void* k, const void* v, void* out, float* lse, int dtype,
+                 int B, int h, int n_q, int n_k, int d_k, int d_v, float scale, int mask_kind,
+                 const int32_t* key_lens, hattn_stream_t stream);
+
+/*
+ * attn_bwd — gradients of multi-head attention: given dout = dL/dout for
+ * out = attn_fwd(q, k, v), writes dq, dk, dv (the layouts and dtype of q, k, v):
+ *     P = exp(scale q.k - lse),  D_t = dout_t . out_t,  dS = P (dout.v - D)
+ *     dv_j = sum_t P_tj dout_t,  dk_j = scale sum_t dS_tj q_t,  dq_t = scale sum_j dS_tj k_j
+ * Training sends the loss gradient back through the attention weights ([P1]
+ * §参数是怎样学出来的？); these are the chain rule applied to the definition of
+ * attn_fwd. out and lse must come from attn_fwd_lse with the same inputs, scale
+ * and mask. Computed on CUDA cores in fp32, any d_k / d_v allowed by attn_fwd.
+ *   workspace  attn_bwd_workspace_bytes(B, h, n_q) bytes, 256-byte aligned
+ *              (fp32 D per row)
+ * Returns HATTN_OK, HATTN_EINVAL, HATTN_EUNSUPPORTED, HATTN_EWORKSPACE or
+ * HATTN_ECUDA; a bad key length zeroes that batch element's gradients and raises
+ * HATTN_EKEYLEN on the device error word.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, int dtype, int B, int h, int n_q,
+             int n_k, int d_k, int d_v, float scale, int mask_kind, const int32_t* key_lens,
+             void* workspace, size_t ws_bytes, hattn_stream_t stream);
+
+size_t attn_bwd_workspace_bytes(int B, int h, int n_q);
+
 /* Bytes of caller-owned workspace mha_fwd needs for these sizes (0 on bad sizes). */
 size_t mha_workspace_bytes(int dtype, int B, int n_q, int n_k, int d_model, int h, int d_k,
                            int d_v);

@@ -26,6 +26,7 @@ STREAM_XQ, STREAM_XKV = 3, 4
 STREAM_WQ, STREAM_WK, STREAM_WV, STREAM_WO = 5, 6, 7, 8
 STREAM_KEYLEN = 9
 STREAM_W1, STREAM_B1, STREAM_W2, STREAM_B2 = 10, 11, 12, 13
+STREAM_DOUT = 14  # upstream gradient of the attention output (backward workloads)
 # A second set of sublayer weights (the decoder layer's cross-attention) draws
 # from the MHA streams offset by this much.
 STREAM_CROSS_OFFSET = 100
@@ -138,7 +139,7 @@ class Workload:
     key_len_range: tuple | None = None  # inclusive (lo, hi) when KEY_PADDING
     d_model: int = 0  # > 0 for the MHA sublayer (and the embedding width for "pe")
     description: str = ""
-    kind: str = "attn"  # "attn", "mha", "decode" (n_q = 1 over a K/V prefix), "pe", "encoder", "decoder"
+    kind: str = "attn"  # "attn", "mha", "decode" (n_q = 1 over a K/V prefix), "pe", "encoder", "decoder", "bwd"
     d_ff: int = 0  # feed-forward width of the encoder / decoder layer
 
     @property
@@ -214,6 +215,11 @@ WORKLOADS = {
         description="post-norm decoder layer (causal self-attention, cross-attention over "
                     "source lengths U[256,512], FFN), bf16, B=16 n_tgt=n_src=512 d_model=512 h=8 "
                     "d=64 d_ff=2048"),
+    "attn_bwd_bf16": Workload(
+        "attn_bwd_bf16", "bf16", B=16, h=8, n_q=512, n_k=512, d_k=64, d_v=64,
+        mask_kind=MASK_CAUSAL, seed=10, kind="bwd",
+        description="attention backward (dQ, dK, dV), causal self-attention, bf16, B=16 h=8 "
+                    "n=512 d=64"),
     "long_causal_d128": Workload(
         "long_causal_d128", "bf16", B=4, h=16, n_q=8192, n_k=8192, d_k=128, d_v=128,
         mask_kind=MASK_CAUSAL, seed=4,
@@ -342,4 +348,11 @@ def layer_inputs(w: Workload) -> dict:
     if w.mask_kind & MASK_KEY_PADDING:
         lo, hi = w.key_len_range if w.key_len_range else (1, w.n_k)
         out["key_lens"] = draw_key_lens(w.seed, STREAM_KEYLEN, w.B, lo, hi)
+    return out
+
+
+def attn_bwd_inputs(w: Workload) -> dict:
+    """attn_inputs plus the upstream gradient dout ~ N(0, 1) [B, n_q, h, d_v] in the kernel dtype."""
+    out = attn_inputs(w)
+    out["dout"] = _to_kernel_dtype(draw_normal(w.seed, STREAM_DOUT, (w.B, w.n_q, w.h, w.d_v)), w.dtype)
     return out
