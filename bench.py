@@ -682,13 +682,13 @@ def run_gpu(args, rank, world, local):
               "encoder": "encoder layer: MHA (proj_gemm, attn_tc_kernel, outproj_ln) + FFN "
                          "(proj_gemm with bias+ReLU, outproj_ln with bias) (one step)",
               "decoder": "decoder layer: two MHA sublayers + FFN (eight launches, one step)",
-              "bwd": "attention backward on CUDA cores: row_dot + key_grads + query_grads (one step)",
+              "bwd": "attention backward on tensor cores: row_dot + key_grads_tc + query_grads_tc (one step)",
               "decode": f"decode_split_kernel<{w.d_k}> + decode_combine_kernel (one step)",
               "pe": "pos_encoding_kernel"}.get(
                   w.kind, f"attn_tc_kernel<{w.d_k}>" if tc_attn else "attn_simt_kernel")
     hbm_bound = w.kind in ("decode", "pe")
     gbs = bytes_alg / (step_ms * 1e-3) / 1e9
-    if w.kind == "bwd":
+    if w.kind == "bwd" and not (w.dtype == "bf16" and w.d_k == w.d_v and w.d_k in (64, 128)):
         # CUDA-core kernels: fp32 FMA peak = SMs x 128 lanes x 2 FLOP x max SM clock.
         alu_peak = 152 * 128 * 2 * 2.07e9 / 1e12
         roofline = {

@@ -384,7 +384,8 @@ int attn_fwd_lse(const void* q, const void* k, const void* v, void* out, float* 
 size_t attn_bwd_workspace_bytes(int B, int h, int n_q)
 {
     if (B <= 0 || h <= 0 || n_q <= 0) return 0;
-    return align256(sizeof(float) * (size_t)B * h * n_q);
+    const size_t nqp = ((size_t)n_q + 127) / 128 * 128;
+    return 2 * sizeof(float) * (size_t)B * h * nqp;  // dsum and lse2, each a multiple of 512 B
 }
 
 int attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
@@ -405,11 +406,24 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
         return HATTN_EWORKSPACE;
     int* err = device_error_ptr();
     if (!err) return HATTN_ECUDA;
-    AttnBwdArgs a{q, k, v, out, dout, lse, dq, dk, dv, static_cast<float*>(workspace), dtype,
+    const size_t nqp = ((size_t)n_q + 127) / 128 * 128;
+    float* dsum = static_cast<float*>(workspace);
+    float* lse2 = dsum + (size_t)B * h * nqp;
+    AttnBwdArgs a{q, k, v, out, dout, lse, dq, dk, dv, dsum, lse2, dtype,
                   B, h, n_q, n_k, d_k, d_v, scale, mask_kind,
                   (mask_kind & HATTN_MASK_KEY_PADDING) ? key_lens : nullptr,
                   reinterpret_cast<cudaStream_t>(stream), err};
-    return from_cuda(launch_attn_bwd(a));
+    rc = from_cuda(launch_attn_bwd_prep(a));
+    if (rc != HATTN_OK) return rc;
+    if (attn_bwd_tc_supported(a)) {
+        AttnMaps m;
+        CUtensorMap g;
+        if (!make_bnhd_map(&m.q, q, B, n_q, h, d_k, 128) || !make_bnhd_map(&m.k, k, B, n_k, h, d_k, 128) ||
+            !make_bnhd_map(&m.v, v, B, n_k, h, d_v, 128) || !make_bnhd_map(&g, dout, B, n_q, h, d_v, 128))
+            return HATTN_ECUDA;
+        return from_cuda(launch_attn_bwd_tc(a, m, g));
+    }
+    return from_cuda(launch_attn_bwd_simt(a));
 }
 
 size_t attn_decode_workspace_bytes(int B, int h, int n_max, int d)

@@ -45,8 +45,9 @@ struct BwdParams {
     void* dq;
     void* dk;
     void* dv;
-    float* dsum;  // D, fp32 [B, h, n_q]
-    int B, h, n_q, n_k, d_k, d_v;
+    float* dsum;  // D, fp32 [B, h, nqp]
+    float* lse2;  // base-2 log-sum-exp, fp32 [B, h, nqp]
+    int B, h, n_q, n_k, d_k, d_v, nqp;
     float scale;
     int mask_kind;
     const int32_t* key_lens;
@@ -70,24 +71,40 @@ __device__ __forceinline__ void stage(float* dst, int ld, const T* src, size_t s
     }
 }
 
-// D_i = dO_i . O_i, one warp per (b, t, head) row.
-template <typename T>
+// D_t = dO_t . O_t and lse2_t = lse_t log2(e) for every (b, head, t) with t
+// over the padded rows (0 and +inf past n_q). A group of kL lanes (a power of
+// two) covers one row with 16-byte loads, groups of a warp take consecutive
+// rows, and the partial dot products meet by shuffles within the group.
+template <typename T, int kL>
 __global__ void __launch_bounds__(kThreads) row_dot_kernel(const BwdParams p)
 {
-    const long long row = (long long)blockIdx.x * (kThreads / 32) + threadIdx.x / 32;
-    const long long rows = (long long)p.B * p.n_q * p.h;
-    if (row >= rows) return;
-    const int lane = threadIdx.x % 32;
-    const T* o = static_cast<const T*>(p.out) + row * p.d_v;
-    const T* g = static_cast<const T*>(p.dout) + row * p.d_v;
+    constexpr int kV = 16 / sizeof(T);  // elements per 16-byte load
+    const int lane = threadIdx.x % 32, gl = lane % kL;
+    const long long row = ((long long)blockIdx.x * kThreads + threadIdx.x) / kL;
+    const long long rows = (long long)p.B * p.h * p.nqp;
+    const bool in = row < rows;
+    const int t = in ? static_cast<int>(row % p.nqp) : 0;
+    const long long bh = in ? row / p.nqp : 0;
+    const int head = static_cast<int>(bh % p.h), b = static_cast<int>(bh / p.h);
     float acc = 0.0f;
-    for (int c = lane; c < p.d_v; c += 32) acc = fmaf(to_f32(o[c]), to_f32(g[c]), acc);
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
-        const int head = static_cast<int>(row % p.h);
-        const long long bt = row / p.h;
-        const int t = static_cast<int>(bt % p.n_q), b = static_cast<int>(bt / p.n_q);
-        p.dsum[((size_t)b * p.h + head) * p.n_q + t] = acc;
+    if (in && t < p.n_q) {
+        const size_t at = (((size_t)b * p.n_q + t) * p.h + head) * p.d_v;
+        const T* o = static_cast<const T*>(p.out) + at;
+        const T* g = static_cast<const T*>(p.dout) + at;
+        for (int c = gl * kV; c < p.d_v; c += kL * kV) {
+            const uint4 ov = *reinterpret_cast<const uint4*>(o + c);
+            const uint4 gv = *reinterpret_cast<const uint4*>(g + c);
+            const T* oe = reinterpret_cast<const T*>(&ov);
+            const T* ge = reinterpret_cast<const T*>(&gv);
+#pragma unroll
+            for (int e = 0; e < kV; ++e) acc = fmaf(to_f32(oe[e]), to_f32(ge[e]), acc);
+        }
+    }
+#pragma unroll
+    for (int off = kL / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (in && gl == 0) {
+        p.dsum[row] = acc;
+        p.lse2[row] = t < p.n_q ? p.lse[bh * p.n_q + t] * 1.4426950408889634f : INFINITY;
     }
 }
 
@@ -117,7 +134,7 @@ __global__ void __launch_bounds__(kThreads) key_grads_kernel(const BwdParams p)
     T* dkb = static_cast<T*>(p.dk) + (size_t)b * p.n_k * sk + (size_t)head * p.d_k;
     T* dvb = static_cast<T*>(p.dv) + (size_t)b * p.n_k * sv + (size_t)head * p.d_v;
     const float* lse_b = p.lse + ((size_t)b * p.h + head) * p.n_q;
-    const float* d_b = p.dsum + ((size_t)b * p.h + head) * p.n_q;
+    const float* d_b = p.dsum + ((size_t)b * p.h + head) * p.nqp;
 
     const int kv_len = key_length(p, b);
     if (kv_len < 1 || kv_len > p.n_k) {
@@ -212,7 +229,7 @@ __global__ void __launch_bounds__(kThreads) query_grads_kernel(const BwdParams p
     const T* gb = static_cast<const T*>(p.dout) + (size_t)b * p.n_q * sv + (size_t)head * p.d_v;
     T* dqb = static_cast<T*>(p.dq) + (size_t)b * p.n_q * sk + (size_t)head * p.d_k;
     const float* lse_b = p.lse + ((size_t)b * p.h + head) * p.n_q;
-    const float* d_b = p.dsum + ((size_t)b * p.h + head) * p.n_q;
+    const float* d_b = p.dsum + ((size_t)b * p.h + head) * p.nqp;
 
     const int kv_len = key_length(p, b);
     if (kv_len < 1 || kv_len > p.n_k) {
@@ -282,15 +299,11 @@ __global__ void __launch_bounds__(kThreads) query_grads_kernel(const BwdParams p
 template <typename T, int kCols, int kPW>
 cudaError_t launch_typed(const BwdParams& p, cudaStream_t stream)
 {
-    const long long rows = (long long)p.B * p.n_q * p.h;
-    row_dot_kernel<T><<<(unsigned)((rows + 3) / 4), kThreads, 0, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     const int dkp = p.d_k + 1, dvp = p.d_v + 1;
     constexpr int kBlock = 4 * kPW;
     const size_t smem_k = sizeof(float) * ((size_t)kBlock * (dkp + dvp) + (size_t)kInner * (dkp + dvp) + 2 * kInner);
-    e = cudaFuncSetAttribute(key_grads_kernel<T, kCols, kPW>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_k);
+    cudaError_t e = cudaFuncSetAttribute(key_grads_kernel<T, kCols, kPW>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_k);
     if (e != cudaSuccess) return e;
     key_grads_kernel<T, kCols, kPW><<<dim3((p.n_k + kBlock - 1) / kBlock, p.h, p.B), kThreads, smem_k, stream>>>(p);
     e = cudaGetLastError();
@@ -312,9 +325,7 @@ cudaError_t launch_cols(const BwdParams& p, cudaStream_t stream)
     return launch_typed<T, 8, 4>(p, stream);
 }
 
-}  // namespace
-
-cudaError_t launch_attn_bwd(const AttnBwdArgs& a)
+BwdParams make_params(const AttnBwdArgs& a)
 {
     BwdParams p;
     p.q = a.q;
@@ -327,16 +338,56 @@ cudaError_t launch_attn_bwd(const AttnBwdArgs& a)
     p.dk = a.dk;
     p.dv = a.dv;
     p.dsum = a.dsum;
+    p.lse2 = a.lse2;
     p.B = a.B;
     p.h = a.h;
     p.n_q = a.n_q;
     p.n_k = a.n_k;
     p.d_k = a.d_k;
     p.d_v = a.d_v;
+    p.nqp = (a.n_q + 127) / 128 * 128;
     p.scale = a.scale;
     p.mask_kind = a.mask_kind;
     p.key_lens = a.key_lens;
     p.err_word = a.err_word;
+    return p;
+}
+
+}  // namespace
+
+namespace {
+
+template <typename T, int kL>
+cudaError_t launch_row_dot(const BwdParams& p, cudaStream_t stream)
+{
+    const long long threads = (long long)p.B * p.h * p.nqp * kL;
+    row_dot_kernel<T, kL><<<(unsigned)((threads + kThreads - 1) / kThreads), kThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_row_dot_for(const BwdParams& p, cudaStream_t stream)
+{
+    // Lanes per row: d / (16-byte vector) rounded up to a power of two, at most 32.
+    const int vecs = (p.d_v * (int)sizeof(T) + 15) / 16;
+    if (vecs <= 4) return launch_row_dot<T, 4>(p, stream);
+    if (vecs <= 8) return launch_row_dot<T, 8>(p, stream);
+    if (vecs <= 16) return launch_row_dot<T, 16>(p, stream);
+    return launch_row_dot<T, 32>(p, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd_prep(const AttnBwdArgs& a)
+{
+    const BwdParams p = make_params(a);
+    if (a.dtype == HATTN_F32) return launch_row_dot_for<float>(p, a.stream);
+    return launch_row_dot_for<__nv_bfloat16>(p, a.stream);
+}
+
+cudaError_t launch_attn_bwd_simt(const AttnBwdArgs& a)
+{
+    const BwdParams p = make_params(a);
     if (a.dtype == HATTN_F32) return launch_cols<float>(p, a.stream);
     return launch_cols<__nv_bfloat16>(p, a.stream);
 }

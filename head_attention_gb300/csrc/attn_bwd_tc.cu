@@ -1,0 +1,565 @@
+// Tensor-core attention backward for sm_103a (bf16 in/out, fp32 accumulation,
+// d_k == d_v == D in {64, 128}, scale > 0).
+//
+// The gradients of sum(dO * O), O = softmax(scale Q K^T [masked]) V, per (b, h):
+//   P = 2^(scale log2(e) Q K^T - lse2)   (lse2: the forward's log-sum-exp in base 2)
+//   dP = dO V^T,  dS = P (dP - D),  D_t = dO_t . O_t
+//   dV = P^T dO,  dK = scale dS^T Q,  dQ = scale dS K
+// Training sends the loss gradient back through the attention weights
+// ("读懂 Attention Is All You Need", §参数是怎样学出来的？); these are the chain
+// rule applied to the forward (§六步算完一行注意力).
+//
+// Two CTA kinds in one grid, no atomics, both with 6 warps: warps 0-3 own TMEM lanes 0-127
+// (one row each: a key in the first kernel, a query in the second), warp 4
+// issues the TMA copies, warp 5 (one thread) the tcgen05 MMAs and owns TMEM.
+//
+//   key_grads_tc:   a CTA keeps one 128-key block of K and V in shared memory
+//                   and streams 128-query blocks of Q, dO, lse2 and D through a
+//                   2-stage ring. Per block: S^T = K Q^T and dP^T = V dO^T (SS
+//                   MMAs into TMEM); the row warps form P^T and dS^T, written back
+//                   to TMEM as bf16 over S^T and dP^T; then dV += P^T dO and
+//                   dK += dS^T Q (TS MMAs). TMEM: S^T | dP^T | dV | dK.
+//   query_grads_tc: a CTA keeps one 128-query block of Q and dO and streams
+//                   128-key blocks of K and V. Per block: S = Q K^T, dP = dO V^T,
+//                   dS (bf16, over S), dQ += dS K. TMEM: S | dP | dQ.
+// Causal: blocks entirely above the diagonal are skipped; key padding: key
+// blocks at or past key_lens[b] are skipped, the last one masked. All waits are
+// bounded; a wait that gives up raises HATTN_ETIMEOUT, and the CTA drains its
+// copies and MMAs before it frees TMEM.
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace hattn {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kWarpLoad = 4;
+constexpr int kWarpMma = 5;
+constexpr uint32_t kBoxBytes = 128 * 64 * 2;  // 128 rows x 64 bf16 columns
+constexpr int kStages = 2;
+
+template <int D>
+struct Tile {
+    static constexpr int kBoxes = D / 64;
+    static constexpr int kBytes = 128 * D * 2;
+    static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
+    static constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, false, true);
+};
+
+// X = A . B^T over the D columns of two K-major 128-row tiles (into 128 TMEM columns).
+template <int D>
+__device__ __forceinline__ void mma_abt(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc)
+{
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        const uint64_t off = ((ks / 4) * kBoxBytes + (ks % 4) * 32) >> 4;
+        mma_ss(d_tmem, a_desc + off, b_desc + off, Tile<D>::kIdescS, ks > 0 ? 1u : 0u);
+    }
+}
+
+// Acc (+)= X . T where X is 128 x 128 bf16 in TMEM (pairs packed in 64 columns)
+// and T a 128-row tile used MN-major (its D columns are the output columns).
+template <int D>
+__device__ __forceinline__ void mma_xt(uint32_t d_tmem, uint32_t x_tmem, uint64_t t_desc,
+                                       bool accumulate)
+{
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+        mma_ts(d_tmem, x_tmem + ks * 8, t_desc + ((ks * 2048) >> 4), Tile<D>::kIdescAcc,
+               (accumulate || ks > 0) ? 1u : 0u);
+}
+
+struct BwdTcParams {
+    int B, h, n_q, n_k, nqp;  // nqp: n_q rounded up to 128 (row stride of lse2 / dsum)
+    int mask_kind;
+    float scale, scale_log2;
+    const int32_t* key_lens;
+    const float* lse2;  // [B, h, nqp], base-2 log-sum-exp of scale*q.k (+inf past n_q)
+    const float* dsum;  // [B, h, nqp], D = dO . O (0 past n_q)
+    __nv_bfloat16* dq;
+    __nv_bfloat16* dk;
+    __nv_bfloat16* dv;
+    int* err_word;
+};
+
+__device__ __forceinline__ void store_row(__nv_bfloat16* dst, uint32_t tmem_row, int ncols, float mul,
+                                          bool valid)
+{
+    for (int c = 0; c < ncols; c += 32) {
+        uint32_t v[32];
+        tmem_ld_x32(tmem_row + c, v);
+        if (valid) {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+                st_global_v4(dst + c + 8 * v4,
+                             pack_bf16x2(mul * __uint_as_float(v[8 * v4]), mul * __uint_as_float(v[8 * v4 + 1])),
+                             pack_bf16x2(mul * __uint_as_float(v[8 * v4 + 2]), mul * __uint_as_float(v[8 * v4 + 3])),
+                             pack_bf16x2(mul * __uint_as_float(v[8 * v4 + 4]), mul * __uint_as_float(v[8 * v4 + 5])),
+                             pack_bf16x2(mul * __uint_as_float(v[8 * v4 + 6]), mul * __uint_as_float(v[8 * v4 + 7])));
+        }
+    }
+}
+
+__device__ __forceinline__ void zero_row(__nv_bfloat16* dst, int ncols)
+{
+    for (int c = 0; c < ncols; c += 8) st_global_v4(dst + c, 0u, 0u, 0u, 0u);
+}
+
+// ------------------------------------------------------------------ dK, dV
+
+template <int D>
+struct KCfg {
+    using T = Tile<D>;
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = T::kBytes;
+    static constexpr int kOffStage = 2 * T::kBytes;  // stage s: Q, dO, lse2[128], D[128]
+    static constexpr int kStageBytes = 2 * T::kBytes + 1024;
+    static constexpr int kOffBar = kOffStage + kStages * kStageBytes;
+    static constexpr int kBarKV = 0, kBarFull = 1, kBarEmpty = 1 + kStages, kBarS = 1 + 2 * kStages,
+                         kBarP = kBarS + 1, kBarO = kBarP + 1, kBarDrain = kBarO + 1,
+                         kNumBars = kBarDrain + 1;
+    static constexpr int kOffSlot = kOffBar + 8 * kNumBars;
+    static constexpr int kSmemBytes = kOffSlot + 16 + 1024;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    // TMEM columns
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+};
+
+// CTA `cta` of the key-gradient work: key block kblk = cta / (B h) of head
+// cta % (B h) (with the causal mask, low key blocks meet the most query blocks).
+template <int D>
+__device__ __forceinline__ void key_grads_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                             const CUtensorMap& tm_v, const CUtensorMap& tm_g,
+                                             const BwdTcParams& p, int cta)
+{
+    using C = KCfg<D>;
+    using T = Tile<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffSlot);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    const int kblk = cta / (p.B * p.h);
+    const int bh = cta % (p.B * p.h);
+    const int b = bh / p.h, head = bh % p.h;
+    const int key0 = kblk * 128;
+    const bool causal = (p.mask_kind & HATTN_MASK_CAUSAL) != 0;
+    const int kv_len = (p.mask_kind & HATTN_MASK_KEY_PADDING) ? p.key_lens[b] : p.n_k;
+    const size_t row_elems = (size_t)p.h * D;
+
+    if (kv_len < 1 || kv_len > p.n_k) {
+        if (threadIdx.x < 128 && key0 + threadIdx.x < p.n_k) {
+            const size_t off = ((size_t)b * p.n_k + key0 + threadIdx.x) * row_elems + (size_t)head * D;
+            zero_row(p.dk + off, D);
+            zero_row(p.dv + off, D);
+        }
+        if (threadIdx.x == 0) raise_device_error(p.err_word, HATTN_EKEYLEN);
+        return;
+    }
+    // Query blocks this key block meets: causal starts at the diagonal block.
+    const int n_qblk = (p.n_q + 127) / 128;
+    const int qb_first = causal ? kblk : 0;
+    const int nblk = key0 < kv_len ? max(0, n_qblk - qb_first) : 0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::kBarKV), 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar(C::kBarFull + s), 1);
+            mbar_init(bar(C::kBarEmpty + s), 1);
+        }
+        mbar_init(bar(C::kBarS), 1);
+        mbar_init(bar(C::kBarP), 4);
+        mbar_init(bar(C::kBarO), 1);
+        mbar_init(bar(C::kBarDrain), 1);
+        fence_barrier_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kWarpLoad) {
+        if (lane == 0 && nblk > 0) {
+            mbar_arrive_expect_tx(bar(C::kBarKV), 2 * T::kBytes);
+            for (int x = 0; x < T::kBoxes; ++x) {
+                tma_load_4d(sbase + C::kOffK + x * kBoxBytes, &tm_k, bar(C::kBarKV), x * 64, head, key0, b);
+                tma_load_4d(sbase + C::kOffV + x * kBoxBytes, &tm_v, bar(C::kBarKV), x * 64, head, key0, b);
+            }
+            const float* lse_row = p.lse2 + ((size_t)b * p.h + head) * p.nqp;
+            const float* d_row = p.dsum + ((size_t)b * p.h + head) * p.nqp;
+            int issued = 0;
+            for (int i = 0; i < nblk; ++i) {
+                const int s = i % kStages;
+                if (!mbar_wait(bar(C::kBarEmpty + s), ((i / kStages) & 1) ^ 1)) {
+                    raise_device_error(p.err_word, HATTN_ETIMEOUT);
+                    break;
+                }
+                const int q0 = (qb_first + i) * 128;
+                const uint32_t st = sbase + C::kOffStage + s * C::kStageBytes;
+                mbar_arrive_expect_tx(bar(C::kBarFull + s), 2 * T::kBytes + 1024);
+                for (int x = 0; x < T::kBoxes; ++x) {
+                    tma_load_4d(st + x * kBoxBytes, &tm_q, bar(C::kBarFull + s), x * 64, head, q0, b);
+                    tma_load_4d(st + T::kBytes + x * kBoxBytes, &tm_g, bar(C::kBarFull + s), x * 64, head, q0, b);
+                }
+                bulk_load(st + 2 * T::kBytes, lse_row + q0, 512, bar(C::kBarFull + s));
+                bulk_load(st + 2 * T::kBytes + 512, d_row + q0, 512, bar(C::kBarFull + s));
+                ++issued;
+            }
+            // Every copy this CTA started must land before the CTA may exit.
+            mbar_wait(bar(C::kBarKV), 0);
+            for (int i = max(0, issued - kStages); i < issued; ++i)
+                mbar_wait(bar(C::kBarFull + i % kStages), (i / kStages) & 1);
+        }
+        __syncwarp();
+    } else if (warp == kWarpMma) {
+        if (lane == 0 && nblk > 0) {
+            const uint64_t k_desc = sdesc_sw128(sbase + C::kOffK, 16, 1024);
+            const uint64_t v_desc = sdesc_sw128(sbase + C::kOffV, 16, 1024);
+            bool ok = mbar_wait(bar(C::kBarKV), 0);
+            for (int i = 0; ok && i < nblk; ++i) {
+                const int s = i % kStages;
+                if (!mbar_wait(bar(C::kBarFull + s), (i / kStages) & 1)) { ok = false; break; }
+                const uint32_t st = sbase + C::kOffStage + s * C::kStageBytes;
+                tc_fence_after();
+                mma_abt<D>(tmem + C::kColS, k_desc, sdesc_sw128(st, 16, 1024));               // S^T
+                mma_abt<D>(tmem + C::kColDP, v_desc, sdesc_sw128(st + T::kBytes, 16, 1024));  // dP^T
+                mma_commit(bar(C::kBarS));
+                if (!mbar_wait(bar(C::kBarP), i & 1)) { ok = false; break; }
+                tc_fence_after();
+                // dV += P^T dO,  dK += dS^T Q  (the Q / dO tiles used MN-major)
+                mma_xt<D>(tmem + C::kColDV, tmem + C::kColS, sdesc_sw128(st + T::kBytes, kBoxBytes, 1024), i > 0);
+                mma_xt<D>(tmem + C::kColDK, tmem + C::kColDP, sdesc_sw128(st, kBoxBytes, 1024), i > 0);
+                mma_commit(bar(C::kBarEmpty + s));
+            }
+            if (ok) mma_commit(bar(C::kBarO));
+            else raise_device_error(p.err_word, HATTN_ETIMEOUT);
+            mma_commit(bar(C::kBarDrain));
+            mbar_wait(bar(C::kBarDrain), 0);
+        }
+        __syncwarp();
+    } else {
+        // Row warps: thread r owns key key0 + r (TMEM lane r).
+        const int r = warp * 32 + lane;
+        const int key = key0 + r;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const bool key_ok = key < kv_len;
+        const size_t off = ((size_t)b * p.n_k + key) * row_elems + (size_t)head * D;
+        bool ok = true;
+        for (int i = 0; ok && i < nblk; ++i) {
+            const int s = i % kStages;
+            const int q0 = (qb_first + i) * 128;
+            const bool got = mbar_wait(bar(C::kBarFull + s), (i / kStages) & 1) && mbar_wait(bar(C::kBarS), i & 1);
+            ok = __all_sync(0xffffffffu, got);
+            if (!ok) break;
+            tc_fence_after();
+            const float* lse_s = reinterpret_cast<const float*>(smem + C::kOffStage + s * C::kStageBytes + 2 * T::kBytes);
+            const float* d_s = lse_s + 128;
+            // Keys at or past the length, or after every query of the block (causal), see nothing.
+            const bool row_live = key_ok && !(causal && key > q0 + 127);
+            const bool diag = causal && key0 + 127 > q0;  // this block straddles the diagonal
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t sv[32], pv[32];
+                tmem_ld_x32(lane_base + C::kColS + 32 * c, sv);
+                tmem_ld_x32(lane_base + C::kColDP + 32 * c, pv);
+                uint32_t pk[16], dk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float pr[2], ds[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int col = 32 * c + e + u;
+                        const int q = q0 + col;
+                        const bool vis = row_live && q < p.n_q && !(diag && key > q);
+                        const float x = fmaf(__uint_as_float(sv[e + u]), p.scale_log2, -lse_s[col]);
+                        pr[u] = vis ? ex2_approx(x) : 0.0f;
+                        ds[u] = pr[u] * (__uint_as_float(pv[e + u]) - d_s[col]);
+                    }
+                    pk[e / 2] = pack_bf16x2(pr[0], pr[1]);
+                    dk[e / 2] = pack_bf16x2(ds[0], ds[1]);
+                }
+                // bf16 P^T over S^T's columns [16c, 16c + 16), dS^T over dP^T's: both
+                // regions were read up to column 32c + 31 already.
+                tmem_st_x16(lane_base + C::kColS + 16 * c, pk);
+                tmem_st_x16(lane_base + C::kColDP + 16 * c, dk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::kBarP));
+        }
+        if (nblk == 0) {
+            if (key < p.n_k) {
+                zero_row(p.dk + off, D);
+                zero_row(p.dv + off, D);
+            }
+        } else if (ok) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarO), 0));
+            if (ok) {
+                tc_fence_after();
+                store_row(p.dv + off, lane_base + C::kColDV, D, 1.0f, key < p.n_k);
+                store_row(p.dk + off, lane_base + C::kColDK, D, p.scale, key < p.n_k);
+            }
+        }
+        if (!ok) raise_device_error(p.err_word, HATTN_ETIMEOUT);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------ dQ
+
+template <int D>
+struct QCfg {
+    using T = Tile<D>;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffG = T::kBytes;
+    static constexpr int kOffStage = 2 * T::kBytes;  // stage s: K, V
+    static constexpr int kStageBytes = 2 * T::kBytes;
+    static constexpr int kOffBar = kOffStage + kStages * kStageBytes;
+    static constexpr int kBarQG = 0, kBarFull = 1, kBarEmpty = 1 + kStages, kBarS = 1 + 2 * kStages,
+                         kBarP = kBarS + 1, kBarO = kBarP + 1, kBarDrain = kBarO + 1,
+                         kNumBars = kBarDrain + 1;
+    static constexpr int kOffSlot = kOffBar + 8 * kNumBars;
+    static constexpr int kSmemBytes = kOffSlot + 16 + 1024;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+};
+
+// CTA `cta` of the query-gradient work: query block n_qblk - 1 - cta / (B h)
+// of head cta % (B h) (with the causal mask, high query blocks meet the most key blocks).
+template <int D>
+__device__ __forceinline__ void query_grads_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                               const CUtensorMap& tm_v, const CUtensorMap& tm_g,
+                                               const BwdTcParams& p, int cta)
+{
+    using C = QCfg<D>;
+    using T = Tile<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) { return sbase + C::kOffBar + 8u * i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffSlot);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    const int n_qblk = (p.n_q + 127) / 128;
+    const int qblk = n_qblk - 1 - cta / (p.B * p.h);
+    const int bh = cta % (p.B * p.h);
+    const int b = bh / p.h, head = bh % p.h;
+    const int q0 = qblk * 128;
+    const bool causal = (p.mask_kind & HATTN_MASK_CAUSAL) != 0;
+    const int kv_len = (p.mask_kind & HATTN_MASK_KEY_PADDING) ? p.key_lens[b] : p.n_k;
+    const size_t row_elems = (size_t)p.h * D;
+
+    if (kv_len < 1 || kv_len > p.n_k) {
+        if (threadIdx.x < 128 && q0 + threadIdx.x < p.n_q)
+            zero_row(p.dq + ((size_t)b * p.n_q + q0 + threadIdx.x) * row_elems + (size_t)head * D, D);
+        return;  // the key-gradient kernel raises the error
+    }
+    int nblk = (kv_len + 127) / 128;
+    if (causal) nblk = min(nblk, qblk + 1);
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::kBarQG), 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar(C::kBarFull + s), 1);
+            mbar_init(bar(C::kBarEmpty + s), 1);
+        }
+        mbar_init(bar(C::kBarS), 1);
+        mbar_init(bar(C::kBarP), 4);
+        mbar_init(bar(C::kBarO), 1);
+        mbar_init(bar(C::kBarDrain), 1);
+        fence_barrier_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kWarpLoad) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar(C::kBarQG), 2 * T::kBytes);
+            for (int x = 0; x < T::kBoxes; ++x) {
+                tma_load_4d(sbase + C::kOffQ + x * kBoxBytes, &tm_q, bar(C::kBarQG), x * 64, head, q0, b);
+                tma_load_4d(sbase + C::kOffG + x * kBoxBytes, &tm_g, bar(C::kBarQG), x * 64, head, q0, b);
+            }
+            int issued = 0;
+            for (int j = 0; j < nblk; ++j) {
+                const int s = j % kStages;
+                if (!mbar_wait(bar(C::kBarEmpty + s), ((j / kStages) & 1) ^ 1)) {
+                    raise_device_error(p.err_word, HATTN_ETIMEOUT);
+                    break;
+                }
+                const uint32_t st = sbase + C::kOffStage + s * C::kStageBytes;
+                mbar_arrive_expect_tx(bar(C::kBarFull + s), 2 * T::kBytes);
+                for (int x = 0; x < T::kBoxes; ++x) {
+                    tma_load_4d(st + x * kBoxBytes, &tm_k, bar(C::kBarFull + s), x * 64, head, j * 128, b);
+                    tma_load_4d(st + T::kBytes + x * kBoxBytes, &tm_v, bar(C::kBarFull + s), x * 64, head, j * 128, b);
+                }
+                ++issued;
+            }
+            mbar_wait(bar(C::kBarQG), 0);
+            for (int j = max(0, issued - kStages); j < issued; ++j)
+                mbar_wait(bar(C::kBarFull + j % kStages), (j / kStages) & 1);
+        }
+        __syncwarp();
+    } else if (warp == kWarpMma) {
+        if (lane == 0) {
+            const uint64_t q_desc = sdesc_sw128(sbase + C::kOffQ, 16, 1024);
+            const uint64_t g_desc = sdesc_sw128(sbase + C::kOffG, 16, 1024);
+            bool ok = mbar_wait(bar(C::kBarQG), 0);
+            for (int j = 0; ok && j < nblk; ++j) {
+                const int s = j % kStages;
+                if (!mbar_wait(bar(C::kBarFull + s), (j / kStages) & 1)) { ok = false; break; }
+                const uint32_t st = sbase + C::kOffStage + s * C::kStageBytes;
+                tc_fence_after();
+                mma_abt<D>(tmem + C::kColS, q_desc, sdesc_sw128(st, 16, 1024));              // S = Q K^T
+                mma_abt<D>(tmem + C::kColDP, g_desc, sdesc_sw128(st + T::kBytes, 16, 1024));  // dP = dO V^T
+                mma_commit(bar(C::kBarS));
+                if (!mbar_wait(bar(C::kBarP), j & 1)) { ok = false; break; }
+                tc_fence_after();
+                mma_xt<D>(tmem + C::kColDQ, tmem + C::kColS, sdesc_sw128(st, kBoxBytes, 1024), j > 0);  // dQ += dS K
+                mma_commit(bar(C::kBarEmpty + s));
+            }
+            if (ok) mma_commit(bar(C::kBarO));
+            else raise_device_error(p.err_word, HATTN_ETIMEOUT);
+            mma_commit(bar(C::kBarDrain));
+            mbar_wait(bar(C::kBarDrain), 0);
+        }
+        __syncwarp();
+    } else {
+        // Row warps: thread r owns query q0 + r.
+        const int r = warp * 32 + lane;
+        const int q = q0 + r;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const float lse2 = q < p.n_q ? p.lse2[((size_t)b * p.h + head) * p.nqp + q] : 0.0f;
+        const float dsum = q < p.n_q ? p.dsum[((size_t)b * p.h + head) * p.nqp + q] : 0.0f;
+        const bool row_ok = q < p.n_q;
+        bool ok = true;
+        for (int j = 0; ok && j < nblk; ++j) {
+            const int k0 = j * 128;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarS), j & 1));
+            if (!ok) break;
+            tc_fence_after();
+            const bool edge = (k0 + 128 > kv_len) || (causal && k0 + 127 > q0);
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t sv[32], pv[32];
+                tmem_ld_x32(lane_base + C::kColS + 32 * c, sv);
+                tmem_ld_x32(lane_base + C::kColDP + 32 * c, pv);
+                uint32_t dk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float ds[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int key = k0 + 32 * c + e + u;
+                        const bool vis = row_ok && !(edge && (key >= kv_len || (causal && key > q)));
+                        const float x = fmaf(__uint_as_float(sv[e + u]), p.scale_log2, -lse2);
+                        const float pr = vis ? ex2_approx(x) : 0.0f;
+                        ds[u] = pr * (__uint_as_float(pv[e + u]) - dsum);
+                    }
+                    dk[e / 2] = pack_bf16x2(ds[0], ds[1]);
+                }
+                tmem_st_x16(lane_base + C::kColS + 16 * c, dk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::kBarP));
+        }
+        if (ok) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarO), 0));
+            if (ok) {
+                tc_fence_after();
+                store_row(p.dq + ((size_t)b * p.n_q + q) * row_elems + (size_t)head * D,
+                          lane_base + C::kColDQ, D, p.scale, row_ok);
+            }
+        }
+        if (!ok) raise_device_error(p.err_word, HATTN_ETIMEOUT);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// Both gradient computations in one grid: the query-gradient CTAs first, then
+// the key-gradient CTAs, so the tail of one overlaps the other.
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    grads_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                    const BwdTcParams p, int q_ctas)
+{
+    if (static_cast<int>(blockIdx.x) < q_ctas) query_grads_tc<D>(tm_q, tm_k, tm_v, tm_g, p, blockIdx.x);
+    else key_grads_tc<D>(tm_q, tm_k, tm_v, tm_g, p, blockIdx.x - q_ctas);
+}
+
+template <int D>
+cudaError_t launch_d(const AttnBwdArgs& a, const AttnMaps& m, const CUtensorMap& tm_g)
+{
+    BwdTcParams p;
+    p.B = a.B;
+    p.h = a.h;
+    p.n_q = a.n_q;
+    p.n_k = a.n_k;
+    p.nqp = (a.n_q + 127) / 128 * 128;
+    p.mask_kind = a.mask_kind;
+    p.scale = a.scale;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.key_lens = a.key_lens;
+    p.lse2 = a.lse2;
+    p.dsum = a.dsum;
+    p.dq = static_cast<__nv_bfloat16*>(a.dq);
+    p.dk = static_cast<__nv_bfloat16*>(a.dk);
+    p.dv = static_cast<__nv_bfloat16*>(a.dv);
+    p.err_word = a.err_word;
+    const long long kctas = (long long)a.B * a.h * ((a.n_k + 127) / 128);
+    const long long qctas = (long long)a.B * a.h * ((a.n_q + 127) / 128);
+    if (kctas + qctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const int smem = KCfg<D>::kSmemBytes > QCfg<D>::kSmemBytes ? KCfg<D>::kSmemBytes : QCfg<D>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(grads_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    grads_tc_kernel<D><<<(unsigned)(kctas + qctas), kThreads, smem, a.stream>>>(m.q, m.k, m.v, tm_g, p,
+                                                                               static_cast<int>(qctas));
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool attn_bwd_tc_supported(const AttnBwdArgs& a)
+{
+    return a.dtype == HATTN_BF16 && a.d_k == a.d_v && (a.d_k == 64 || a.d_k == 128) && a.scale > 0.0f;
+}
+
+cudaError_t launch_attn_bwd_tc(const AttnBwdArgs& a, const AttnMaps& maps, const CUtensorMap& tm_dout)
+{
+    return a.d_k == 64 ? launch_d<64>(a, maps, tm_dout) : launch_d<128>(a, maps, tm_dout);
+}
+
+}  // namespace hattn

@@ -50,8 +50,10 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const vo
 // 128-byte swizzle, zero fill past n within each batch element.
 bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int n, int h, int d, int box_rows);
 
-// Attention backward (CUDA cores): dQ, dK, dV from Q, K, V, O, dO and the
-// forward's row log-sum-exp; dsum is fp32 scratch [B, h, n_q] for D = dO . O.
+// Attention backward: dQ, dK, dV from Q, K, V, O, dO and the forward's row
+// log-sum-exp. Scratch (fp32, rows padded to nqp = n_q rounded up to 128):
+// dsum [B, h, nqp] = dO . O (0 past n_q) and lse2 [B, h, nqp] = lse * log2(e)
+// (+inf past n_q), both written by the preparation kernel.
 struct AttnBwdArgs {
     const void* q;
     const void* k;
@@ -63,6 +65,7 @@ struct AttnBwdArgs {
     void* dk;
     void* dv;
     float* dsum;
+    float* lse2;
     int dtype;
     int B, h, n_q, n_k, d_k, d_v;
     float scale;
@@ -71,7 +74,10 @@ struct AttnBwdArgs {
     cudaStream_t stream;
     int* err_word;
 };
-cudaError_t launch_attn_bwd(const AttnBwdArgs& a);
+cudaError_t launch_attn_bwd_prep(const AttnBwdArgs& a);
+cudaError_t launch_attn_bwd_simt(const AttnBwdArgs& a);  // CUDA cores, any supported shape
+bool attn_bwd_tc_supported(const AttnBwdArgs& a);          // bf16, d_k == d_v in {64, 128}
+cudaError_t launch_attn_bwd_tc(const AttnBwdArgs& a, const AttnMaps& maps, const CUtensorMap& tm_dout);
 
 // Sinusoidal positional encoding added to scaled embeddings (emb may be NULL).
 cudaError_t launch_pos_encoding(const void* emb, void* out, int dtype, int B, int n, int d_model,

@@ -227,9 +227,11 @@ int attn_fwd_lse(const void* q, const void* k, const void* v, void* out, float* 
  * Training sends the loss gradient back through the attention weights ([P1]
  * §参数是怎样学出来的？); these are the chain rule applied to the definition of
  * attn_fwd. out and lse must come from attn_fwd_lse with the same inputs, scale
- * and mask. Computed on CUDA cores in fp32, any d_k / d_v allowed by attn_fwd.
+ * and mask. bf16 with d_k == d_v in {64, 128} and scale > 0 runs on the tensor
+ * cores (bf16 P and dS, fp32 accumulation); every other shape attn_fwd accepts
+ * runs on CUDA cores in fp32.
  *   workspace  attn_bwd_workspace_bytes(B, h, n_q) bytes, 256-byte aligned
- *              (fp32 D per row)
+ *              (fp32 D and base-2 log-sum-exp per row, rows padded to 128)
  * Returns HATTN_OK, HATTN_EINVAL, HATTN_EUNSUPPORTED, HATTN_EWORKSPACE or
  * HATTN_ECUDA; a bad key length zeroes that batch element's gradients and raises
  * HATTN_EKEYLEN on the device error word.

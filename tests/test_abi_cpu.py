@@ -245,7 +245,7 @@ def test_layers_reject_bad_arguments(lib):
 
 BWD_GOOD = dict(q=A, k=2 * A, v=3 * A, out=4 * A, dout=5 * A, lse=6 * A, dq=7 * A, dk=8 * A,
                 dv=9 * A, dtype=1, B=2, h=4, n_q=128, n_k=128, d_k=64, d_v=64, scale=0.125,
-                mask_kind=0, key_lens=None, workspace=0x100000, ws_bytes=2 * 4 * 128 * 4, stream=0)
+                mask_kind=0, key_lens=None, workspace=0x100000, ws_bytes=2 * 2 * 4 * 128 * 4, stream=0)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -257,7 +257,7 @@ BWD_GOOD = dict(q=A, k=2 * A, v=3 * A, out=4 * A, dout=5 * A, lse=6 * A, dq=7 * 
     (dict(mask_kind=2), hattn._binding.EINVAL),
     (dict(d_k=256, dtype=0), hattn._binding.EUNSUPPORTED),
     (dict(workspace=None), hattn._binding.EWORKSPACE),
-    (dict(ws_bytes=2 * 4 * 128 * 4 - 4), hattn._binding.EWORKSPACE),
+    (dict(ws_bytes=2 * 2 * 4 * 128 * 4 - 4), hattn._binding.EWORKSPACE),
 ])
 def test_attn_bwd_rejects_bad_arguments(lib, kw, code):
     args = dict(BWD_GOOD)
@@ -270,5 +270,7 @@ def test_attn_fwd_lse_rejects_bad_arguments(lib):
     assert hattn.attn_fwd_lse_raw(**dict(args, lse=None)) == hattn._binding.EINVAL
     assert hattn.attn_fwd_lse_raw(**dict(args, lse=6 * A + 8)) == hattn._binding.EINVAL
     assert hattn.attn_fwd_lse_raw(**dict(args, q=None)) == hattn._binding.EINVAL
-    assert hattn.attn_bwd_workspace_bytes(2, 4, 128) == 4096
-    assert hattn.attn_bwd_workspace_bytes(1, 1, 1) == 256
+    # Two fp32 arrays (D and the base-2 log-sum-exp) of B * h rows padded to 128.
+    assert hattn.attn_bwd_workspace_bytes(2, 4, 128) == 2 * 4 * 2 * 4 * 128
+    assert hattn.attn_bwd_workspace_bytes(1, 1, 1) == 2 * 4 * 128
+    assert hattn.attn_bwd_workspace_bytes(1, 1, 129) == 2 * 4 * 256

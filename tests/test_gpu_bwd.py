@@ -42,6 +42,9 @@ CASES = [
     ("bf16", 2, 2, 300, 300, 128, 128, 3, (100, 300)),
     ("bf16", 1, 2, 150, 90, 64, 32, 2, (40, 90)),
     ("bf16", 2, 4, 512, 512, 64, 64, 1, None),
+    ("bf16", 2, 2, 256, 384, 128, 128, 0, None),
+    ("bf16", 1, 3, 333, 333, 128, 128, 1, None),
+    ("bf16", 4, 1, 129, 257, 64, 64, 2, (1, 257)),
 ]
 
 
