@@ -466,7 +466,7 @@ __device__ __forceinline__ float row_max(const uint32_t (&sr)[128])
     return max3f(max3f(part[0], part[1], part[2]), part[3], fmaxf(part[4], part[15]));
 }
 
-template <int D, bool kTable, class Sched>
+template <int D, bool kTable, bool kLse, class Sched>
 __device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, int wq, int lane)
 {
     using C = Cfg<D>;
@@ -487,7 +487,7 @@ __device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, 
             __nv_bfloat16* orow = p.out + (((size_t)c.b * p.n_q + row) * p.h + c.head) * D;
             if (row < p.n_q) {
                 for (int k = 0; k < D; k += 8) st_global_v4(orow + k, 0u, 0u, 0u, 0u);
-                if (p.lse) p.lse[((size_t)c.b * p.h + c.head) * p.n_q + row] = -INFINITY;
+                if constexpr (kLse) p.lse[((size_t)c.b * p.h + c.head) * p.n_q + row] = -INFINITY;
             }
             if (t == 0 && r == 0) raise_device_error(p.err_word, HATTN_EKEYLEN);
             continue;
@@ -581,8 +581,10 @@ __device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, 
         __nv_bfloat16* orow = p.out + (((size_t)c.b * p.n_q + row) * p.h + c.head) * D;
         // Natural-log log-sum-exp of the scaled scores: the exponentials ran in base 2
         // on s * scale * log2(e) with the running max m, so ln sum = (m + log2 l) ln 2.
-        if (p.lse && row < p.n_q)
-            p.lse[((size_t)c.b * p.h + c.head) * p.n_q + row] = (m_used + log2f(l)) * 0.6931471805599453f;
+        if constexpr (kLse) {
+            if (row < p.n_q)
+                p.lse[((size_t)c.b * p.h + c.head) * p.n_q + row] = (m_used + log2f(l)) * 0.6931471805599453f;
+        }
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) {
             uint32_t o[32];
@@ -604,7 +606,7 @@ __device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, 
 
 // ---------------------------------------------------------------- kernel
 
-template <int D, bool kTable, class Sched>
+template <int D, bool kTable, bool kLse, class Sched>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const TcParams p,
@@ -671,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         regs_inc<kRegsSoftmax>();
-        softmax_tile<D, kTable>(c, p, sch, warp / 4, warp % 4, lane);
+        softmax_tile<D, kTable, kLse>(c, p, sch, warp / 4, warp % 4, lane);
     }
 
     tc_fence_before();
@@ -748,17 +750,27 @@ std::shared_ptr<const SchedTable> greedy_table(const TcParams& p, int grid)
     return tab;
 }
 
+template <int D, bool kTable, bool kLse, class Sched>
+cudaError_t launch_kernel_lse(const AttnArgs& a, const AttnMaps& m, const TcParams& p, int grid,
+                              const Sched& sch)
+{
+    using C = Cfg<D>;
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, kTable, kLse, Sched>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attn_tc_kernel<D, kTable, kLse, Sched><<<grid, kThreads, C::kSmemBytes, a.stream>>>(m.q, m.k, m.v, p, sch);
+    return cudaGetLastError();
+}
+
+// The log-sum-exp output is a separate instantiation, so the plain forward's
+// softmax code (and its register allocation) does not carry it.
 template <int D, bool kTable, class Sched>
 cudaError_t launch_kernel(const AttnArgs& a, const AttnMaps& m, const TcParams& p, int grid,
                           const Sched& sch)
 {
-    using C = Cfg<D>;
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D, kTable, Sched>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attn_tc_kernel<D, kTable, Sched><<<grid, kThreads, C::kSmemBytes, a.stream>>>(m.q, m.k, m.v, p, sch);
-    return cudaGetLastError();
+    if (p.lse) return launch_kernel_lse<D, kTable, true>(a, m, p, grid, sch);
+    return launch_kernel_lse<D, kTable, false>(a, m, p, grid, sch);
 }
 
 template <int D>
