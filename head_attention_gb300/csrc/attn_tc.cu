@@ -661,6 +661,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     c.tmem = *tmem_slot;
+    // Set-up above overlaps the previous kernel's tail; its outputs are read below.
+    griddep_wait();
+    griddep_launch_dependents();
 
     if (warp >= 8) {
         regs_dec<kRegsControl>();
@@ -759,8 +762,17 @@ cudaError_t launch_kernel_lse(const AttnArgs& a, const AttnMaps& m, const TcPara
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attn_tc_kernel<D, kTable, kLse, Sched><<<grid, kThreads, C::kSmemBytes, a.stream>>>(m.q, m.k, m.v, p, sch);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, kTable, kLse, Sched>, m.q, m.k, m.v, p, sch);
 }
 
 // The log-sum-exp output is a separate instantiation, so the plain forward's

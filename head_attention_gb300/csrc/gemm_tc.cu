@@ -11,8 +11,9 @@
 //           W^O, or the second feed-forward layer W2, with the residual and
 //           the post-norm). The mean and biased variance need whole rows: a
 //           row of up to 256 columns stays in one CTA; wider rows (d_model up
-//           to 512) are split over the two CTAs of a cluster, which exchange
-//           their per-row partial sums through distributed shared memory.
+//           to 512) are split over the two CTAs of a cluster: each computes the
+//           mean and squared deviations of its half-row, and one exchange through
+//           distributed shared memory merges them pairwise.
 //
 // Tiles are 128 rows x up to 256 columns. Warp 0 streams A (128 x 64 boxes,
 // K-major) and W ([K][N] row-major, i.e. N-major, 64 x 64 boxes) through a
@@ -42,25 +43,39 @@ constexpr int kThreads = 192;
 constexpr int kWarpLoad = 0;
 constexpr int kWarpMma = 1;  // also owns the TMEM allocation
 constexpr int kBM = 128, kBN = 256, kBK = 64;
-constexpr int kStages = 4;
 constexpr uint32_t kABoxBytes = kBM * kBK * 2;  // A box: 128 rows x 64 columns
 constexpr uint32_t kWBoxBytes = 64 * kBK * 2;   // W box: 64 K-rows x 64 N-columns
 constexpr uint32_t kStageBytes = kABoxBytes + (kBN / 64) * kWBoxBytes;
-// Barrier indices.
-constexpr int kBarFull = 0;
-constexpr int kBarEmpty = kStages;
-constexpr int kBarAccFull = 2 * kStages;       // 2: accumulator b holds a finished tile
-constexpr int kBarAccEmpty = 2 * kStages + 2;  // 2: the epilogue has read accumulator b
-constexpr int kBarSum = 2 * kStages + 4;       // the peer's per-row partial sums arrived
-constexpr int kBarSq = 2 * kStages + 5;        // the peer's per-row squared deviations arrived
-constexpr int kBarDrain = 2 * kStages + 6;
-constexpr int kNumBars = 2 * kStages + 7;
-constexpr int kOffBar = kStages * kStageBytes;
-constexpr int kOffStat = kOffBar + 8 * kNumBars;  // float recv_sum[128], recv_sq[128]
-constexpr int kOffSlot = kOffStat + 2 * kBM * 4;  // TMEM base address
-constexpr int kSmemBytes = kOffSlot + 16 + 1024;  // + slack to align the base to 1024 B
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 constexpr int kEpiThreads = 128;
+
+// Shared-memory layout and barrier indices. The norm epilogue also stages the
+// tile's residual rows (up to 256 columns) by TMA, which costs one ring stage.
+template <bool kNorm>
+struct Layout {
+    static constexpr int kStages = kNorm ? 3 : 4;
+    static constexpr int kBarFull = 0;
+    static constexpr int kBarEmpty = kStages;
+    static constexpr int kBarAccFull = 2 * kStages;       // 2: accumulator b holds a finished tile
+    static constexpr int kBarAccEmpty = 2 * kStages + 2;  // 2: the epilogue has read accumulator b
+    static constexpr int kBarSum = 2 * kStages + 4;       // the peer's per-row partial sums arrived
+    static constexpr int kBarSq = 2 * kStages + 5;        // the peer's squared deviations arrived
+    static constexpr int kBarDrain = 2 * kStages + 6;
+    static constexpr int kBarXFull = 2 * kStages + 7;     // the tile's residual rows landed
+    static constexpr int kBarXEmpty = 2 * kStages + 8;    // their buffer (reused for the output) is free
+    static constexpr int kBarYReady = 2 * kStages + 9;    // every epilogue warp wrote its output rows
+    static constexpr int kNumBars = 2 * kStages + 10;
+    static constexpr int kOffX = kStages * kStageBytes;  // residual: 4 boxes of 128 rows x 64 columns
+    static constexpr int kXBytes = kNorm ? 4 * kABoxBytes : 0;
+    static constexpr int kOffBar = kOffX + kXBytes;
+    // float recv_sum[128], recv_sq[128] (16-byte aligned, as are the vectors after them)
+    static constexpr int kOffStat = (kOffBar + 8 * kNumBars + 15) / 16 * 16;
+    // norm: gamma, beta and bias of this CTA's columns (fp32, up to 256 each)
+    static constexpr int kOffVec = kOffStat + 2 * kBM * 4;
+    static constexpr int kVecBytes = kNorm ? 3 * kBN * 4 : 0;
+    static constexpr int kOffSlot = kOffVec + kVecBytes;  // TMEM base address
+    static constexpr int kSmemBytes = kOffSlot + 16 + 1024;  // + slack to align the base to 1024 B
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
 
 struct GemmProblem {
     void* c;            // bf16 [M][N] (store epilogue) or y (norm epilogue)
@@ -147,16 +162,23 @@ __device__ __forceinline__ float ld_volatile_shared_f32(uint32_t addr)
 // peer's partial for the same row. Each exchange barrier completes once per
 // tile: the peer's next arrival on it needs this CTA's next exchange, which
 // happens only after this one has been read.
-__device__ __forceinline__ bool exchange_partial(float v, float& peer_v, uint32_t sbase,
-                                                 int stat_off, int bar_index, uint32_t parity,
-                                                 int r, uint32_t peer)
+// Sends this row's (a, b) to the peer CTA of the pair and returns the peer's
+// pair for the same row; the exchange barrier completes once per tile (the
+// peer's next arrival needs this CTA's next exchange, after this one was read).
+template <bool kNorm>
+__device__ __forceinline__ bool exchange_pair(float a, float b, float& peer_a, float& peer_b,
+                                              uint32_t sbase, uint32_t parity, int r, uint32_t peer)
 {
-    const uint32_t slot = sbase + kOffStat + stat_off + 4u * r;
-    const uint32_t bar = sbase + kOffBar + 8u * bar_index;
-    st_cluster_f32(mapa_shared(slot, peer), v);
+    using Lay = Layout<kNorm>;
+    const uint32_t slot_a = sbase + Lay::kOffStat + 4u * r;
+    const uint32_t slot_b = slot_a + 4u * kBM;
+    const uint32_t bar = sbase + Lay::kOffBar + 8u * Lay::kBarSum;
+    st_cluster_f32(mapa_shared(slot_a, peer), a);
+    st_cluster_f32(mapa_shared(slot_b, peer), b);
     mbar_arrive_cluster(mapa_shared(bar, peer));
     if (!mbar_wait_cluster(bar, parity)) return false;
-    peer_v = ld_volatile_shared_f32(slot);
+    peer_a = ld_volatile_shared_f32(slot_a);
+    peer_b = ld_volatile_shared_f32(slot_b);
     return true;
 }
 
@@ -167,28 +189,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap w1, const __grid_constant__ CUtensorMap w2,
                 const __grid_constant__ GemmParams p)
 {
+    using Lay = Layout<kNorm>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sbar = sbase + kOffBar;
+    const uint32_t sbar = sbase + Lay::kOffBar;
     auto bar = [&](int i) { return sbar + 8u * i; };
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffSlot);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffSlot);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t rank = p.split == 2 ? cluster_ctarank() : 0u;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar(kBarFull + s), 1);
-            mbar_init(bar(kBarEmpty + s), 1);
+        for (int s = 0; s < Lay::kStages; ++s) {
+            mbar_init(bar(Lay::kBarFull + s), 1);
+            mbar_init(bar(Lay::kBarEmpty + s), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(kBarAccFull + b), 1);
-            mbar_init(bar(kBarAccEmpty + b), kEpiThreads / 32);
+            mbar_init(bar(Lay::kBarAccFull + b), 1);
+            mbar_init(bar(Lay::kBarAccEmpty + b), kEpiThreads / 32);
         }
-        mbar_init(bar(kBarSum), kEpiThreads);
-        mbar_init(bar(kBarSq), kEpiThreads);
-        mbar_init(bar(kBarDrain), 1);
+        mbar_init(bar(Lay::kBarSum), kEpiThreads);
+        mbar_init(bar(Lay::kBarSq), kEpiThreads);
+        mbar_init(bar(Lay::kBarDrain), 1);
+        mbar_init(bar(Lay::kBarXFull), 1);
+        mbar_init(bar(Lay::kBarXEmpty), 1);
+        mbar_init(bar(Lay::kBarYReady), kEpiThreads / 32);
         fence_barrier_init();
     }
     if (warp == kWarpMma) {
@@ -207,38 +233,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.split == 2) cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Set-up above overlaps the previous kernel's tail; its outputs are read below.
+    griddep_wait();
+    griddep_launch_dependents();
     const TileRange tr = tile_range(p);
 
     if (warp == kWarpLoad) {
         if (lane == 0) {
-            uint32_t it = 0;
+            uint32_t it = 0, tcount = 0;
             bool ok = true;
-            for (int t = tr.first; ok && t < p.tiles; t += tr.stride) {
+            for (int t = tr.first; ok && t < p.tiles; t += tr.stride, ++tcount) {
                 const TileGeom g = tile_geom<kNorm>(p, t, rank);
-                const CUtensorMap* am = pick(g.p, &a0, &a1, &a2);
+                const CUtensorMap* am = pick(kNorm ? 0 : g.p, &a0, &a1, &a2);
                 const CUtensorMap* wm = pick(g.p, &w0, &w1, &w2);
                 const int kblocks = p.prob[g.p].K / kBK;
                 const int nbox = g.bn / 64;
+                if constexpr (kNorm) {
+                    // The tile's residual rows (map a1), once the previous tile's epilogue read them.
+                    if (!mbar_wait(bar(Lay::kBarXEmpty), (tcount & 1) ^ 1)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(Lay::kBarXFull), nbox * kABoxBytes);
+                    for (int j = 0; j < nbox; ++j)
+                        tma_load_2d(sbase + Lay::kOffX + j * kABoxBytes, &a1, bar(Lay::kBarXFull),
+                                    g.n0 + 64 * j, g.m0);
+                }
                 const uint32_t tx = kABoxBytes + nbox * kWBoxBytes;
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    const uint32_t s = it % kStages;
-                    if (!mbar_wait(bar(kBarEmpty + s), ((it / kStages) & 1) ^ 1)) {
+                    const uint32_t s = it % Lay::kStages;
+                    if (!mbar_wait(bar(Lay::kBarEmpty + s), ((it / Lay::kStages) & 1) ^ 1)) {
                         ok = false;
                         break;
                     }
                     const uint32_t st = sbase + s * kStageBytes;
-                    mbar_arrive_expect_tx(bar(kBarFull + s), tx);
-                    tma_load_2d(st, am, bar(kBarFull + s), kb * kBK, g.m0);
+                    mbar_arrive_expect_tx(bar(Lay::kBarFull + s), tx);
+                    tma_load_2d(st, am, bar(Lay::kBarFull + s), kb * kBK, g.m0);
                     for (int j = 0; j < nbox; ++j)
-                        tma_load_2d(st + kABoxBytes + j * kWBoxBytes, wm, bar(kBarFull + s),
+                        tma_load_2d(st + kABoxBytes + j * kWBoxBytes, wm, bar(Lay::kBarFull + s),
                                     g.n0 + 64 * j, kb * kBK);
                     ++it;
                 }
             }
             if (!ok) raise_device_error(p.err_word, HATTN_ETIMEOUT);
             // Every copy this CTA started must land before the CTA may exit.
-            for (uint32_t i = it > (uint32_t)kStages ? it - kStages : 0u; i < it; ++i)
-                mbar_wait(bar(kBarFull + i % kStages), (i / kStages) & 1);
+            for (uint32_t i = it > (uint32_t)Lay::kStages ? it - Lay::kStages : 0u; i < it; ++i)
+                mbar_wait(bar(Lay::kBarFull + i % Lay::kStages), (i / Lay::kStages) & 1);
+            if (kNorm && tcount > 0) mbar_wait(bar(Lay::kBarXFull), (tcount - 1) & 1);
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
@@ -249,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const TileGeom g = tile_geom<kNorm>(p, t, rank);
                 const int kblocks = p.prob[g.p].K / kBK;
                 const uint32_t b = i & 1;
-                if (!mbar_wait(bar(kBarAccEmpty + b), ((i >> 1) & 1) ^ 1)) {
+                if (!mbar_wait(bar(Lay::kBarAccEmpty + b), ((i >> 1) & 1) ^ 1)) {
                     ok = false;
                     break;
                 }
@@ -257,8 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t d = tmem + 256u * b;
                 const uint32_t idesc = idesc_bf16_f32(128, g.bn, false, true);
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    const uint32_t s = it % kStages;
-                    if (!mbar_wait(bar(kBarFull + s), (it / kStages) & 1)) {
+                    const uint32_t s = it % Lay::kStages;
+                    if (!mbar_wait(bar(Lay::kBarFull + s), (it / Lay::kStages) & 1)) {
                         ok = false;
                         break;
                     }
@@ -269,15 +310,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_ss(d, sdesc_sw128(st + ks * 32, 16, 1024),
                                sdesc_sw128(st + kABoxBytes + ks * 2048, kWBoxBytes, 1024), idesc,
                                (kb > 0 || ks > 0) ? 1u : 0u);
-                    mma_commit(bar(kBarEmpty + s));
+                    mma_commit(bar(Lay::kBarEmpty + s));
                     ++it;
                 }
-                if (ok) mma_commit(bar(kBarAccFull + b));
+                if (ok) mma_commit(bar(Lay::kBarAccFull + b));
             }
             if (!ok) raise_device_error(p.err_word, HATTN_ETIMEOUT);
             // All issued MMAs must complete before TMEM is released.
-            mma_commit(bar(kBarDrain));
-            mbar_wait(bar(kBarDrain), 0);
+            mma_commit(bar(Lay::kBarDrain));
+            mbar_wait(bar(Lay::kBarDrain), 0);
         }
         __syncwarp();
     } else {
@@ -285,6 +326,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = q * 32 + lane;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
         const uint32_t peer = rank ^ 1u;
+        if constexpr (kNorm) {
+            // This CTA's columns of gamma, beta and the bias (the same for all its tiles),
+            // staged while the first mainloop runs; all four epilogue warps come here
+            // before any wait, so the named barrier cannot be left waiting.
+            const TileGeom g0 = tile_geom<kNorm>(p, 0, rank);
+            float* vec = reinterpret_cast<float*>(smem + Lay::kOffVec);
+            for (int c = r; c < g0.bn; c += kEpiThreads) {
+                vec[c] = p.gamma[g0.n0 + c];
+                vec[kBN + c] = p.beta[g0.n0 + c];
+                vec[2 * kBN + c] = p.prob[0].bias ? p.prob[0].bias[g0.n0 + c] : 0.0f;
+            }
+            named_sync(1, kEpiThreads);
+        }
         uint32_t i = 0;
         bool ok = true;
         for (int t = tr.first; ok && t < p.tiles; t += tr.stride, ++i) {
@@ -292,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const GemmProblem& pr = p.prob[g.p];
             const uint32_t b = i & 1;
             {
-                const bool got = mbar_wait(bar(kBarAccFull + b), (i >> 1) & 1);
+                const bool got = mbar_wait(bar(Lay::kBarAccFull + b), (i >> 1) & 1);
                 ok = __all_sync(0xffffffffu, got);
             }
             if (!ok) break;
@@ -328,74 +382,109 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else {
                 const int N = pr.N;
-                const __nv_bfloat16* xrow = p.x + (size_t)row * N + g.n0;
+                {
+                    const bool got = mbar_wait(bar(Lay::kBarXFull), i & 1);
+                    ok = __all_sync(0xffffffffu, got);
+                }
+                if (!ok) break;
+                // Row r of residual box j sits at kOffX + j * 16 KB + r * 128 B, its 16-byte
+                // chunks permuted by the 128-byte swizzle (chunk k at k ^ (r % 8)).
+                const uint8_t* xbase = smem + Lay::kOffX + r * 128;
                 // Pass 1: z = acc [+ bias] + x, kept in TMEM; partial row sum.
                 float sum = 0.0f;
                 for (int c = 0; c < nchunks; ++c) {
                     uint32_t z[32];
                     tmem_ld_x32(acc + 32 * c, z);
-                    uint4 xv[4] = {};
-                    if (valid) {
-                        const uint4* src = reinterpret_cast<const uint4*>(xrow + 32 * c);
+                    uint4 xv[4];
 #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4) xv[v4] = src[v4];
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        const int kc = (c % 2) * 4 + v4;
+                        xv[v4] = *reinterpret_cast<const uint4*>(xbase + (c / 2) * kABoxBytes + ((kc ^ (r & 7)) * 16));
                     }
                     const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(xv);
+                    const float4* bias4 = reinterpret_cast<const float4*>(smem + Lay::kOffVec + 2 * kBN * 4) + 8 * c;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        float zi = __uint_as_float(z[e]) + __bfloat162float(xb[e]);
-                        if (pr.bias) zi += __ldg(pr.bias + g.n0 + 32 * c + e);
-                        sum += zi;
-                        z[e] = __float_as_uint(zi);
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const float4 bv = bias4[e4];
+                        const float bb[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int e = 4 * e4 + u;
+                            const float zi = __uint_as_float(z[e]) + __bfloat162float(xb[e]) + bb[u];
+                            sum += zi;
+                            z[e] = __float_as_uint(zi);
+                        }
                     }
                     tmem_st_x32(acc + 32 * c, z);
                 }
                 tmem_st_wait();
-                if (p.split == 2) {
-                    float other = 0.0f;
-                    const bool got = exchange_partial(sum, other, sbase, 0, kBarSum, i & 1, r, peer);
-                    ok = __all_sync(0xffffffffu, got);
-                    sum += other;
-                }
-                const float mean = sum / static_cast<float>(N);
-                // Pass 2: biased variance about the mean.
+                // Pass 2: squared deviations about this CTA's own mean (two passes, robust).
+                const float n_own = static_cast<float>(g.bn);
+                const float m_own = sum / n_own;
                 float sq = 0.0f;
-                for (int c = 0; ok && c < nchunks; ++c) {
+                for (int c = 0; c < nchunks; ++c) {
                     uint32_t z[32];
                     tmem_ld_x32(acc + 32 * c, z);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
-                        const float dz = __uint_as_float(z[e]) - mean;
+                        const float dz = __uint_as_float(z[e]) - m_own;
                         sq = fmaf(dz, dz, sq);
                     }
                 }
-                if (ok && p.split == 2) {
-                    float other = 0.0f;
-                    const bool got = exchange_partial(sq, other, sbase, 4 * kBM, kBarSq, i & 1, r, peer);
+                float mean = m_own;
+                if (p.split == 2) {
+                    // One exchange of (mean, M2) with the peer's half of the row, merged by
+                    // the pairwise formula: M2 = M2_a + M2_b + (m_a - m_b)^2 n_a n_b / N.
+                    float m_peer = 0.0f, sq_peer = 0.0f;
+                    const bool got = exchange_pair<kNorm>(m_own, sq, m_peer, sq_peer, sbase, i & 1, r, peer);
                     ok = __all_sync(0xffffffffu, got);
-                    sq += other;
+                    const float n_peer = static_cast<float>(N) - n_own;
+                    const float delta = m_own - m_peer;
+                    mean = (n_own * m_own + n_peer * m_peer) / static_cast<float>(N);
+                    sq = sq + sq_peer + delta * delta * (n_own * n_peer / static_cast<float>(N));
                 }
                 const float rstd = 1.0f / sqrtf(sq / static_cast<float>(N) + p.eps);
-                // Pass 3: normalise, scale, shift, round once to bf16.
-                __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(pr.c) + (size_t)row * N + g.n0;
+                // Pass 3: normalise, scale, shift, round once to bf16, into the residual
+                // buffer (same swizzled 128 x 64 boxes), which TMA then stores.
+                const float4* gam4 = reinterpret_cast<const float4*>(smem + Lay::kOffVec);
+                const float4* bet4 = reinterpret_cast<const float4*>(smem + Lay::kOffVec + kBN * 4);
+                uint8_t* ybase = smem + Lay::kOffX + r * 128;
                 for (int c = 0; ok && c < nchunks; ++c) {
                     uint32_t z[32];
                     tmem_ld_x32(acc + 32 * c, z);
                     uint32_t w[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int col = g.n0 + 32 * c + 2 * e;
-                        const float y0 = (__uint_as_float(z[2 * e]) - mean) * rstd * __ldg(p.gamma + col) +
-                                         __ldg(p.beta + col);
-                        const float y1 = (__uint_as_float(z[2 * e + 1]) - mean) * rstd *
-                                             __ldg(p.gamma + col + 1) + __ldg(p.beta + col + 1);
-                        w[e] = pack_bf16x2(y0, y1);
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const float4 gv = gam4[8 * c + e4], bv = bet4[8 * c + e4];
+                        const float y0 = (__uint_as_float(z[4 * e4]) - mean) * rstd * gv.x + bv.x;
+                        const float y1 = (__uint_as_float(z[4 * e4 + 1]) - mean) * rstd * gv.y + bv.y;
+                        const float y2 = (__uint_as_float(z[4 * e4 + 2]) - mean) * rstd * gv.z + bv.z;
+                        const float y3 = (__uint_as_float(z[4 * e4 + 3]) - mean) * rstd * gv.w + bv.w;
+                        w[2 * e4] = pack_bf16x2(y0, y1);
+                        w[2 * e4 + 1] = pack_bf16x2(y2, y3);
                     }
-                    if (valid) {
 #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4)
-                            st_global_v4(yrow + 32 * c + 8 * v4, w[4 * v4], w[4 * v4 + 1],
-                                         w[4 * v4 + 2], w[4 * v4 + 3]);
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        const int kc = (c % 2) * 4 + v4;
+                        *reinterpret_cast<uint4*>(ybase + (c / 2) * kABoxBytes + ((kc ^ (r & 7)) * 16)) =
+                            make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+                    }
+                }
+                // All rows written (each warp's writes made visible to the async proxy):
+                // one thread stores the tile (map a2) and, once the stores have read the
+                // buffer, frees it for the next tile's residual.
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(Lay::kBarYReady));
+                if (warp == 2 && lane == 0) {
+                    if (mbar_wait(bar(Lay::kBarYReady), i & 1)) {
+                        for (int j = 0; j < nchunks / 2; ++j)
+                            tma_store_2d(&a2, sbase + Lay::kOffX + j * kABoxBytes, g.n0 + 64 * j, g.m0);
+                        bulk_commit_group();
+                        bulk_wait_group_read_all();
+                        mbar_arrive(bar(Lay::kBarXEmpty));
+                    } else {
+                        raise_device_error(p.err_word, HATTN_ETIMEOUT);
                     }
                 }
                 if (!ok) break;
@@ -403,9 +492,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // The accumulator has been read: the MMA warp may reuse it.
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarAccEmpty + b));
+            if (lane == 0) mbar_arrive(bar(Lay::kBarAccEmpty + b));
         }
         if (!ok) raise_device_error(p.err_word, HATTN_ETIMEOUT);
+        if (kNorm && warp == 2 && lane == 0) bulk_wait_group_all();
     }
 
     tc_fence_before();
@@ -431,6 +521,7 @@ template <bool kNorm>
 cudaError_t launch(const CUtensorMap* a, const CUtensorMap* w, const GemmParams& p, int grid,
                    int cluster, cudaStream_t stream)
 {
+    constexpr int kSmemBytes = Layout<kNorm>::kSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<kNorm>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -439,13 +530,15 @@ cudaError_t launch(const CUtensorMap* a, const CUtensorMap* w, const GemmParams&
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, gemm_kernel<kNorm>, a[0], a[1], a[2], w[0], w[1], w[2], p);
 }
 
@@ -504,7 +597,7 @@ cudaError_t launch_outproj_ln(const OutProjLnArgs& args, cudaStream_t stream, in
     p.split = N > kBN ? 2 : 1;
     p.n_half = ((N / 2 + 63) / 64) * 64;
     p.tiles = (args.M + kBM - 1) / kBM;
-    const CUtensorMap a[3] = {args.a, args.a, args.a};
+    const CUtensorMap a[3] = {args.a, args.xmap, args.ymap};  // a[1]: residual, a[2]: output
     const CUtensorMap w[3] = {args.wo, args.wo, args.wo};
     int grid;
     if (p.split == 2) grid = 2 * std::min(p.tiles, sm_count() / 2);

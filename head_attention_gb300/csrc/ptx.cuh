@@ -188,6 +188,56 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// 2-D tiled tensor store shared -> global (a bulk async-group; rows and columns
+// past the tensor's extent are not written). The shared-memory writes it reads
+// must be made visible to the async proxy first (fence_proxy_async_smem).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Waits until the committed bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_group_read_all()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Waits until the committed bulk stores have completed.
+__device__ __forceinline__ void bulk_wait_group_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ programmatic dependent launch
+
+// Waits until the grids this one depends on (launched before it on the stream
+// with programmatic serialization) have completed and their writes are
+// visible; a no-op when there is no such grid. Every global read of a
+// predecessor's output, and every global write, must come after it.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next grid on the stream start launching (its CTAs then run their
+// own set-up on free SMs and wait in griddep_wait).
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ named barriers
 
 // Waits until `count` threads (this one included) have reached barrier `id`.
