@@ -45,8 +45,8 @@ struct BwdParams {
     void* dq;
     void* dk;
     void* dv;
-    float* dsum;  // D, fp32 [B, h, nqp]
-    float* lse2;  // base-2 log-sum-exp, fp32 [B, h, nqp]
+    float* dsum;  // -D, fp32 [B, h, nqp]
+    float* lse2;  // minus the base-2 log-sum-exp, fp32 [B, h, nqp]
     int B, h, n_q, n_k, d_k, d_v, nqp;
     float scale;
     int mask_kind;
@@ -71,8 +71,9 @@ __device__ __forceinline__ void stage(float* dst, int ld, const T* src, size_t s
     }
 }
 
-// D_t = dO_t . O_t and lse2_t = lse_t log2(e) for every (b, head, t) with t
-// over the padded rows (0 and +inf past n_q). A group of kL lanes (a power of
+// -D_t = -(dO_t . O_t) and -lse2_t = -lse_t log2(e) for every (b, head, t)
+// with t over the padded rows (0 and -inf past n_q); stored negated so that the
+// kernels add them in packed fp32 instructions. A group of kL lanes (a power of
 // two) covers one row with 16-byte loads, groups of a warp take consecutive
 // rows, and the partial dot products meet by shuffles within the group.
 template <typename T, int kL>
@@ -103,8 +104,8 @@ __global__ void __launch_bounds__(kThreads) row_dot_kernel(const BwdParams p)
 #pragma unroll
     for (int off = kL / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (in && gl == 0) {
-        p.dsum[row] = acc;
-        p.lse2[row] = t < p.n_q ? p.lse[bh * p.n_q + t] * 1.4426950408889634f : INFINITY;
+        p.dsum[row] = -acc;
+        p.lse2[row] = t < p.n_q ? -p.lse[bh * p.n_q + t] * 1.4426950408889634f : -INFINITY;
     }
 }
 
@@ -181,7 +182,7 @@ __global__ void __launch_bounds__(kThreads) key_grads_kernel(const BwdParams p)
             const float* vr = v_s + jl * dvp;
             for (int c = 0; c < p.d_v; ++c) dp = fmaf(gr[c], vr[c], dp);
             const float pr = visible ? expf(p.scale * s - lse_s[lane]) : 0.0f;
-            const float ds = pr * (dp - d_s[lane]);
+            const float ds = pr * (dp + d_s[lane]);  // d_s holds -D
             for (int ii = 0; ii < kInner; ++ii) {
                 const float pi = __shfl_sync(0xffffffffu, pr, ii);
                 const float dsi = __shfl_sync(0xffffffffu, ds, ii);
@@ -273,7 +274,7 @@ __global__ void __launch_bounds__(kThreads) query_grads_kernel(const BwdParams p
             const float* vr = v_s + lane * dvp;
             for (int c = 0; c < p.d_v; ++c) dp = fmaf(gr[c], vr[c], dp);
             const float pr = visible ? expf(p.scale * s - lse_r[u]) : 0.0f;
-            const float ds = pr * (dp - d_r[u]);
+            const float ds = pr * (dp + d_r[u]);  // d_r holds -D
             for (int jj = 0; jj < kInner; ++jj) {
                 const float dsj = __shfl_sync(0xffffffffu, ds, jj);
 #pragma unroll

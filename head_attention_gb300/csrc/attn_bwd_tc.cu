@@ -78,8 +78,8 @@ struct BwdTcParams {
     int mask_kind;
     float scale, scale_log2;
     const int32_t* key_lens;
-    const float* lse2;  // [B, h, nqp], base-2 log-sum-exp of scale*q.k (+inf past n_q)
-    const float* dsum;  // [B, h, nqp], D = dO . O (0 past n_q)
+    const float* lse2;  // [B, h, nqp], minus the base-2 log-sum-exp of scale*q.k (-inf past n_q)
+    const float* dsum;  // [B, h, nqp], -D = -(dO . O) (0 past n_q)
     __nv_bfloat16* dq;
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
@@ -263,31 +263,63 @@ __device__ __forceinline__ void key_grads_tc(const CUtensorMap& tm_q, const CUte
             ok = __all_sync(0xffffffffu, got);
             if (!ok) break;
             tc_fence_after();
-            const float* lse_s = reinterpret_cast<const float*>(smem + C::kOffStage + s * C::kStageBytes + 2 * T::kBytes);
-            const float* d_s = lse_s + 128;
+            // Per query column: -lse2 and -D of this stage (16-byte broadcast reads).
+            const float* nlse_s = reinterpret_cast<const float*>(smem + C::kOffStage + s * C::kStageBytes + 2 * T::kBytes);
+            const float* nd_s = nlse_s + 128;
             // Keys at or past the length, or after every query of the block (causal), see nothing.
             const bool row_live = key_ok && !(causal && key > q0 + 127);
             const bool diag = causal && key0 + 127 > q0;  // this block straddles the diagonal
+            // Without the diagonal or the query tail, no element of the block is masked.
+            const bool plain = !diag && q0 + 127 < p.n_q;
+            const uint64_t c2 = f32x2(p.scale_log2, p.scale_log2);
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t sv[32], pv[32];
                 tmem_ld_x32(lane_base + C::kColS + 32 * c, sv);
                 tmem_ld_x32(lane_base + C::kColDP + 32 * c, pv);
                 uint32_t pk[16], dk[16];
+                if (plain) {
+                    const float4* l4 = reinterpret_cast<const float4*>(nlse_s + 32 * c);
+                    const float4* d4 = reinterpret_cast<const float4*>(nd_s + 32 * c);
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float pr[2], ds[2];
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const float4 L = l4[e4], Dn = d4[e4];
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int col = 32 * c + e + u;
-                        const int q = q0 + col;
-                        const bool vis = row_live && q < p.n_q && !(diag && key > q);
-                        const float x = fmaf(__uint_as_float(sv[e + u]), p.scale_log2, -lse_s[col]);
-                        pr[u] = vis ? ex2_approx(x) : 0.0f;
-                        ds[u] = pr[u] * (__uint_as_float(pv[e + u]) - d_s[col]);
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const int e = 4 * e4 + 2 * h2;
+                            const uint64_t x2 = fma_f32x2(f32x2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2,
+                                                          h2 ? f32x2(L.z, L.w) : f32x2(L.x, L.y));
+                            float x0, x1;
+                            f32x2_split(x2, x0, x1);
+                            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                            const uint64_t t2 = add_f32x2(f32x2(__uint_as_float(pv[e]), __uint_as_float(pv[e + 1])),
+                                                          h2 ? f32x2(Dn.z, Dn.w) : f32x2(Dn.x, Dn.y));
+                            float t0, t1;
+                            f32x2_split(t2, t0, t1);
+                            pk[e / 2] = pack_bf16x2(p0, p1);
+                            dk[e / 2] = pack_bf16x2(p0 * t0, p1 * t1);
+                        }
                     }
-                    pk[e / 2] = pack_bf16x2(pr[0], pr[1]);
-                    dk[e / 2] = pack_bf16x2(ds[0], ds[1]);
+                    if (!row_live) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) pk[e] = dk[e] = 0u;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float pr[2], ds[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int col = 32 * c + e + u;
+                            const int q = q0 + col;
+                            const bool vis = row_live && q < p.n_q && !(diag && key > q);
+                            const float x = fmaf(__uint_as_float(sv[e + u]), p.scale_log2, nlse_s[col]);
+                            pr[u] = vis ? ex2_approx(x) : 0.0f;
+                            ds[u] = pr[u] * (__uint_as_float(pv[e + u]) + nd_s[col]);
+                        }
+                        pk[e / 2] = pack_bf16x2(pr[0], pr[1]);
+                        dk[e / 2] = pack_bf16x2(ds[0], ds[1]);
+                    }
                 }
                 // bf16 P^T over S^T's columns [16c, 16c + 16), dS^T over dP^T's: both
                 // regions were read up to column 32c + 31 already.
@@ -453,8 +485,10 @@ __device__ __forceinline__ void query_grads_tc(const CUtensorMap& tm_q, const CU
         const int r = warp * 32 + lane;
         const int q = q0 + r;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        const float lse2 = q < p.n_q ? p.lse2[((size_t)b * p.h + head) * p.nqp + q] : 0.0f;
-        const float dsum = q < p.n_q ? p.dsum[((size_t)b * p.h + head) * p.nqp + q] : 0.0f;
+        const float nlse2 = q < p.n_q ? p.lse2[((size_t)b * p.h + head) * p.nqp + q] : 0.0f;  // -lse2
+        const float nd = q < p.n_q ? p.dsum[((size_t)b * p.h + head) * p.nqp + q] : 0.0f;     // -D
+        const uint64_t c2 = f32x2(p.scale_log2, p.scale_log2);
+        const uint64_t nl2 = f32x2(nlse2, nlse2), nd2 = f32x2(nd, nd);
         const bool row_ok = q < p.n_q;
         bool ok = true;
         for (int j = 0; ok && j < nblk; ++j) {
@@ -469,18 +503,34 @@ __device__ __forceinline__ void query_grads_tc(const CUtensorMap& tm_q, const CU
                 tmem_ld_x32(lane_base + C::kColS + 32 * c, sv);
                 tmem_ld_x32(lane_base + C::kColDP + 32 * c, pv);
                 uint32_t dk[16];
+                if (!edge) {
+                    // No key of the block is masked, so the packed path needs no per-element
+                    // test (a query row past n_q is zeroed whole).
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float ds[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int key = k0 + 32 * c + e + u;
-                        const bool vis = row_ok && !(edge && (key >= kv_len || (causal && key > q)));
-                        const float x = fmaf(__uint_as_float(sv[e + u]), p.scale_log2, -lse2);
-                        const float pr = vis ? ex2_approx(x) : 0.0f;
-                        ds[u] = pr * (__uint_as_float(pv[e + u]) - dsum);
+                    for (int e = 0; e < 32; e += 2) {
+                        const uint64_t x2 = fma_f32x2(f32x2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2, nl2);
+                        float x0, x1;
+                        f32x2_split(x2, x0, x1);
+                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        const uint64_t t2 = add_f32x2(f32x2(__uint_as_float(pv[e]), __uint_as_float(pv[e + 1])), nd2);
+                        float t0, t1;
+                        f32x2_split(t2, t0, t1);
+                        dk[e / 2] = pack_bf16x2(row_ok ? p0 * t0 : 0.0f, row_ok ? p1 * t1 : 0.0f);
                     }
-                    dk[e / 2] = pack_bf16x2(ds[0], ds[1]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float ds[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int key = k0 + 32 * c + e + u;
+                            const bool vis = row_ok && !(key >= kv_len || (causal && key > q));
+                            const float x = fmaf(__uint_as_float(sv[e + u]), p.scale_log2, nlse2);
+                            const float pr = vis ? ex2_approx(x) : 0.0f;
+                            ds[u] = pr * (__uint_as_float(pv[e + u]) + nd);
+                        }
+                        dk[e / 2] = pack_bf16x2(ds[0], ds[1]);
+                    }
                 }
                 tmem_st_x16(lane_base + C::kColS + 16 * c, dk);
             }

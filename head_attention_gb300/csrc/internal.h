@@ -51,9 +51,9 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const vo
 bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int n, int h, int d, int box_rows);
 
 // Attention backward: dQ, dK, dV from Q, K, V, O, dO and the forward's row
-// log-sum-exp. Scratch (fp32, rows padded to nqp = n_q rounded up to 128):
-// dsum [B, h, nqp] = dO . O (0 past n_q) and lse2 [B, h, nqp] = lse * log2(e)
-// (+inf past n_q), both written by the preparation kernel.
+// log-sum-exp. Scratch (fp32, rows padded to nqp = n_q rounded up to 128), both
+// written negated by the preparation kernel: dsum [B, h, nqp] = -(dO . O) (0
+// past n_q) and lse2 [B, h, nqp] = -lse * log2(e) (-inf past n_q).
 struct AttnBwdArgs {
     const void* q;
     const void* k;

@@ -220,6 +220,11 @@ WORKLOADS = {
         mask_kind=MASK_CAUSAL, seed=10, kind="bwd",
         description="attention backward (dQ, dK, dV), causal self-attention, bf16, B=16 h=8 "
                     "n=512 d=64"),
+    "attn_bwd_long_d128": Workload(
+        "attn_bwd_long_d128", "bf16", B=4, h=16, n_q=8192, n_k=8192, d_k=128, d_v=128,
+        mask_kind=MASK_CAUSAL, seed=11, kind="bwd",
+        description="attention backward (dQ, dK, dV) of the long-sequence causal self-attention, "
+                    "bf16, B=4 h=16 n=8192 d=128"),
     "long_causal_d128": Workload(
         "long_causal_d128", "bf16", B=4, h=16, n_q=8192, n_k=8192, d_k=128, d_v=128,
         mask_kind=MASK_CAUSAL, seed=4,
