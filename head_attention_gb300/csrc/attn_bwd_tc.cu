@@ -9,9 +9,10 @@
 // ("读懂 Attention Is All You Need", §参数是怎样学出来的？); these are the chain
 // rule applied to the forward (§六步算完一行注意力).
 //
-// Two CTA kinds in one grid, no atomics, both with 6 warps: warps 0-3 own TMEM lanes 0-127
-// (one row each: a key in the first kernel, a query in the second), warp 4
-// issues the TMA copies, warp 5 (one thread) the tcgen05 MMAs and owns TMEM.
+// Two CTA kinds in one grid, no atomics, both with 10 warps: warps w and w + 4
+// (w < 4) own TMEM lanes 32w .. 32w + 31 (one row each: a key in the first
+// kernel, a query in the second) and split each block's 128 columns in halves;
+// warp 8 issues the TMA copies, warp 9 (one thread) the tcgen05 MMAs and owns TMEM.
 //
 //   key_grads_tc:   a CTA keeps one 128-key block of K and V in shared memory
 //                   and streams 128-query blocks of Q, dO, lse2 and D through a
@@ -36,9 +37,10 @@
 namespace hattn {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kWarpLoad = 4;
-constexpr int kWarpMma = 5;
+constexpr int kThreads = 320;
+constexpr int kWarpLoad = 8;
+constexpr int kWarpMma = 9;
+constexpr int kRowWarps = 8;
 constexpr uint32_t kBoxBytes = 128 * 64 * 2;  // 128 rows x 64 bf16 columns
 constexpr int kStages = 2;
 
@@ -61,16 +63,19 @@ __device__ __forceinline__ void mma_abt(uint32_t d_tmem, uint64_t a_desc, uint64
     }
 }
 
-// Acc (+)= X . T where X is 128 x 128 bf16 in TMEM (pairs packed in 64 columns)
-// and T a 128-row tile used MN-major (its D columns are the output columns).
+// Acc (+)= X . T where X is 128 x 128 bf16 in TMEM and T a 128-row tile used
+// MN-major (its D columns are the output columns). X's column pairs are packed
+// in two runs of 32 TMEM columns, at x_tmem (X columns 0-63) and x_tmem + 64
+// (X columns 64-127): each half is written by its own row warp inside the
+// columns it has already read.
 template <int D>
 __device__ __forceinline__ void mma_xt(uint32_t d_tmem, uint32_t x_tmem, uint64_t t_desc,
                                        bool accumulate)
 {
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks)
-        mma_ts(d_tmem, x_tmem + ks * 8, t_desc + ((ks * 2048) >> 4), Tile<D>::kIdescAcc,
-               (accumulate || ks > 0) ? 1u : 0u);
+        mma_ts(d_tmem, x_tmem + (ks / 4) * 64 + (ks % 4) * 8, t_desc + ((ks * 2048) >> 4),
+               Tile<D>::kIdescAcc, (accumulate || ks > 0) ? 1u : 0u);
 }
 
 struct BwdTcParams {
@@ -175,7 +180,7 @@ __device__ __forceinline__ void key_grads_tc(const CUtensorMap& tm_q, const CUte
             mbar_init(bar(C::kBarEmpty + s), 1);
         }
         mbar_init(bar(C::kBarS), 1);
-        mbar_init(bar(C::kBarP), 4);
+        mbar_init(bar(C::kBarP), kRowWarps);
         mbar_init(bar(C::kBarO), 1);
         mbar_init(bar(C::kBarDrain), 1);
         fence_barrier_init();
@@ -249,34 +254,39 @@ __device__ __forceinline__ void key_grads_tc(const CUtensorMap& tm_q, const CUte
         }
         __syncwarp();
     } else {
-        // Row warps: thread r owns key key0 + r (TMEM lane r).
-        const int r = warp * 32 + lane;
+        // Row warps: warp w owns keys key0 + 32 (w % 4) .. + 31 (the TMEM lanes of
+        // its quadrant) and query columns [64 (w / 4), 64 (w / 4) + 64) of each block.
+        const int quad = warp % 4, half = warp / 4;
+        const int r = quad * 32 + lane;
         const int key = key0 + r;
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         const bool key_ok = key < kv_len;
         const size_t off = ((size_t)b * p.n_k + key) * row_elems + (size_t)head * D;
+        const uint64_t c2 = f32x2(p.scale_log2, p.scale_log2);
         bool ok = true;
-        for (int i = 0; ok && i < nblk; ++i) {
+        for (int i = 0; i < nblk; ++i) {
             const int s = i % kStages;
             const int q0 = (qb_first + i) * 128;
-            const bool got = mbar_wait(bar(C::kBarFull + s), (i / kStages) & 1) && mbar_wait(bar(C::kBarS), i & 1);
-            ok = __all_sync(0xffffffffu, got);
-            if (!ok) break;
+            if (ok) {
+                const bool got = mbar_wait(bar(C::kBarFull + s), (i / kStages) & 1) && mbar_wait(bar(C::kBarS), i & 1);
+                ok = __all_sync(0xffffffffu, got);
+            }
+            if (!ok) continue;
             tc_fence_after();
             // Per query column: -lse2 and -D of this stage (16-byte broadcast reads).
-            const float* nlse_s = reinterpret_cast<const float*>(smem + C::kOffStage + s * C::kStageBytes + 2 * T::kBytes);
+            const float* nlse_s = reinterpret_cast<const float*>(smem + C::kOffStage + s * C::kStageBytes + 2 * T::kBytes) + 64 * half;
             const float* nd_s = nlse_s + 128;
             // Keys at or past the length, or after every query of the block (causal), see nothing.
             const bool row_live = key_ok && !(causal && key > q0 + 127);
             const bool diag = causal && key0 + 127 > q0;  // this block straddles the diagonal
             // Without the diagonal or the query tail, no element of the block is masked.
             const bool plain = !diag && q0 + 127 < p.n_q;
-            const uint64_t c2 = f32x2(p.scale_log2, p.scale_log2);
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
+                const uint32_t col = 64 * half + 32 * c;  // this chunk's first S^T / dP^T column
                 uint32_t sv[32], pv[32];
-                tmem_ld_x32(lane_base + C::kColS + 32 * c, sv);
-                tmem_ld_x32(lane_base + C::kColDP + 32 * c, pv);
+                tmem_ld_x32(lane_base + C::kColS + col, sv);
+                tmem_ld_x32(lane_base + C::kColDP + col, pv);
                 uint32_t pk[16], dk[16];
                 if (plain) {
                     const float4* l4 = reinterpret_cast<const float4*>(nlse_s + 32 * c);
@@ -310,38 +320,39 @@ __device__ __forceinline__ void key_grads_tc(const CUtensorMap& tm_q, const CUte
                         float pr[2], ds[2];
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
-                            const int col = 32 * c + e + u;
-                            const int q = q0 + col;
+                            const int q = q0 + col + e + u;
                             const bool vis = row_live && q < p.n_q && !(diag && key > q);
-                            const float x = fmaf(__uint_as_float(sv[e + u]), p.scale_log2, nlse_s[col]);
+                            const float x = fmaf(__uint_as_float(sv[e + u]), p.scale_log2, nlse_s[32 * c + e + u]);
                             pr[u] = vis ? ex2_approx(x) : 0.0f;
-                            ds[u] = pr[u] * (__uint_as_float(pv[e + u]) + nd_s[col]);
+                            ds[u] = pr[u] * (__uint_as_float(pv[e + u]) + nd_s[32 * c + e + u]);
                         }
                         pk[e / 2] = pack_bf16x2(pr[0], pr[1]);
                         dk[e / 2] = pack_bf16x2(ds[0], ds[1]);
                     }
                 }
-                // bf16 P^T over S^T's columns [16c, 16c + 16), dS^T over dP^T's: both
-                // regions were read up to column 32c + 31 already.
-                tmem_st_x16(lane_base + C::kColS + 16 * c, pk);
-                tmem_st_x16(lane_base + C::kColDP + 16 * c, dk);
+                // bf16 P^T over S^T's columns [64 half + 16 c, + 16), dS^T over dP^T's:
+                // columns this warp has already read.
+                tmem_st_x16(lane_base + C::kColS + 64 * half + 16 * c, pk);
+                tmem_st_x16(lane_base + C::kColDP + 64 * half + 16 * c, dk);
             }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::kBarP));
         }
+        // Each warp of the quadrant stores half of the D columns of dV and dK.
+        constexpr int kHalfD = D / 2;
         if (nblk == 0) {
             if (key < p.n_k) {
-                zero_row(p.dk + off, D);
-                zero_row(p.dv + off, D);
+                zero_row(p.dk + off + kHalfD * half, kHalfD);
+                zero_row(p.dv + off + kHalfD * half, kHalfD);
             }
         } else if (ok) {
             ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarO), 0));
             if (ok) {
                 tc_fence_after();
-                store_row(p.dv + off, lane_base + C::kColDV, D, 1.0f, key < p.n_k);
-                store_row(p.dk + off, lane_base + C::kColDK, D, p.scale, key < p.n_k);
+                store_row(p.dv + off + kHalfD * half, lane_base + C::kColDV + kHalfD * half, kHalfD, 1.0f, key < p.n_k);
+                store_row(p.dk + off + kHalfD * half, lane_base + C::kColDK + kHalfD * half, kHalfD, p.scale, key < p.n_k);
             }
         }
         if (!ok) raise_device_error(p.err_word, HATTN_ETIMEOUT);
@@ -415,7 +426,7 @@ __device__ __forceinline__ void query_grads_tc(const CUtensorMap& tm_q, const CU
             mbar_init(bar(C::kBarEmpty + s), 1);
         }
         mbar_init(bar(C::kBarS), 1);
-        mbar_init(bar(C::kBarP), 4);
+        mbar_init(bar(C::kBarP), kRowWarps);
         mbar_init(bar(C::kBarO), 1);
         mbar_init(bar(C::kBarDrain), 1);
         fence_barrier_init();
@@ -481,27 +492,30 @@ __device__ __forceinline__ void query_grads_tc(const CUtensorMap& tm_q, const CU
         }
         __syncwarp();
     } else {
-        // Row warps: thread r owns query q0 + r.
-        const int r = warp * 32 + lane;
+        // Row warps: warp w owns queries q0 + 32 (w % 4) .. + 31 and key columns
+        // [64 (w / 4), 64 (w / 4) + 64) of each block.
+        const int quad = warp % 4, half = warp / 4;
+        const int r = quad * 32 + lane;
         const int q = q0 + r;
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         const float nlse2 = q < p.n_q ? p.lse2[((size_t)b * p.h + head) * p.nqp + q] : 0.0f;  // -lse2
         const float nd = q < p.n_q ? p.dsum[((size_t)b * p.h + head) * p.nqp + q] : 0.0f;     // -D
         const uint64_t c2 = f32x2(p.scale_log2, p.scale_log2);
         const uint64_t nl2 = f32x2(nlse2, nlse2), nd2 = f32x2(nd, nd);
         const bool row_ok = q < p.n_q;
         bool ok = true;
-        for (int j = 0; ok && j < nblk; ++j) {
+        for (int j = 0; j < nblk; ++j) {
             const int k0 = j * 128;
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarS), j & 1));
-            if (!ok) break;
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarS), j & 1));
+            if (!ok) continue;
             tc_fence_after();
             const bool edge = (k0 + 128 > kv_len) || (causal && k0 + 127 > q0);
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
+                const uint32_t col = 64 * half + 32 * c;
                 uint32_t sv[32], pv[32];
-                tmem_ld_x32(lane_base + C::kColS + 32 * c, sv);
-                tmem_ld_x32(lane_base + C::kColDP + 32 * c, pv);
+                tmem_ld_x32(lane_base + C::kColS + col, sv);
+                tmem_ld_x32(lane_base + C::kColDP + col, pv);
                 uint32_t dk[16];
                 if (!edge) {
                     // No key of the block is masked, so the packed path needs no per-element
@@ -523,7 +537,7 @@ __device__ __forceinline__ void query_grads_tc(const CUtensorMap& tm_q, const CU
                         float ds[2];
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
-                            const int key = k0 + 32 * c + e + u;
+                            const int key = k0 + col + e + u;
                             const bool vis = row_ok && !(key >= kv_len || (causal && key > q));
                             const float x = fmaf(__uint_as_float(sv[e + u]), p.scale_log2, nlse2);
                             const float pr = vis ? ex2_approx(x) : 0.0f;
@@ -532,19 +546,21 @@ __device__ __forceinline__ void query_grads_tc(const CUtensorMap& tm_q, const CU
                         dk[e / 2] = pack_bf16x2(ds[0], ds[1]);
                     }
                 }
-                tmem_st_x16(lane_base + C::kColS + 16 * c, dk);
+                // bf16 dS over S's columns [64 half + 16 c, + 16), already read.
+                tmem_st_x16(lane_base + C::kColS + 64 * half + 16 * c, dk);
             }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::kBarP));
         }
+        constexpr int kHalfD = D / 2;
         if (ok) {
             ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarO), 0));
             if (ok) {
                 tc_fence_after();
-                store_row(p.dq + ((size_t)b * p.n_q + q) * row_elems + (size_t)head * D,
-                          lane_base + C::kColDQ, D, p.scale, row_ok);
+                store_row(p.dq + ((size_t)b * p.n_q + q) * row_elems + (size_t)head * D + kHalfD * half,
+                          lane_base + C::kColDQ + kHalfD * half, kHalfD, p.scale, row_ok);
             }
         }
         if (!ok) raise_device_error(p.err_word, HATTN_ETIMEOUT);
