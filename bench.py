@@ -447,12 +447,19 @@ def _setup_attention(w, inp):
     kl = None if inp["key_lens"] is None else torch.from_numpy(inp["key_lens"]).cuda()
     out = torch.empty((w.B, w.n_q, w.h, w.d_v), dtype=q.dtype, device="cuda")
 
-    def step():
-        hattn.attn_fwd(q, k, v, out=out, scale=w.scale, mask_kind=w.mask_kind, key_lens=kl)
+    def bind(q, k, v, out):
+        def step():
+            hattn.attn_fwd(q, k, v, out=out, scale=w.scale, mask_kind=w.mask_kind, key_lens=kl)
+        return step
+
+    def rebind():
+        """The same step on a second set of device buffers (for the pipelined e2e leg)."""
+        q2, k2, v2, o2 = (torch.empty_like(t) for t in (q, k, v, out))
+        return {"q": (inp["q"], q2), "k": (inp["k"], k2), "v": (inp["v"], v2)}, o2, bind(q2, k2, v2, o2)
 
     host = {"inputs": {"q": (inp["q"], q), "k": (inp["k"], k), "v": (inp["v"], v)},
-            "output": out}
-    return step, host, 1
+            "output": out, "rebind": rebind}
+    return bind(q, k, v, out), host, 1
 
 
 def _setup_mha(w, inp):
@@ -771,10 +778,77 @@ def run_gpu(args, rank, world, local):
     return result
 
 
+def e2e_pipelined(args, w, host, step, flops, world, pinned):
+    """The e2e leg with copies overlapped across steps: two sets of device
+    buffers and three streams (host-to-device, compute, device-to-host). Step i
+    still copies its own inputs in and its own result out; its compute runs
+    while step i+1's inputs arrive and step i-1's result leaves."""
+    import torch
+    sets = []
+    for k in range(2):
+        if k == 0:
+            inputs, out, fn = host["inputs"], host["output"], step
+        else:
+            inputs, out, fn = host["rebind"]()
+        pairs = [(pinned(h), d) for h, d in inputs.values()]
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        sets.append((pairs, out, hout, fn))
+    s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = [{n: torch.cuda.Event() for n in ("in", "run", "out")} for _ in range(2)]
+    for e in ev:  # every buffer starts free
+        for n in ("run", "out"):
+            e[n].record(torch.cuda.current_stream())
+
+    def e2e_step(i):
+        pairs, out, hout, fn = sets[i % 2]
+        e = ev[i % 2]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(e["run"])   # the previous compute on these buffers is done
+            for h, d in pairs:
+                d.copy_(h, non_blocking=True)
+            e["in"].record(s_in)
+        with torch.cuda.stream(s_run):
+            s_run.wait_event(e["in"])
+            s_run.wait_event(e["out"])  # the previous result left this output buffer
+            fn()
+            e["run"].record(s_run)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(e["run"])
+            hout.copy_(out, non_blocking=True)
+            e["out"].record(s_out)
+
+    steps = max(1, min(args.steps, 100))
+    for i in range(4):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    main = torch.cuda.current_stream()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(main)
+    for s in (s_in, s_run, s_out):
+        s.wait_event(start)
+    for i in range(steps):
+        e2e_step(i)
+    for s in (s_in, s_run, s_out):
+        main.wait_stream(s)
+    end.record(main)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = reduce_max(start.elapsed_time(end), world) / steps
+    h2d = sum(h.numel() * h.element_size() for h, _ in sets[0][0])
+    d2h = sets[0][2].numel() * sets[0][2].element_size()
+    return {"value": round(flops * world / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4), "steps": steps, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "launches": steps,
+            "pipeline": "2 buffer sets; host-to-device / compute / device-to-host streams"}
+
+
 def e2e_leg(args, w, host, step, flops, world):
     """Same metric through the public API with host buffers: every step copies
     the step's inputs from pinned host memory to the device, runs the eager
-    call, and copies the result back to pinned host memory."""
+    call, and copies the result back to pinned host memory (overlapped across
+    steps where the workload can bind its step to a second buffer set)."""
     import numpy as np
     import torch
 
@@ -784,6 +858,9 @@ def e2e_leg(args, w, host, step, flops, world):
         t = t.pin_memory()
         return t if w.dtype == "f32" else t.view(torch.bfloat16)
 
+    in_bytes = sum(np.asarray(h).nbytes for h, _ in host["inputs"].values())
+    if "rebind" in host and in_bytes >= (8 << 20):  # small steps: stream overhead would dominate
+        return e2e_pipelined(args, w, host, step, flops, world, pinned)
     pairs = [(pinned(h), d) for h, d in host["inputs"].values()]
     out = host["output"]
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
