@@ -17,35 +17,42 @@
 // is loaded as soon as the previous unit's last S MMA of that tile retired,
 // and a tile's epilogue overlaps its first S MMA of the next unit.
 // 12 warps in three warpgroups; a register split gives the softmax warps 208
-// registers and the control warps 72.
-//   warp 8      TMA: the unit's Q tiles, then K_j (128 keys) through a
+// registers and the control warps 72. The control warps come first: the warp
+// schedulers favour lower-numbered warps among the ready ones, and an MMA
+// issuer that waits behind a busy softmax warp for issue slots delays the
+// tensor pipe (measured: 7% at D=64, 3% at D=128).
+//   warp 0      TMA: the unit's Q tiles, then K_j (128 keys) through a
 //               3-stage (D=128) / 5-stage (D=64) shared-memory ring.
-//   warp 10     TMA: V_j through a 2-stage (D=128) / 4-stage (D=64) ring. K
-//               runs one block ahead of V because S(j+1) follows PV(j).
-//   warps 9, 11 MMA issuers, one thread per tile: S_t = Q_t K_j^T into TMEM,
+//   warp 2      TMA: V_j through a 2-stage (D=128) / 4-stage (D=64) ring. K
+//               runs one block ahead of V because S(j+1) precedes PV(j) (D=64)
+//               or follows it at once (D=128).
+//   warps 1, 3  MMA issuers, one thread per tile: S_t = Q_t K_j^T into TMEM,
 //               then per block PV_t(j) (O_t += P_t V_j, P_t read from TMEM)
-//               followed at once by S_t(j+1). Completion is reported by
-//               tcgen05.commit onto mbarriers. With one issuer per tile, a tile
-//               whose P is ready never waits behind the other tile's MMA issue,
-//               and one tile's softmax overlaps the other tile's MMAs.
-//   warps 0-3   softmax of tile 0, warps 4-7 softmax of tile 1, taking turns
+//               and S_t(j+1). Completion is reported by tcgen05.commit onto
+//               mbarriers. With one issuer per tile, a tile whose P is ready
+//               never waits behind the other tile's MMA issue, and one tile's
+//               softmax overlaps the other tile's MMAs.
+//   warps 4-7   softmax of tile 0, warps 8-11 softmax of tile 1, taking turns
 //               on the exponentials (two named barriers), so that the MUFU work
 //               of one tile overlaps the MMAs of the other: thread r owns
 //               query row r (TMEM lane r), so the row max and row sum are
 //               thread-local. Streaming softmax in base 2: running max m and
-//               sum l, p = 2^(s*scale*log2e - m), P stored back to TMEM as bf16
-//               over the first half of S's columns. The exponentials of a block
-//               use the running max while the block's own max is computed
-//               alongside; O is rescaled (and the block redone) only when a
-//               row's max grows by more than 2^8. The final 1/l uses the same
-//               max as the numerator, so the result is unchanged; p <= 2^8.
+//               sum l, p = 2^(s*scale*log2e - m), P stored back to TMEM as bf16.
+//               The exponentials of a block use the running max while the
+//               block's own max is computed alongside; O is rescaled (and the
+//               block redone) only when a row's max grows by more than 2^8. The
+//               final 1/l uses the same max as the numerator, so the result is
+//               unchanged; p <= 2^8.
 //   Causal: key blocks above the diagonal are never loaded or multiplied; only
 //   the diagonal block is masked element-wise. Key padding: blocks at or past
 //   key_lens[b] are skipped and the last block is masked column-wise.
 //   Epilogue (softmax warps): O / l packed to bf16, 16-byte stores into
 //   [B, n_q, h, D].
 //
-// TMEM columns: tile t holds S at [256t, 256t+128) and O at [256t+128, 256t+128+D).
+// TMEM columns (tile t owns [256t, 256t+256)): D = 128: S at +0, P over S's
+// first 64 columns, O at +128; S(j+1) then waits for PV(j). D = 64: S at +0,
+// P at +128, O at +192; S(j+1) is computed as soon as the softmax has read
+// S(j) out, while block j's exponentials run.
 // Every mbarrier wait is bounded; on a timeout the CTA records HATTN_ETIMEOUT in
 // the device error word, drains its own copies and MMAs, frees TMEM and exits.
 #include <cuda_bf16.h>
@@ -66,10 +73,11 @@ namespace hattn {
 namespace {
 
 constexpr int kThreads = 384;
-constexpr int kWarpLoadK = 8;
-constexpr int kWarpMma0 = 9;   // MMA issuer of tile 0 (also owns the TMEM allocation)
-constexpr int kWarpLoadV = 10;
-constexpr int kWarpMma1 = 11;  // MMA issuer of tile 1
+constexpr int kWarpLoadK = 0;
+constexpr int kWarpMma0 = 1;   // MMA issuer of tile 0 (also owns the TMEM allocation)
+constexpr int kWarpLoadV = 2;
+constexpr int kWarpMma1 = 3;   // MMA issuer of tile 1
+constexpr int kWarpSoftmax0 = 4;  // warps 4-7 softmax of tile 0, 8-11 of tile 1
 // Launched at 168 registers per thread (384 x 168 = 64512 of the SM's 65536).
 constexpr int kRegsSoftmax = 208;
 constexpr int kRegsControl = 72;
@@ -105,7 +113,18 @@ struct Cfg {
     static constexpr int kBarP = kBarS + 2;              // 2: P_t written (one arrival per warp)
     static constexpr int kBarO = kBarP + 2;              // 2: final O_t ready
     static constexpr int kBarDrain = kBarO + 2;  // 2: one per issuer
-    static constexpr int kNumBars = kBarDrain + 2;
+    // Separate P columns only: S_t read out of TMEM (one arrival per warp), and
+    // PV_t(j) retired for a block that is not the tile's last.
+    static constexpr int kBarSFree = kBarDrain + 2;
+    static constexpr int kBarPVDone = kBarSFree + 2;
+    static constexpr int kNumBars = kBarPVDone + 2;
+    // TMEM columns inside a tile's 256. With D = 64 P gets columns of its own
+    // (S 128 + P 64 + O 64), so S(j+1) can be computed while block j's
+    // exponentials run; with D = 128 P is written over the first half of S.
+    static constexpr bool kSepP = (D == 64);
+    static constexpr uint32_t kColP = kSepP ? 128u : 0u;
+    static constexpr uint32_t kColO = kSepP ? 192u : 128u;
+    static_assert(kColO + D <= 256, "TMEM columns of a tile");
     static constexpr int kOffSlot = kOffBar + 8 * kNumBars;  // TMEM base address + abort flag
     static constexpr int kSmemUsed = kOffSlot + 16;
     static constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base to 1024 B
@@ -330,7 +349,7 @@ template <int D, bool kTable, class Sched>
 __device__ void issue_tile_mmas(Cta c, const TcParams& p, const Sched& sch, int t)
 {
     using C = Cfg<D>;
-    const uint32_t tS = c.tmem + 256u * t, tO = tS + 128u;
+    const uint32_t tS = c.tmem + 256u * t, tP = tS + C::kColP, tO = tS + C::kColO;
     // K-major Q/K tiles: SBO = 1024 (8-row groups); MN-major V: LBO = one 64-column box.
     const uint64_t q_desc = sdesc_sw128(c.sbase + C::kOffQ + t * C::kTileBytes, 16, 1024);
     const uint64_t k_desc0 = sdesc_sw128(c.sbase + C::kOffK, 16, 1024);
@@ -339,6 +358,7 @@ __device__ void issue_tile_mmas(Cta c, const TcParams& p, const Sched& sch, int 
     auto vdesc = [&](uint32_t s) { return v_desc0 + static_cast<uint64_t>((s * C::kTileBytes) >> 4); };
 
     uint32_t kc = 0, vc = 0, pc = 0, qn = 0;  // K / V blocks, P handoffs, Q tiles so far
+    uint32_t sfc = 0;                         // S read-outs waited for (separate P only)
     bool ok = true;
     UnitIter<kTable> it;
     for (int slot; ok && (slot = it.next(p, sch)) >= 0;) {
@@ -371,6 +391,35 @@ __device__ void issue_tile_mmas(Cta c, const TcParams& p, const Sched& sch, int 
             const uint32_t sv = vi % C::kVStages, phv = (vi / C::kVStages) & 1;
             const uint32_t sk1 = ki % C::kKStages, phk1 = (ki / C::kKStages) & 1;
             const bool has_next = j + 1 < R;
+            if constexpr (C::kSepP) {
+                // S(j+1) first: it only needs the softmax to have read S(j) out of TMEM.
+                if (has_next) {
+                    if (!mbar_wait(c.bar(C::kBarKFull + sk1), phk1)) { ok = false; break; }
+                    if (j + 1 < nb) {
+                        if (c.aborted() || !mbar_wait(c.bar(C::kBarSFree + t), sfc & 1)) { ok = false; break; }
+                        ++sfc;
+                        tc_fence_after();
+                        issue_qk<D>(tS, q_desc, kdesc(sk1));
+                        mma_commit(c.bar(C::kBarS + t));
+                        mma_commit(c.bar(C::kBarKEmpty + sk1));
+                        if (j + 1 == nb - 1) mma_commit(c.bar(C::kBarQEmpty + t));
+                    } else {
+                        mbar_arrive(c.bar(C::kBarKEmpty + sk1));
+                    }
+                }
+                if (!mbar_wait(c.bar(C::kBarVFull + sv), phv)) { ok = false; break; }
+                if (j < nb) {
+                    if (c.aborted() || !mbar_wait(c.bar(C::kBarP + t), pc & 1)) { ok = false; break; }
+                    ++pc;
+                    tc_fence_after();
+                    issue_pv<D>(tO, tP, vdesc(sv), j > 0);
+                    mma_commit(c.bar(j == nb - 1 ? C::kBarO + t : C::kBarPVDone + t));
+                    mma_commit(c.bar(C::kBarVEmpty + sv));
+                } else {
+                    mbar_arrive(c.bar(C::kBarVEmpty + sv));
+                }
+                continue;
+            }
             if (!mbar_wait(c.bar(C::kBarVFull + sv), phv)) { ok = false; break; }
             if (j < nb) {
                 if (c.aborted() || !mbar_wait(c.bar(C::kBarP + t), pc & 1)) { ok = false; break; }
@@ -411,7 +460,7 @@ __device__ void issue_tile_mmas(Cta c, const TcParams& p, const Sched& sch, int 
 // ---------------------------------------------------------------- softmax + epilogue
 
 // p = 2^(s * c - m) for the 128 scores of this thread's row, packed to bf16 and
-// stored over the first 64 TMEM columns of S; the fp32 sum goes to acc. With
+// stored into 64 TMEM columns from p_taddr; the fp32 sum goes to acc. With
 // kMax, the row max of the raw scores is computed alongside (on the ALU pipe,
 // while the exponentials occupy MUFU and FMA) and returned.
 template <bool kMax>
@@ -472,9 +521,10 @@ __device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, 
     using C = Cfg<D>;
     const int r = wq * 32 + lane;
     const uint32_t lane_base = c.tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    const uint32_t cS = 256u * t, cO = 256u * t + 128u;
+    const uint32_t cS = 256u * t, cP = cS + C::kColP, cO = cS + C::kColO;
     const uint32_t my_turn = t ? kTurn1 : kTurn0, other_turn = t ? kTurn0 : kTurn1;
     uint32_t sc = 0, oc = 0;  // S blocks and O results waited for so far
+    uint32_t pvc = 0;         // PV retirements waited for (separate P only)
     bool ok = true;
     UnitIter<kTable> it;
     for (int slot; (slot = it.next(p, sch)) >= 0;) {
@@ -512,6 +562,14 @@ __device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, 
             if (work && ok) {
                 tc_fence_after();
                 tmem_ld_x128(lane_base + cS, sr);
+                if constexpr (C::kSepP) {
+                    // S is in registers: the issuer may overwrite it with S(j+1).
+                    if (j + 1 < nb) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(c.bar(C::kBarSFree + t));
+                    }
+                }
                 const int kbase = j * 128;
                 const bool need_mask = (kbase + 128 > c.kv_len) || (c.causal && kbase + 127 > my_row0);
                 if (need_mask) {
@@ -526,6 +584,16 @@ __device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, 
                 if (j == 0) m_used = row_max(sr) * p.scale_log2;
             }
             if (kPingPong) named_sync(my_turn, 256);
+            if constexpr (C::kSepP) {
+                // PV(j-1) must have read P before it is overwritten (and O must be
+                // complete before a rescale).
+                if (work && ok && j > 0) {
+                    const bool got = mbar_wait(c.bar(C::kBarPVDone + t), pvc & 1);
+                    ++pvc;
+                    ok = __all_sync(0xffffffffu, got);
+                    tc_fence_after();
+                }
+            }
             if (work && ok) {
                 // p = 2^(s * scale * log2(e) - m) with the running max m (scale > 0, so
                 // the max of scale * s is scale * max s). After the first block the
@@ -533,7 +601,7 @@ __device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, 
                 // grows by more than 2^8 (rare) rescales O and l and redoes the block.
                 const uint64_t c2 = f32x2(p.scale_log2, p.scale_log2);
                 uint64_t acc[4] = {0, 0, 0, 0};
-                const float mx = exp_block<true>(sr, c2, f32x2(-m_used, -m_used), acc, lane_base + cS) *
+                const float mx = exp_block<true>(sr, c2, f32x2(-m_used, -m_used), acc, lane_base + cP) *
                                  p.scale_log2;
                 const bool grow = j > 0 && mx > m_used + kRescaleLog2;
                 if (__any_sync(0xffffffffu, grow)) {
@@ -550,7 +618,7 @@ __device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, 
                     l *= alpha;
                     m_used = m_new;
                     acc[0] = acc[1] = acc[2] = acc[3] = 0;
-                    exp_block<false>(sr, c2, f32x2(-m_used, -m_used), acc, lane_base + cS);
+                    exp_block<false>(sr, c2, f32x2(-m_used, -m_used), acc, lane_base + cP);
                 }
                 if (kPingPong && (t == 0 || j + 1 < R)) named_arrive(other_turn, 256);
                 float a0, a1;
@@ -642,6 +710,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(c.bar(C::kBarS + t), 1);
             mbar_init(c.bar(C::kBarP + t), 4);
             mbar_init(c.bar(C::kBarO + t), 1);
+            mbar_init(c.bar(C::kBarSFree + t), 4);
+            mbar_init(c.bar(C::kBarPVDone + t), 1);
         }
         mbar_init(c.bar(C::kBarDrain), 1);
         mbar_init(c.bar(C::kBarDrain + 1), 1);
@@ -665,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     griddep_wait();
     griddep_launch_dependents();
 
-    if (warp >= 8) {
+    if (warp < kWarpSoftmax0) {
         regs_dec<kRegsControl>();
         if (lane == 0) {
             if (warp == kWarpLoadK) produce_qk<D, kTable>(c, p, sch, &tm_q, &tm_k);
@@ -676,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         regs_inc<kRegsSoftmax>();
-        softmax_tile<D, kTable, kLse>(c, p, sch, warp / 4, warp % 4, lane);
+        softmax_tile<D, kTable, kLse>(c, p, sch, (warp - kWarpSoftmax0) / 4, warp % 4, lane);
     }
 
     tc_fence_before();

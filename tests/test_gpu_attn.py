@@ -158,6 +158,30 @@ def test_padding_contents_are_bitwise_invisible(dtype, d):
     assert torch().equal(out1, out2)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("mask_kind", [0, 1])
+def test_growing_row_max_is_rescaled(d, mask_kind):
+    # Scores that climb with the key index (q_0 = 1, k_j0 = j / 16, scale 1):
+    # every 128-key block raises the row max by 8 = 2^3 in base e, i.e. by more
+    # than 2^8 in the base-2 exponent, so the running sum and O are rescaled at
+    # every block and the result must still match the oracle.
+    n = 700
+    w = _sweep_workload("bf16", 2, 2, n, n, d, d, mask_kind)
+    inp = synth.attn_inputs(w)
+    q = synth.widen(inp["q"], "bf16").copy()
+    k = synth.widen(inp["k"], "bf16").copy()
+    q[..., 1:] *= 0.25  # keeps the random part of the scores small against the ramp
+    q[..., 0] = 1.0
+    k[..., 0] = (np.arange(n) / 16.0)[None, :, None]
+    qb, kb = synth.round_to_bf16_bits(q), synth.round_to_bf16_bits(k)
+    qd, kd, vd = to_device(qb, "bf16"), to_device(kb, "bf16"), to_device(inp["v"], "bf16")
+    got = from_device(hattn.attn_fwd(qd, kd, vd, scale=1.0, mask_kind=mask_kind))
+    assert hattn.check_device_error() == 0
+    ref = oracle.attn(synth.widen(qb, "bf16"), synth.widen(kb, "bf16"), synth.widen(inp["v"], "bf16"),
+                      1.0, mask_kind, None)
+    assert_close(got, ref, "bf16", f"growing max d={d}")
+
+
 @pytest.mark.parametrize("dtype,d", [("bf16", 64), ("bf16", 128), ("f32", 64)])
 def test_weights_sum_to_one(dtype, d):
     # V = 1 everywhere: every output is the sum of the row's weights, i.e. 1.
