@@ -9,10 +9,12 @@
 // ("读懂 Attention Is All You Need", §参数是怎样学出来的？); these are the chain
 // rule applied to the forward (§六步算完一行注意力).
 //
-// Two CTA kinds in one grid, no atomics, both with 10 warps: warps w and w + 4
-// (w < 4) own TMEM lanes 32w .. 32w + 31 (one row each: a key in the first
-// kernel, a query in the second) and split each block's 128 columns in halves;
-// warp 8 issues the TMA copies, warp 9 (one thread) the tcgen05 MMAs and owns TMEM.
+// Two CTA kinds in one grid, no atomics, both with 10 warps: warp 0 issues the
+// TMA copies, warp 1 (one thread) the tcgen05 MMAs and owns TMEM (the control
+// warps come first because the warp schedulers favour lower-numbered ready
+// warps); row warps 2-9: warp w owns TMEM lanes 32 (w % 4) .. + 31 (one row
+// each: a key in the first kernel, a query in the second), and warps 2-5 and
+// 6-9 take the two halves of each block's 128 columns.
 //
 //   key_grads_tc:   a CTA keeps one 128-key block of K and V in shared memory
 //                   and streams 128-query blocks of Q, dO, lse2 and D through a
@@ -38,8 +40,9 @@ namespace hattn {
 namespace {
 
 constexpr int kThreads = 320;
-constexpr int kWarpLoad = 8;
-constexpr int kWarpMma = 9;
+constexpr int kWarpLoad = 0;
+constexpr int kWarpMma = 1;
+constexpr int kWarpRow0 = 2;  // row warps 2-9
 constexpr int kRowWarps = 8;
 constexpr uint32_t kBoxBytes = 128 * 64 * 2;  // 128 rows x 64 bf16 columns
 constexpr int kStages = 2;
@@ -255,8 +258,8 @@ __device__ __forceinline__ void key_grads_tc(const CUtensorMap& tm_q, const CUte
         __syncwarp();
     } else {
         // Row warps: warp w owns keys key0 + 32 (w % 4) .. + 31 (the TMEM lanes of
-        // its quadrant) and query columns [64 (w / 4), 64 (w / 4) + 64) of each block.
-        const int quad = warp % 4, half = warp / 4;
+        // its quadrant) and query columns [64 half, 64 half + 64) of each block.
+        const int quad = warp % 4, half = (warp - kWarpRow0) / 4;
         const int r = quad * 32 + lane;
         const int key = key0 + r;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
@@ -493,8 +496,8 @@ __device__ __forceinline__ void query_grads_tc(const CUtensorMap& tm_q, const CU
         __syncwarp();
     } else {
         // Row warps: warp w owns queries q0 + 32 (w % 4) .. + 31 and key columns
-        // [64 (w / 4), 64 (w / 4) + 64) of each block.
-        const int quad = warp % 4, half = warp / 4;
+        // [64 half, 64 half + 64) of each block.
+        const int quad = warp % 4, half = (warp - kWarpRow0) / 4;
         const int r = quad * 32 + lane;
         const int q = q0 + r;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
