@@ -206,7 +206,13 @@ struct UnitIter {
 
 // Unit order: groups of group_heads (b, i) heads; within a group, query pairs
 // from the heaviest (causal: the last rows) down, heads inner.
-__device__ __forceinline__ void unit_setup(Cta& c, const TcParams& p, int slot)
+// The per-unit fields of Cta, decoded from a unit slot.
+struct UnitInfo {
+    int b, head, row0, nblk0, nblk1, kv_len;
+    bool valid;
+};
+
+__device__ __forceinline__ UnitInfo unit_decode(const TcParams& p, bool causal, int slot)
 {
     const int per_group = p.group_heads * p.n_pairs;
     const int g = slot / per_group;
@@ -214,21 +220,72 @@ __device__ __forceinline__ void unit_setup(Cta& c, const TcParams& p, int slot)
     const int heads_here = min(p.group_heads, p.B * p.h - g * p.group_heads);
     const int pi = w / heads_here;
     const int bh = g * p.group_heads + (w - pi * heads_here);
-    const int pair = c.causal ? p.n_pairs - 1 - pi : pi;
-    c.b = bh / p.h;
-    c.head = bh % p.h;
-    c.row0[0] = pair * kRowsPerCta;
-    c.row0[1] = c.row0[0] + 128;
-    c.kv_len = (p.mask_kind & HATTN_MASK_KEY_PADDING) ? p.key_lens[c.b] : p.n_k;
-    c.valid = c.kv_len >= 1 && c.kv_len <= p.n_k;
-    const int kv_blocks = (c.kv_len + 127) / 128;
+    const int pair = causal ? p.n_pairs - 1 - pi : pi;
+    UnitInfo u;
+    u.b = bh / p.h;
+    u.head = bh % p.h;
+    u.row0 = pair * kRowsPerCta;
+    u.kv_len = (p.mask_kind & HATTN_MASK_KEY_PADDING) ? p.key_lens[u.b] : p.n_k;
+    u.valid = u.kv_len >= 1 && u.kv_len <= p.n_k;
+    const int kv_blocks = (u.kv_len + 127) / 128;
+    int nb[2];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-        if (!c.valid || c.row0[t] >= p.n_q) c.nblk[t] = 0;
-        else c.nblk[t] = c.causal ? min(kv_blocks, c.row0[t] / 128 + 1) : kv_blocks;
+        const int row0 = u.row0 + 128 * t;
+        if (!u.valid || row0 >= p.n_q) nb[t] = 0;
+        else nb[t] = causal ? min(kv_blocks, row0 / 128 + 1) : kv_blocks;
     }
-    c.nblk_max = max(c.nblk[0], c.nblk[1]);
+    u.nblk0 = nb[0];
+    u.nblk1 = nb[1];
+    return u;
 }
+
+__device__ __forceinline__ void unit_apply(Cta& c, const UnitInfo& u)
+{
+    c.b = u.b;
+    c.head = u.head;
+    c.row0[0] = u.row0;
+    c.row0[1] = u.row0 + 128;
+    c.kv_len = u.kv_len;
+    c.valid = u.valid;
+    c.nblk[0] = u.nblk0;
+    c.nblk[1] = u.nblk1;
+    c.nblk_max = max(u.nblk0, u.nblk1);
+}
+
+__device__ __forceinline__ void unit_setup(Cta& c, const TcParams& p, int slot)
+{
+    unit_apply(c, unit_decode(p, c.causal, slot));
+}
+
+// The unit slots of this CTA with the next one decoded ahead: a role calls
+// prefetch() where it waits anyway (so the integer divisions, the key-length
+// load and the rarely run code behind them leave its critical path) and
+// advance() at its unit boundary. Measured on the cross-attention workload,
+// decoding at the boundary kept the MMA issuer ~1.5k cycles per unit from its
+// next S MMA.
+template <bool kTable>
+struct UnitAhead {
+    UnitIter<kTable> it;
+    int slot = -2;  // -2: the next slot is not fetched yet; -1: no more units
+    UnitInfo info;
+    template <class Sched>
+    __device__ __forceinline__ void prefetch(const Cta& c, const TcParams& p, const Sched& sch)
+    {
+        if (slot != -2) return;
+        slot = it.next(p, sch);
+        if (slot >= 0) info = unit_decode(p, c.causal, slot);
+    }
+    template <class Sched>
+    __device__ __forceinline__ bool advance(Cta& c, const TcParams& p, const Sched& sch)
+    {
+        prefetch(c, p, sch);
+        if (slot < 0) return false;
+        unit_apply(c, info);
+        slot = -2;
+        return true;
+    }
+};
 
 __device__ __forceinline__ void give_up(const Cta& c, int* err_word)
 {
@@ -365,13 +422,12 @@ __device__ void issue_tile_mmas(Cta c, const TcParams& p, const Sched& sch, int 
     uint32_t kc = 0, vc = 0, pc = 0, qn = 0;  // K / V blocks, P handoffs, Q tiles so far
     uint32_t sfc = 0;                         // S read-outs waited for (separate P only)
     bool ok = true;
-    UnitIter<kTable> it;
-    for (int slot; ok && (slot = it.next(p, sch)) >= 0;) {
+    UnitAhead<kTable> units;
+    while (ok && units.advance(c, p, sch)) {
         if (c.aborted()) {
             ok = false;
             break;
         }
-        unit_setup(c, p, slot);
         const int nb = t ? c.nblk[1] : c.nblk[0], R = c.nblk_max;
         if (R == 0) continue;
         if (nb > 0) {
@@ -391,6 +447,7 @@ __device__ void issue_tile_mmas(Cta c, const TcParams& p, const Sched& sch, int 
                 mbar_arrive(c.bar(C::kBarKEmpty + s));
             }
         }
+        units.prefetch(c, p, sch);  // while this unit's blocks are waited for
         for (int j = 0; ok && j < R; ++j) {
             const uint32_t vi = vc + j, ki = kc + j + 1;
             const uint32_t sv = vi % C::kVStages, phv = (vi / C::kVStages) & 1;
@@ -531,9 +588,8 @@ __device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, 
     uint32_t sc = 0, oc = 0;  // S blocks and O results waited for so far
     uint32_t pvc = 0;         // PV retirements waited for (separate P only)
     bool ok = true;
-    UnitIter<kTable> it;
-    for (int slot; (slot = it.next(p, sch)) >= 0;) {
-        unit_setup(c, p, slot);
+    UnitAhead<kTable> units;
+    while (units.advance(c, p, sch)) {
         // Selects, not indexing by the runtime tile number (keeps Cta in registers).
         const int my_row0 = t ? c.row0[1] : c.row0[0];
         const int row = my_row0 + r;
@@ -548,6 +604,7 @@ __device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, 
             continue;
         }
         const int nb = t ? c.nblk[1] : c.nblk[0], R = c.nblk_max;
+        units.prefetch(c, p, sch);  // while S(0) is waited for
         float m_used = -INFINITY, l = 0.0f;
         // Turn protocol over the unit's R rounds (every round is taken, with or
         // without work, so both warpgroups pass the named barriers the same number
