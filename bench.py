@@ -64,6 +64,8 @@ def metric_of(w):
 DEFAULT_WORKLOAD = "long_causal_d128"
 NOMINAL_BF16_TFLOPS = 2250.0
 NOMINAL_HBM_GBS = 8000.0
+L2_BYTES = 129e6
+FLUSH_BYTES = 256 << 20  # > L2: written before every timed step when the inputs fit in L2
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = ("head_attention_gb300/csrc/attn_tc.cu", "head_attention_gb300/csrc/ptx.cuh")
@@ -581,6 +583,35 @@ def _setup_bwd(w, inp):
     return step, host, 3
 
 
+def io_bytes(w, inp):
+    """(input bytes, algorithmic bytes moved) of one step: every input read once, the output
+    written once."""
+    esize = 4 if w.dtype == "f32" else 2
+    if w.kind == "mha":
+        bytes_in = (2 * w.B * w.n_q * w.d_model + 4 * w.d_model * w.h * w.d_k) * esize
+        bytes_alg = bytes_in + w.B * w.n_q * w.d_model * esize
+    elif w.kind in ("encoder", "decoder"):
+        n_mha = 1 if w.kind == "encoder" else 2
+        weights = n_mha * 4 * w.d_model * w.h * w.d_k + 2 * w.d_model * w.d_ff
+        acts = w.B * w.n_q * w.d_model + (w.B * w.n_k * w.d_model if w.kind == "decoder" else 0)
+        bytes_in = (acts + weights) * esize
+        bytes_alg = bytes_in + w.B * w.n_q * w.d_model * esize
+    elif w.kind == "bwd":
+        qkv = w.B * (w.n_q * w.h * w.d_k + w.n_k * w.h * (w.d_k + w.d_v))
+        bytes_in = (qkv + 2 * w.B * w.n_q * w.h * w.d_v) * esize + 4 * w.B * w.h * w.n_q
+        bytes_alg = bytes_in + qkv * esize
+    elif w.kind == "decode":
+        bytes_in = (float(inp["key_lens"].sum()) * w.h * (w.d_k + w.d_v) + w.B * w.h * w.d_k) * esize
+        bytes_alg = bytes_in + w.B * w.h * w.d_v * esize
+    elif w.kind == "pe":
+        bytes_in = w.B * w.n_q * w.d_model * esize
+        bytes_alg = 2 * bytes_in
+    else:
+        bytes_in = (w.B * w.n_q * w.h * w.d_k + w.B * w.n_k * w.h * (w.d_k + w.d_v)) * esize
+        bytes_alg = bytes_in + w.B * w.n_q * w.h * w.d_v * esize
+    return bytes_in, bytes_alg
+
+
 def run_gpu(args, rank, world, local):
     import torch
 
@@ -634,23 +665,38 @@ def run_gpu(args, rank, world, local):
         torch.cuda.synchronize()
         run_step = graph.replay
 
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # Inputs that fit in the 129 MB L2 would be served from it after the first
+    # step: then every timed step is preceded by a 256 MB write (outside its
+    # events) and the per-step times are summed.
+    bytes_in, bytes_alg = io_bytes(w, inp)
+    flush_l2 = bytes_in <= L2_BYTES
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda") if flush_l2 else None
+    n_ev = args.steps if flush_l2 else 1
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
     sampler = ClockSampler(gpu_uuid(local))
     with sampler:
         time.sleep(0.25)  # let the sampler start
         barrier(world)
         torch.cuda.synchronize()
         t_wall0 = time.time()
-        start.record(stream)
-        for _ in range(args.steps):
-            run_step()
-        end.record(stream)
+        if flush_l2:
+            for i in range(args.steps):
+                flush.fill_(i & 255)
+                starts[i].record(stream)
+                run_step()
+                ends[i].record(stream)
+        else:
+            starts[0].record(stream)
+            for _ in range(args.steps):
+                run_step()
+            ends[0].record(stream)
         torch.cuda.synchronize()
         t_wall1 = time.time()
         barrier(world)
         sampler.mark(t_wall0, t_wall1)
         time.sleep(0.15)
-    ms_local = start.elapsed_time(end)
+    ms_local = sum(s_.elapsed_time(e_) for s_, e_ in zip(starts, ends))
     if hattn.check_device_error(stream) != 0:
         raise RuntimeError("device error during the timed region")
     ms_total = reduce_max(ms_local, world)
@@ -661,29 +707,6 @@ def run_gpu(args, rank, world, local):
     peaks, peak_src = load_peaks()
     step_ms = ms_local / args.steps
     achieved = flops / (step_ms * 1e-3) / 1e12
-    esize = 4 if w.dtype == "f32" else 2
-    if w.kind == "mha":
-        bytes_in = (2 * w.B * w.n_q * w.d_model + 4 * w.d_model * w.h * w.d_k) * esize
-        bytes_alg = bytes_in + w.B * w.n_q * w.d_model * esize
-    elif w.kind in ("encoder", "decoder"):
-        n_mha = 1 if w.kind == "encoder" else 2
-        weights = n_mha * 4 * w.d_model * w.h * w.d_k + 2 * w.d_model * w.d_ff
-        acts = w.B * w.n_q * w.d_model + (w.B * w.n_k * w.d_model if w.kind == "decoder" else 0)
-        bytes_in = (acts + weights) * esize
-        bytes_alg = bytes_in + w.B * w.n_q * w.d_model * esize
-    elif w.kind == "bwd":
-        qkv = w.B * (w.n_q * w.h * w.d_k + w.n_k * w.h * (w.d_k + w.d_v))
-        bytes_in = (qkv + 2 * w.B * w.n_q * w.h * w.d_v) * esize + 4 * w.B * w.h * w.n_q
-        bytes_alg = bytes_in + qkv * esize
-    elif w.kind == "decode":
-        bytes_in = (float(inp["key_lens"].sum()) * w.h * (w.d_k + w.d_v) + w.B * w.h * w.d_k) * esize
-        bytes_alg = bytes_in + w.B * w.h * w.d_v * esize
-    elif w.kind == "pe":
-        bytes_in = w.B * w.n_q * w.d_model * esize
-        bytes_alg = 2 * bytes_in
-    else:
-        bytes_in = (w.B * w.n_q * w.h * w.d_k + w.B * w.n_k * w.h * (w.d_k + w.d_v)) * esize
-        bytes_alg = bytes_in + w.B * w.n_q * w.h * w.d_v * esize
     tc_attn = w.dtype == "bf16" and w.d_k == w.d_v and w.d_k in (64, 128)
     kernel = {"mha": "mha sublayer: proj_gemm + attn_tc_kernel + outproj_ln (one step)",
               "encoder": "encoder layer: MHA (proj_gemm, attn_tc_kernel, outproj_ln) + FFN "
@@ -751,8 +774,9 @@ def run_gpu(args, rank, world, local):
                    "timing": "CUDA-graph replay of one step" if not args.no_graph else "eager calls",
                    "parallelism": f"replicas x{world} (independent (batch, head) work per GPU)",
                    "l2": (f"inputs {bytes_in / 1e6:.0f} MB > 129 MB L2: streamed from HBM every step, no flush"
-                          if bytes_in > 129e6 else
-                          f"inputs {bytes_in / 1e6:.1f} MB fit in L2: warm-L2 number")},
+                          if not flush_l2 else
+                          f"inputs {bytes_in / 1e6:.1f} MB fit in L2: a {FLUSH_BYTES >> 20} MB write "
+                          "flushes L2 before every timed step (outside its events); step times summed")},
         "tokens_per_s": round(tokens_s, 1),
         "pct_of_measured_bf16_peak": round(100 * tflops / world / peaks["bf16_tflops"], 2),
         "pct_of_nominal_bf16_peak": round(100 * tflops / world / NOMINAL_BF16_TFLOPS, 2),
