@@ -64,6 +64,7 @@
 #include <memory>
 #include <mutex>
 #include <queue>
+#include <type_traits>
 #include <utility>
 #include <vector>
 
@@ -145,7 +146,7 @@ struct TcParams {
     int n_pairs;      // 256-row query pairs per (b, i)
     int units;        // B * h * n_pairs
     int group_heads;  // heads per L2 group in the unit order
-    int issuers;      // 2 when any unit has a second tile (n_q > 128), else 1
+    int issuers;      // 2 when any unit has a second tile, else 1
     const int32_t* key_lens;
     __nv_bfloat16* out;
     float* lse;  // optional [B, h, n_q]
@@ -162,6 +163,12 @@ struct SchedTable {
     uint16_t list[kTableUnits];
 };
 struct SchedSnake {};
+// Query rows that fit one tile (n_q <= 128): a unit's two tiles take two (b, i)
+// heads, units in snake order. A type of its own, so that the other launches
+// compile without the paired bookkeeping.
+struct SchedPaired {};
+template <class Sched>
+constexpr bool kPaired = std::is_same<Sched, SchedPaired>::value;
 
 // Per-CTA state shared by the role functions; the unit fields are rewritten
 // by unit_setup for every unit.
@@ -171,12 +178,15 @@ struct Cta {
     uint32_t tmem;        // TMEM base address
     uint32_t abort_flag;  // shared address of the word set when any wait gave up
     bool causal;
-    int b, head;
-    int row0[2];          // first query row of each tile
-    int nblk[2];          // key blocks each tile multiplies (0: tile absent)
+    // Per tile: the (b, i) head, its first query row, its key blocks (0: tile
+    // absent), its key length and whether that is within [1, n_k]. Both tiles
+    // share one head except in paired units.
+    int b[2], head[2];
+    int row0[2];
+    int nblk[2];
     int nblk_max;
-    int kv_len;
-    bool valid;           // key length within [1, n_k]
+    int kv_len[2];
+    bool valid[2];
     __device__ uint32_t bar(int i) const { return bar0 + 8u * i; }
     __device__ bool aborted() const { return ld_volatile_shared(abort_flag) != 0u; }
 };
@@ -208,12 +218,31 @@ struct UnitIter {
 // from the heaviest (causal: the last rows) down, heads inner.
 // The per-unit fields of Cta, decoded from a unit slot.
 struct UnitInfo {
-    int b, head, row0, nblk0, nblk1, kv_len;
-    bool valid;
+    int b[2], head[2], row0[2], nblk[2], kv_len[2];
+    bool valid[2];
 };
 
+template <bool kPairedUnit>
 __device__ __forceinline__ UnitInfo unit_decode(const TcParams& p, bool causal, int slot)
 {
+    UnitInfo u;
+    if constexpr (kPairedUnit) {
+        // Tile t takes head 2 slot + t (absent past the last head), all its n_q <= 128
+        // query rows in one tile.
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int bh = 2 * slot + t;
+            const bool present = bh < p.B * p.h;
+            u.b[t] = present ? bh / p.h : 0;
+            u.head[t] = present ? bh % p.h : 0;
+            u.row0[t] = 0;
+            u.kv_len[t] = (p.mask_kind & HATTN_MASK_KEY_PADDING) ? p.key_lens[u.b[t]] : p.n_k;
+            u.valid[t] = !present || (u.kv_len[t] >= 1 && u.kv_len[t] <= p.n_k);
+            const int kv_blocks = (u.kv_len[t] + 127) / 128;
+            u.nblk[t] = (present && u.valid[t]) ? (causal ? min(kv_blocks, 1) : kv_blocks) : 0;
+        }
+        return u;
+    }
     const int per_group = p.group_heads * p.n_pairs;
     const int g = slot / per_group;
     const int w = slot - g * per_group;
@@ -221,70 +250,76 @@ __device__ __forceinline__ UnitInfo unit_decode(const TcParams& p, bool causal, 
     const int pi = w / heads_here;
     const int bh = g * p.group_heads + (w - pi * heads_here);
     const int pair = causal ? p.n_pairs - 1 - pi : pi;
-    UnitInfo u;
-    u.b = bh / p.h;
-    u.head = bh % p.h;
-    u.row0 = pair * kRowsPerCta;
-    u.kv_len = (p.mask_kind & HATTN_MASK_KEY_PADDING) ? p.key_lens[u.b] : p.n_k;
-    u.valid = u.kv_len >= 1 && u.kv_len <= p.n_k;
-    const int kv_blocks = (u.kv_len + 127) / 128;
-    int nb[2];
+    const int b = bh / p.h, head = bh % p.h;
+    const int kv_len = (p.mask_kind & HATTN_MASK_KEY_PADDING) ? p.key_lens[b] : p.n_k;
+    const bool valid = kv_len >= 1 && kv_len <= p.n_k;
+    const int kv_blocks = (kv_len + 127) / 128;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-        const int row0 = u.row0 + 128 * t;
-        if (!u.valid || row0 >= p.n_q) nb[t] = 0;
-        else nb[t] = causal ? min(kv_blocks, row0 / 128 + 1) : kv_blocks;
+        u.b[t] = b;
+        u.head[t] = head;
+        u.row0[t] = pair * kRowsPerCta + 128 * t;
+        u.kv_len[t] = kv_len;
+        u.valid[t] = valid;
+        if (!valid || u.row0[t] >= p.n_q) u.nblk[t] = 0;
+        else u.nblk[t] = causal ? min(kv_blocks, u.row0[t] / 128 + 1) : kv_blocks;
     }
-    u.nblk0 = nb[0];
-    u.nblk1 = nb[1];
     return u;
 }
 
 __device__ __forceinline__ void unit_apply(Cta& c, const UnitInfo& u)
 {
-    c.b = u.b;
-    c.head = u.head;
-    c.row0[0] = u.row0;
-    c.row0[1] = u.row0 + 128;
-    c.kv_len = u.kv_len;
-    c.valid = u.valid;
-    c.nblk[0] = u.nblk0;
-    c.nblk[1] = u.nblk1;
-    c.nblk_max = max(u.nblk0, u.nblk1);
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        c.b[t] = u.b[t];
+        c.head[t] = u.head[t];
+        c.row0[t] = u.row0[t];
+        c.kv_len[t] = u.kv_len[t];
+        c.valid[t] = u.valid[t];
+        c.nblk[t] = u.nblk[t];
+    }
+    c.nblk_max = max(u.nblk[0], u.nblk[1]);
 }
 
+template <class Sched>
 __device__ __forceinline__ void unit_setup(Cta& c, const TcParams& p, int slot)
 {
-    unit_apply(c, unit_decode(p, c.causal, slot));
+    unit_apply(c, unit_decode<kPaired<Sched>>(p, c.causal, slot));
 }
 
 // The unit slots of this CTA with the next one decoded ahead: a role calls
 // prefetch() where it waits anyway (so the integer divisions, the key-length
 // load and the rarely run code behind them leave its critical path) and
-// advance() at its unit boundary. Measured on the cross-attention workload,
-// decoding at the boundary kept the MMA issuer ~1.5k cycles per unit from its
-// next S MMA.
-template <bool kTable>
-struct UnitAhead {
+// advance() at its unit boundary. A role keeps only its View of a unit (the
+// fewest live registers). Measured on the cross-attention workload, decoding
+// at the boundary kept the MMA issuer ~1.5k cycles per unit from its next S MMA.
+template <bool kTable, class View>
+struct Ahead {
     UnitIter<kTable> it;
     int slot = -2;  // -2: the next slot is not fetched yet; -1: no more units
-    UnitInfo info;
+    View info;
     template <class Sched>
-    __device__ __forceinline__ void prefetch(const Cta& c, const TcParams& p, const Sched& sch)
+    __device__ __forceinline__ void prefetch(const TcParams& p, const Sched& sch, bool causal, int t)
     {
         if (slot != -2) return;
         slot = it.next(p, sch);
-        if (slot >= 0) info = unit_decode(p, c.causal, slot);
+        if (slot >= 0) info = View::of(unit_decode<kPaired<Sched>>(p, causal, slot), t);
     }
     template <class Sched>
-    __device__ __forceinline__ bool advance(Cta& c, const TcParams& p, const Sched& sch)
+    __device__ __forceinline__ bool advance(View& v, const TcParams& p, const Sched& sch, bool causal, int t)
     {
-        prefetch(c, p, sch);
+        prefetch(p, sch, causal, t);
         if (slot < 0) return false;
-        unit_apply(c, info);
+        v = info;
         slot = -2;
         return true;
     }
+};
+
+// The MMA issuer's view: the key blocks of both tiles.
+struct BlockCounts {
+    int n0, n1;
+    __device__ __forceinline__ static BlockCounts of(const UnitInfo& u, int) { return {u.nblk[0], u.nblk[1]}; }
 };
 
 __device__ __forceinline__ void give_up(const Cta& c, int* err_word)
@@ -336,7 +371,7 @@ __device__ void produce_qk(Cta c, const TcParams& p, const Sched& sch, const CUt
     UnitIter<kTable> it;
     for (int slot; ok && (slot = it.next(p, sch)) >= 0;) {
         if (c.aborted()) break;
-        unit_setup(c, p, slot);
+        unit_setup<Sched>(c, p, slot);
         for (int t = 0; t < 2 && ok; ++t) {
             if (c.nblk[t] == 0) continue;
             // The previous unit's S MMAs of this tile must have finished reading Q_t.
@@ -347,20 +382,25 @@ __device__ void produce_qk(Cta c, const TcParams& p, const Sched& sch, const CUt
             mbar_arrive_expect_tx(c.bar(C::kBarQFull + t), C::kTileBytes);
             for (int x = 0; x < C::kBoxes; ++x)
                 tma_load_4d(c.sbase + C::kOffQ + t * C::kTileBytes + x * kBoxBytes, tm_q,
-                            c.bar(C::kBarQFull + t), x * 64, c.head, c.row0[t], c.b);
+                            c.bar(C::kBarQFull + t), x * 64, c.head[t], c.row0[t], c.b[t]);
             ++qn[t];
         }
+        // K_j of the unit's head (paired units: K_j of tile 0's head, then of tile 1's,
+        // for the tiles that multiply block j), in the order the issuers consume them.
         for (int j = 0; ok && j < c.nblk_max; ++j) {
-            const uint32_t s = kc % C::kKStages;
-            if (c.aborted() || !mbar_wait(c.bar(C::kBarKEmpty + s), ((kc / C::kKStages) & 1) ^ 1)) {
-                ok = false;
-                break;
+            for (int t = 0; ok && t < 2; ++t) {
+                if (kPaired<Sched> ? j >= c.nblk[t] : t > 0) continue;
+                const uint32_t s = kc % C::kKStages;
+                if (c.aborted() || !mbar_wait(c.bar(C::kBarKEmpty + s), ((kc / C::kKStages) & 1) ^ 1)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(c.bar(C::kBarKFull + s), C::kTileBytes);
+                for (int x = 0; x < C::kBoxes; ++x)
+                    tma_load_4d(c.sbase + C::kOffK + s * C::kTileBytes + x * kBoxBytes, tm_k,
+                                c.bar(C::kBarKFull + s), x * 64, c.head[t], j * 128, c.b[t]);
+                ++kc;
             }
-            mbar_arrive_expect_tx(c.bar(C::kBarKFull + s), C::kTileBytes);
-            for (int x = 0; x < C::kBoxes; ++x)
-                tma_load_4d(c.sbase + C::kOffK + s * C::kTileBytes + x * kBoxBytes, tm_k,
-                            c.bar(C::kBarKFull + s), x * 64, c.head, j * 128, c.b);
-            ++kc;
         }
     }
     if (!ok) give_up(c, p.err_word);
@@ -380,18 +420,21 @@ __device__ void produce_v(Cta c, const TcParams& p, const Sched& sch, const CUte
     UnitIter<kTable> it;
     for (int slot; ok && (slot = it.next(p, sch)) >= 0;) {
         if (c.aborted()) break;
-        unit_setup(c, p, slot);
+        unit_setup<Sched>(c, p, slot);
         for (int j = 0; ok && j < c.nblk_max; ++j) {
-            const uint32_t s = vc % C::kVStages;
-            if (c.aborted() || !mbar_wait(c.bar(C::kBarVEmpty + s), ((vc / C::kVStages) & 1) ^ 1)) {
-                ok = false;
-                break;
+            for (int t = 0; ok && t < 2; ++t) {
+                if (kPaired<Sched> ? j >= c.nblk[t] : t > 0) continue;
+                const uint32_t s = vc % C::kVStages;
+                if (c.aborted() || !mbar_wait(c.bar(C::kBarVEmpty + s), ((vc / C::kVStages) & 1) ^ 1)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(c.bar(C::kBarVFull + s), C::kTileBytes);
+                for (int x = 0; x < C::kBoxes; ++x)
+                    tma_load_4d(c.sbase + C::kOffV + s * C::kTileBytes + x * kBoxBytes, tm_v,
+                                c.bar(C::kBarVFull + s), x * 64, c.head[t], j * 128, c.b[t]);
+                ++vc;
             }
-            mbar_arrive_expect_tx(c.bar(C::kBarVFull + s), C::kTileBytes);
-            for (int x = 0; x < C::kBoxes; ++x)
-                tma_load_4d(c.sbase + C::kOffV + s * C::kTileBytes + x * kBoxBytes, tm_v,
-                            c.bar(C::kBarVFull + s), x * 64, c.head, j * 128, c.b);
-            ++vc;
         }
     }
     if (!ok) give_up(c, p.err_word);
@@ -422,21 +465,38 @@ __device__ void issue_tile_mmas(Cta c, const TcParams& p, const Sched& sch, int 
     uint32_t kc = 0, vc = 0, pc = 0, qn = 0;  // K / V blocks, P handoffs, Q tiles so far
     uint32_t sfc = 0;                         // S read-outs waited for (separate P only)
     bool ok = true;
-    UnitAhead<kTable> units;
-    while (ok && units.advance(c, p, sch)) {
+    Ahead<kTable, BlockCounts> units;
+    BlockCounts u;
+    while (ok && units.advance(u, p, sch, c.causal, t)) {
         if (c.aborted()) {
             ok = false;
             break;
         }
-        const int nb = t ? c.nblk[1] : c.nblk[0], R = c.nblk_max;
-        if (R == 0) continue;
+        const int n0 = u.n0, n1 = u.n1;
+        const int nb = t ? n1 : n0;
+        // Rounds this issuer walks: every block of a shared unit (releasing the ones
+        // its tile does not multiply), only its own blocks in a paired unit.
+        const int R = kPaired<Sched> ? nb : max(n0, n1);
+        // The unit's K/V ring entries, and the position of this tile's block j among
+        // them (paired units: block j of tile 0, then of tile 1, for the tiles that have it).
+        const uint32_t entries = static_cast<uint32_t>(kPaired<Sched> ? n0 + n1 : max(n0, n1));
+        auto pos = [&](int j) -> uint32_t {
+            if constexpr (!kPaired<Sched>) return static_cast<uint32_t>(j);
+            return static_cast<uint32_t>(min(j, n0) + min(j, n1) + ((t == 1 && j < n0) ? 1 : 0));
+        };
+        if (R == 0) {
+            kc += entries;
+            vc += entries;
+            continue;
+        }
         if (nb > 0) {
             if (!mbar_wait(c.bar(C::kBarQFull + t), qn & 1)) { ok = false; break; }
             ++qn;
         }
         {
-            const uint32_t s = kc % C::kKStages;
-            if (!mbar_wait(c.bar(C::kBarKFull + s), (kc / C::kKStages) & 1)) { ok = false; break; }
+            const uint32_t k0 = kc + pos(0);
+            const uint32_t s = k0 % C::kKStages;
+            if (!mbar_wait(c.bar(C::kBarKFull + s), (k0 / C::kKStages) & 1)) { ok = false; break; }
             if (nb > 0) {
                 tc_fence_after();
                 issue_qk<D>(tS, q_desc, kdesc(s));
@@ -447,9 +507,9 @@ __device__ void issue_tile_mmas(Cta c, const TcParams& p, const Sched& sch, int 
                 mbar_arrive(c.bar(C::kBarKEmpty + s));
             }
         }
-        units.prefetch(c, p, sch);  // while this unit's blocks are waited for
+        units.prefetch(p, sch, c.causal, t);  // while this unit's blocks are waited for
         for (int j = 0; ok && j < R; ++j) {
-            const uint32_t vi = vc + j, ki = kc + j + 1;
+            const uint32_t vi = vc + pos(j), ki = kc + pos(j + 1);
             const uint32_t sv = vi % C::kVStages, phv = (vi / C::kVStages) & 1;
             const uint32_t sk1 = ki % C::kKStages, phk1 = (ki / C::kKStages) & 1;
             const bool has_next = j + 1 < R;
@@ -510,8 +570,8 @@ __device__ void issue_tile_mmas(Cta c, const TcParams& p, const Sched& sch, int 
                 }
             }
         }
-        kc += R;
-        vc += R;
+        kc += entries;
+        vc += entries;
     }
     if (!ok) give_up(c, p.err_word);
     // All issued MMAs must complete before TMEM is released.
@@ -520,6 +580,27 @@ __device__ void issue_tile_mmas(Cta c, const TcParams& p, const Sched& sch, int 
 }
 
 // ---------------------------------------------------------------- softmax + epilogue
+
+// One tile's view of a unit, all that its softmax warps keep (fewer live
+// registers next to the 128 scores of a row than the whole unit).
+struct TileUnit {
+    int b, head, row0, nb, R, kv_len;
+    bool valid;
+    __device__ __forceinline__ static TileUnit of(const UnitInfo& u, int t);
+};
+
+__device__ __forceinline__ TileUnit TileUnit::of(const UnitInfo& u, int t)
+{
+    TileUnit v;
+    v.b = t ? u.b[1] : u.b[0];
+    v.head = t ? u.head[1] : u.head[0];
+    v.row0 = t ? u.row0[1] : u.row0[0];
+    v.nb = t ? u.nblk[1] : u.nblk[0];
+    v.R = max(u.nblk[0], u.nblk[1]);
+    v.kv_len = t ? u.kv_len[1] : u.kv_len[0];
+    v.valid = t ? u.valid[1] : u.valid[0];
+    return v;
+}
 
 // p = 2^(s * c - m) for the 128 scores of this thread's row, packed to bf16 and
 // stored into 64 TMEM columns from p_taddr; the fp32 sum goes to acc. With
@@ -588,23 +669,26 @@ __device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, 
     uint32_t sc = 0, oc = 0;  // S blocks and O results waited for so far
     uint32_t pvc = 0;         // PV retirements waited for (separate P only)
     bool ok = true;
-    UnitAhead<kTable> units;
-    while (units.advance(c, p, sch)) {
-        // Selects, not indexing by the runtime tile number (keeps Cta in registers).
-        const int my_row0 = t ? c.row0[1] : c.row0[0];
+    Ahead<kTable, TileUnit> units;
+    TileUnit u;
+    while (units.advance(u, p, sch, c.causal, t)) {
+        const int my_row0 = u.row0;
         const int row = my_row0 + r;
-        if (!c.valid) {
-            // Key length outside [1, n_k]: this unit's rows are zero and the error is raised.
-            __nv_bfloat16* orow = p.out + (((size_t)c.b * p.n_q + row) * p.h + c.head) * D;
+        const int my_b = u.b, my_head = u.head;
+        const int kv_len = u.kv_len;
+        if (!u.valid) {
+            // Key length outside [1, n_k]: this tile's rows are zero and the error is
+            // raised. The tile has no blocks, so it still takes the unit's rounds (the
+            // other tile of a paired unit may have work) without doing any.
+            __nv_bfloat16* orow = p.out + (((size_t)my_b * p.n_q + row) * p.h + my_head) * D;
             if (row < p.n_q) {
                 for (int k = 0; k < D; k += 8) st_global_v4(orow + k, 0u, 0u, 0u, 0u);
-                if constexpr (kLse) p.lse[((size_t)c.b * p.h + c.head) * p.n_q + row] = -INFINITY;
+                if constexpr (kLse) p.lse[((size_t)my_b * p.h + my_head) * p.n_q + row] = -INFINITY;
             }
-            if (t == 0 && r == 0) raise_device_error(p.err_word, HATTN_EKEYLEN);
-            continue;
+            if (r == 0) raise_device_error(p.err_word, HATTN_EKEYLEN);
         }
-        const int nb = t ? c.nblk[1] : c.nblk[0], R = c.nblk_max;
-        units.prefetch(c, p, sch);  // while S(0) is waited for
+        const int nb = u.nb, R = u.R;
+        units.prefetch(p, sch, c.causal, t);  // while S(0) is waited for
         float m_used = -INFINITY, l = 0.0f;
         // Turn protocol over the unit's R rounds (every round is taken, with or
         // without work, so both warpgroups pass the named barriers the same number
@@ -633,11 +717,11 @@ __device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, 
                     }
                 }
                 const int kbase = j * 128;
-                const bool need_mask = (kbase + 128 > c.kv_len) || (c.causal && kbase + 127 > my_row0);
+                const bool need_mask = (kbase + 128 > kv_len) || (c.causal && kbase + 127 > my_row0);
                 if (need_mask) {
                     // Key kbase + i is visible iff i < lim (inside the key length and,
                     // when causal, not after this row): one compare per score.
-                    const int lim = min(c.kv_len, c.causal ? row + 1 : c.kv_len) - kbase;
+                    const int lim = min(kv_len, c.causal ? row + 1 : kv_len) - kbase;
 #pragma unroll
                     for (int i = 0; i < 128; ++i)
                         if (i >= lim) sr[i] = __float_as_uint(-INFINITY);
@@ -708,12 +792,12 @@ __device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, 
         // O is in registers after the loads below; the next unit's first PV of this
         // tile (which overwrites O) waits for this warpgroup's next P handoff.
         const float inv = 1.0f / l;
-        __nv_bfloat16* orow = p.out + (((size_t)c.b * p.n_q + row) * p.h + c.head) * D;
+        __nv_bfloat16* orow = p.out + (((size_t)my_b * p.n_q + row) * p.h + my_head) * D;
         // Natural-log log-sum-exp of the scaled scores: the exponentials ran in base 2
         // on s * scale * log2(e) with the running max m, so ln sum = (m + log2 l) ln 2.
         if constexpr (kLse) {
             if (row < p.n_q)
-                p.lse[((size_t)c.b * p.h + c.head) * p.n_q + row] = (m_used + log2f(l)) * 0.6931471805599453f;
+                p.lse[((size_t)my_b * p.h + my_head) * p.n_q + row] = (m_used + log2f(l)) * 0.6931471805599453f;
         }
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) {
@@ -760,13 +844,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(c.bar(C::kBarQFull + t), 1);
             mbar_init(c.bar(C::kBarQEmpty + t), 1);
         }
+        // A K/V entry is released by every issuer of a shared unit, by its own
+        // tile's issuer alone in a paired unit.
+        const uint32_t releases = kPaired<Sched> ? 1u : static_cast<uint32_t>(p.issuers);
         for (int s = 0; s < C::kKStages; ++s) {
             mbar_init(c.bar(C::kBarKFull + s), 1);
-            mbar_init(c.bar(C::kBarKEmpty + s), p.issuers);
+            mbar_init(c.bar(C::kBarKEmpty + s), releases);
         }
         for (int s = 0; s < C::kVStages; ++s) {
             mbar_init(c.bar(C::kBarVFull + s), 1);
-            mbar_init(c.bar(C::kBarVEmpty + s), p.issuers);
+            mbar_init(c.bar(C::kBarVEmpty + s), releases);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(c.bar(C::kBarS + t), 1);
@@ -932,8 +1019,10 @@ cudaError_t launch_d(const AttnArgs& a, const AttnMaps& m)
     p.out = static_cast<__nv_bfloat16*>(a.out);
     p.lse = a.lse;
     p.err_word = a.err_word;
-    p.issuers = a.n_q > 128 ? 2 : 1;
-    const long long units = (long long)p.n_pairs * a.B * a.h;
+    // Query rows that fit one tile: a unit's two tiles take two heads.
+    const bool paired = a.n_q <= 128;
+    p.issuers = (a.n_q > 128 || (paired && (long long)a.B * a.h > 1)) ? 2 : 1;
+    const long long units = paired ? ((long long)a.B * a.h + 1) / 2 : (long long)p.n_pairs * a.B * a.h;
     if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     p.units = static_cast<int>(units);
     // Heads per group: their K and V together take at most ~64 MB of the 129 MB L2.
@@ -943,6 +1032,7 @@ cudaError_t launch_d(const AttnArgs& a, const AttnMaps& m)
     p.group_heads = static_cast<int>(g);
     const int grid = static_cast<int>(std::min<long long>(units, std::min(sm_count(), kTableCtas)));
     const bool causal = (a.mask_kind & HATTN_MASK_CAUSAL) != 0;
+    if (paired) return launch_kernel<D, false>(a, m, p, grid, SchedPaired{});
     if (causal && units > grid && units <= kTableUnits) {
         const std::shared_ptr<const SchedTable> tab = greedy_table(p, grid);
         return launch_kernel<D, true>(a, m, p, grid, *tab);
