@@ -8,7 +8,8 @@
 // §掩码必须在 softmax 之前生效).
 //
 // How. A persistent kernel: one CTA per SM loops over work units, a unit being
-// one (b, i) and 256 consecutive query rows = two 128-row tiles. Units are
+// one (b, i) and 256 consecutive query rows = two 128-row tiles (when n_q <= 128,
+// two (b, i) heads instead, one per tile, each with its own K/V stream). Units are
 // ordered in groups of heads whose K/V fit in L2 together, heaviest causal
 // rows first within a group; for causal problems the host assigns units to
 // CTAs by greedy list scheduling on their block counts (a table passed with
