@@ -72,8 +72,10 @@ def test_long_sequence_sampled_parity(name):
 
 # ---------------------------------------------------------------- shape sweeps
 
+# n_q <= 128 runs two heads per unit on the tensor-core path: (3, 3, ...) pairs heads of
+# different batches (different key lengths) and leaves the last unit's second tile empty.
 SHAPES = [(1, 1, 1, 1), (2, 3, 100, 100), (1, 2, 129, 129), (2, 2, 300, 300), (1, 1, 520, 520),
-          (3, 2, 77, 300), (2, 1, 256, 64), (1, 1, 1, 700)]
+          (3, 2, 77, 300), (2, 1, 256, 64), (1, 1, 1, 700), (3, 3, 50, 200), (3, 3, 128, 128)]
 
 
 def _sweep_workload(dtype, B, h, n_q, n_k, d_k, d_v, mask_kind):
@@ -241,6 +243,25 @@ def test_repeatable_bitwise():
 
 
 # ---------------------------------------------------------------- device-side errors
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bad_key_length_in_paired_units(d):
+    # n_q <= 128 with h = 3: a unit's two heads can come from different batch
+    # elements, so one tile of a unit is valid while the other is not.
+    t = torch()
+    w = _sweep_workload("bf16", 3, 3, 100, 200, d, d, synth.MASK_KEY_PADDING)
+    inp = synth.attn_inputs(w)
+    q, k, v = _device_inputs(w, inp)
+    kl_host = np.array([50, 0, 201], dtype=np.int32)  # only batch 0 is valid
+    out = t.full((3, 100, 3, d), float("nan"), device="cuda", dtype=t.bfloat16)
+    hattn.attn_fwd(q, k, v, out=out, scale=w.scale, mask_kind=2, key_lens=keylens_device(kl_host))
+    assert hattn.check_device_error() == hattn._binding.EKEYLEN
+    got = from_device(out)
+    assert np.all(got[1:] == 0.0)
+    wq, wk, wv = (synth.widen(inp[n], w.dtype) for n in ("q", "k", "v"))
+    ref = oracle.attn(wq[:1], wk[:1], wv[:1], w.scale, 2, kl_host[:1])
+    assert_close(got[:1], ref, "bf16", "valid batch element")
+
 
 @pytest.mark.parametrize("dtype,d", [("bf16", 64), ("bf16", 128), ("f32", 64), ("bf16", 32)])
 def test_bad_key_length_zeroes_that_batch_and_raises(dtype, d):
