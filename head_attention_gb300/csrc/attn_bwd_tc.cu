@@ -22,9 +22,14 @@
 //                   MMAs into TMEM); the row warps form P^T and dS^T, written back
 //                   to TMEM as bf16 over S^T and dP^T; then dV += P^T dO and
 //                   dK += dS^T Q (TS MMAs). TMEM: S^T | dP^T | dV | dK.
+//                   Each block runs as two halves of 64 queries (N = 64 MMAs,
+//                   one handoff per half), pipelined: the row warps of half 1
+//                   work on block i while the tensor pipe runs half 0's dV/dK of
+//                   block i and half 0's S^T/dP^T of block i + 1.
 //   query_grads_tc: a CTA keeps one 128-query block of Q and dO and streams
 //                   128-key blocks of K and V. Per block: S = Q K^T, dP = dO V^T,
-//                   dS (bf16, over S), dQ += dS K. TMEM: S | dP | dQ.
+//                   dS (bf16, over S), dQ += dS K. TMEM: S | dP | dQ. The same
+//                   pipeline over halves of 64 keys.
 // Causal: blocks entirely above the diagonal are skipped; key padding: key
 // blocks at or past key_lens[b] are skipped, the last one masked. All waits are
 // bounded; a wait that gives up raises HATTN_ETIMEOUT, and the CTA drains its
@@ -51,34 +56,43 @@ template <int D>
 struct Tile {
     static constexpr int kBoxes = D / 64;
     static constexpr int kBytes = 128 * D * 2;
-    static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
+    static constexpr uint32_t kIdescHalf = idesc_bf16_f32(128, 64, false, false);
     static constexpr uint32_t kIdescAcc = idesc_bf16_f32(128, D, false, true);
 };
 
-// X = A . B^T over the D columns of two K-major 128-row tiles (into 128 TMEM columns).
+// The 64-row half h of a K-major 128-row tile starts 8 row groups (8 KB) in.
+constexpr uint32_t kHalfRowsBytes = 64 * 128;
+
+// X_h = A . B_h^T over the D columns, B_h the 64-row half h of a K-major tile
+// (into 64 TMEM columns from d_tmem): one column half of a block, so the row
+// warps of that half can start while the other half is multiplied.
 template <int D>
-__device__ __forceinline__ void mma_abt(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc)
+__device__ __forceinline__ void mma_abt_half(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, int h)
 {
+    const uint64_t bh = b_desc + ((h * kHalfRowsBytes) >> 4);
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
         const uint64_t off = ((ks / 4) * kBoxBytes + (ks % 4) * 32) >> 4;
-        mma_ss(d_tmem, a_desc + off, b_desc + off, Tile<D>::kIdescS, ks > 0 ? 1u : 0u);
+        mma_ss(d_tmem, a_desc + off, bh + off, Tile<D>::kIdescHalf, ks > 0 ? 1u : 0u);
     }
 }
 
-// Acc (+)= X . T where X is 128 x 128 bf16 in TMEM and T a 128-row tile used
-// MN-major (its D columns are the output columns). X's column pairs are packed
-// in two runs of 32 TMEM columns, at x_tmem (X columns 0-63) and x_tmem + 64
-// (X columns 64-127): each half is written by its own row warp inside the
-// columns it has already read.
+// Acc (+)= X_h . T_h over the column half h of X (128 x 128 bf16 in TMEM) and
+// the matching rows 64 h .. 64 h + 63 of a 128-row tile T used MN-major (its D
+// columns are the output columns). X's column pairs are packed in two runs of
+// 32 TMEM columns, at x_tmem (X columns 0-63) and x_tmem + 64 (X columns
+// 64-127): each half is written by its own row warps inside the columns they
+// have already read.
 template <int D>
-__device__ __forceinline__ void mma_xt(uint32_t d_tmem, uint32_t x_tmem, uint64_t t_desc,
-                                       bool accumulate)
+__device__ __forceinline__ void mma_xt_half(uint32_t d_tmem, uint32_t x_tmem, uint64_t t_desc, int h,
+                                            bool accumulate)
 {
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
-        mma_ts(d_tmem, x_tmem + (ks / 4) * 64 + (ks % 4) * 8, t_desc + ((ks * 2048) >> 4),
-               Tile<D>::kIdescAcc, (accumulate || ks > 0) ? 1u : 0u);
+    for (int k = 0; k < 4; ++k) {
+        const int ks = 4 * h + k;
+        mma_ts(d_tmem, x_tmem + h * 64 + k * 8, t_desc + ((ks * 2048) >> 4), Tile<D>::kIdescAcc,
+               (accumulate || ks > 0) ? 1u : 0u);
+    }
 }
 
 struct BwdTcParams {
@@ -127,8 +141,9 @@ struct KCfg {
     static constexpr int kOffStage = 2 * T::kBytes;  // stage s: Q, dO, lse2[128], D[128]
     static constexpr int kStageBytes = 2 * T::kBytes + 1024;
     static constexpr int kOffBar = kOffStage + kStages * kStageBytes;
+    // kBarS + h: S^T and dP^T of query half h ready; kBarP + h: its P^T and dS^T written.
     static constexpr int kBarKV = 0, kBarFull = 1, kBarEmpty = 1 + kStages, kBarS = 1 + 2 * kStages,
-                         kBarP = kBarS + 1, kBarO = kBarP + 1, kBarDrain = kBarO + 1,
+                         kBarP = kBarS + 2, kBarO = kBarP + 2, kBarDrain = kBarO + 1,
                          kNumBars = kBarDrain + 1;
     static constexpr int kOffSlot = kOffBar + 8 * kNumBars;
     static constexpr int kSmemBytes = kOffSlot + 16 + 1024;
@@ -182,8 +197,10 @@ __device__ __forceinline__ void key_grads_tc(const CUtensorMap& tm_q, const CUte
             mbar_init(bar(C::kBarFull + s), 1);
             mbar_init(bar(C::kBarEmpty + s), 1);
         }
-        mbar_init(bar(C::kBarS), 1);
-        mbar_init(bar(C::kBarP), kRowWarps);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(bar(C::kBarS + h), 1);
+            mbar_init(bar(C::kBarP + h), kRowWarps / 2);
+        }
         mbar_init(bar(C::kBarO), 1);
         mbar_init(bar(C::kBarDrain), 1);
         fence_barrier_init();
@@ -234,21 +251,46 @@ __device__ __forceinline__ void key_grads_tc(const CUtensorMap& tm_q, const CUte
         if (lane == 0 && nblk > 0) {
             const uint64_t k_desc = sdesc_sw128(sbase + C::kOffK, 16, 1024);
             const uint64_t v_desc = sdesc_sw128(sbase + C::kOffV, 16, 1024);
-            bool ok = mbar_wait(bar(C::kBarKV), 0);
-            for (int i = 0; ok && i < nblk; ++i) {
-                const int s = i % kStages;
-                if (!mbar_wait(bar(C::kBarFull + s), (i / kStages) & 1)) { ok = false; break; }
-                const uint32_t st = sbase + C::kOffStage + s * C::kStageBytes;
+            auto stage = [&](int i) { return sbase + C::kOffStage + (i % kStages) * C::kStageBytes; };
+            // S^T = K Q^T and dP^T = V dO^T for the queries of half h of block i.
+            auto issue_sdp = [&](int i, int h) {
+                const uint32_t st = stage(i);
+                mma_abt_half<D>(tmem + C::kColS + 64 * h, k_desc, sdesc_sw128(st, 16, 1024), h);
+                mma_abt_half<D>(tmem + C::kColDP + 64 * h, v_desc, sdesc_sw128(st + T::kBytes, 16, 1024), h);
+                mma_commit(bar(C::kBarS + h));
+            };
+            // dV += P^T dO and dK += dS^T Q over the queries of half h (Q / dO used MN-major).
+            auto issue_acc = [&](int i, int h) {
+                const uint32_t st = stage(i);
+                mma_xt_half<D>(tmem + C::kColDV, tmem + C::kColS, sdesc_sw128(st + T::kBytes, kBoxBytes, 1024), h, i > 0);
+                mma_xt_half<D>(tmem + C::kColDK, tmem + C::kColDP, sdesc_sw128(st, kBoxBytes, 1024), h, i > 0);
+            };
+            // Two-stage pipeline over the query halves of each block: while the row
+            // warps of half 1 work on block i, the tensor pipe runs half 0's dV/dK of
+            // block i and half 0's S^T/dP^T of block i + 1. Each S^T/dP^T half
+            // overwrites TMEM columns whose P^T/dS^T were read by MMAs issued before it.
+            bool ok = mbar_wait(bar(C::kBarKV), 0) && mbar_wait(bar(C::kBarFull), 0);
+            if (ok) {
                 tc_fence_after();
-                mma_abt<D>(tmem + C::kColS, k_desc, sdesc_sw128(st, 16, 1024));               // S^T
-                mma_abt<D>(tmem + C::kColDP, v_desc, sdesc_sw128(st + T::kBytes, 16, 1024));  // dP^T
-                mma_commit(bar(C::kBarS));
+                issue_sdp(0, 0);
+                issue_sdp(0, 1);
+            }
+            for (int i = 0; ok && i < nblk; ++i) {
+                const bool next = i + 1 < nblk;
                 if (!mbar_wait(bar(C::kBarP), i & 1)) { ok = false; break; }
                 tc_fence_after();
-                // dV += P^T dO,  dK += dS^T Q  (the Q / dO tiles used MN-major)
-                mma_xt<D>(tmem + C::kColDV, tmem + C::kColS, sdesc_sw128(st + T::kBytes, kBoxBytes, 1024), i > 0);
-                mma_xt<D>(tmem + C::kColDK, tmem + C::kColDP, sdesc_sw128(st, kBoxBytes, 1024), i > 0);
-                mma_commit(bar(C::kBarEmpty + s));
+                issue_acc(i, 0);
+                if (next) {
+                    const int s1 = (i + 1) % kStages;
+                    if (!mbar_wait(bar(C::kBarFull + s1), ((i + 1) / kStages) & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_sdp(i + 1, 0);
+                }
+                if (!mbar_wait(bar(C::kBarP + 1), i & 1)) { ok = false; break; }
+                tc_fence_after();
+                issue_acc(i, 1);
+                mma_commit(bar(C::kBarEmpty + i % kStages));
+                if (next) issue_sdp(i + 1, 1);
             }
             if (ok) mma_commit(bar(C::kBarO));
             else raise_device_error(p.err_word, HATTN_ETIMEOUT);
@@ -271,7 +313,8 @@ __device__ __forceinline__ void key_grads_tc(const CUtensorMap& tm_q, const CUte
             const int s = i % kStages;
             const int q0 = (qb_first + i) * 128;
             if (ok) {
-                const bool got = mbar_wait(bar(C::kBarFull + s), (i / kStages) & 1) && mbar_wait(bar(C::kBarS), i & 1);
+                const bool got = mbar_wait(bar(C::kBarFull + s), (i / kStages) & 1) &&
+                                 mbar_wait(bar(C::kBarS + half), i & 1);
                 ok = __all_sync(0xffffffffu, got);
             }
             if (!ok) continue;
@@ -341,7 +384,7 @@ __device__ __forceinline__ void key_grads_tc(const CUtensorMap& tm_q, const CUte
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::kBarP));
+            if (lane == 0) mbar_arrive(bar(C::kBarP + half));
         }
         // Each warp of the quadrant stores half of the D columns of dV and dK.
         constexpr int kHalfD = D / 2;
@@ -379,8 +422,9 @@ struct QCfg {
     static constexpr int kOffStage = 2 * T::kBytes;  // stage s: K, V
     static constexpr int kStageBytes = 2 * T::kBytes;
     static constexpr int kOffBar = kOffStage + kStages * kStageBytes;
+    // kBarS + h: S and dP of key half h ready; kBarP + h: its dS written.
     static constexpr int kBarQG = 0, kBarFull = 1, kBarEmpty = 1 + kStages, kBarS = 1 + 2 * kStages,
-                         kBarP = kBarS + 1, kBarO = kBarP + 1, kBarDrain = kBarO + 1,
+                         kBarP = kBarS + 2, kBarO = kBarP + 2, kBarDrain = kBarO + 1,
                          kNumBars = kBarDrain + 1;
     static constexpr int kOffSlot = kOffBar + 8 * kNumBars;
     static constexpr int kSmemBytes = kOffSlot + 16 + 1024;
@@ -428,8 +472,10 @@ __device__ __forceinline__ void query_grads_tc(const CUtensorMap& tm_q, const CU
             mbar_init(bar(C::kBarFull + s), 1);
             mbar_init(bar(C::kBarEmpty + s), 1);
         }
-        mbar_init(bar(C::kBarS), 1);
-        mbar_init(bar(C::kBarP), kRowWarps);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(bar(C::kBarS + h), 1);
+            mbar_init(bar(C::kBarP + h), kRowWarps / 2);
+        }
         mbar_init(bar(C::kBarO), 1);
         mbar_init(bar(C::kBarDrain), 1);
         fence_barrier_init();
@@ -474,19 +520,38 @@ __device__ __forceinline__ void query_grads_tc(const CUtensorMap& tm_q, const CU
         if (lane == 0) {
             const uint64_t q_desc = sdesc_sw128(sbase + C::kOffQ, 16, 1024);
             const uint64_t g_desc = sdesc_sw128(sbase + C::kOffG, 16, 1024);
-            bool ok = mbar_wait(bar(C::kBarQG), 0);
-            for (int j = 0; ok && j < nblk; ++j) {
-                const int s = j % kStages;
-                if (!mbar_wait(bar(C::kBarFull + s), (j / kStages) & 1)) { ok = false; break; }
-                const uint32_t st = sbase + C::kOffStage + s * C::kStageBytes;
+            auto stage = [&](int j) { return sbase + C::kOffStage + (j % kStages) * C::kStageBytes; };
+            // S = Q K^T and dP = dO V^T for the keys of half h of block j.
+            auto issue_sdp = [&](int j, int h) {
+                const uint32_t st = stage(j);
+                mma_abt_half<D>(tmem + C::kColS + 64 * h, q_desc, sdesc_sw128(st, 16, 1024), h);
+                mma_abt_half<D>(tmem + C::kColDP + 64 * h, g_desc, sdesc_sw128(st + T::kBytes, 16, 1024), h);
+                mma_commit(bar(C::kBarS + h));
+            };
+            // The same two-stage pipeline over key halves as the key-gradient CTAs.
+            bool ok = mbar_wait(bar(C::kBarQG), 0) && (nblk == 0 || mbar_wait(bar(C::kBarFull), 0));
+            if (ok && nblk > 0) {
                 tc_fence_after();
-                mma_abt<D>(tmem + C::kColS, q_desc, sdesc_sw128(st, 16, 1024));              // S = Q K^T
-                mma_abt<D>(tmem + C::kColDP, g_desc, sdesc_sw128(st + T::kBytes, 16, 1024));  // dP = dO V^T
-                mma_commit(bar(C::kBarS));
+                issue_sdp(0, 0);
+                issue_sdp(0, 1);
+            }
+            for (int j = 0; ok && j < nblk; ++j) {
+                const bool next = j + 1 < nblk;
+                const uint32_t st = stage(j);
                 if (!mbar_wait(bar(C::kBarP), j & 1)) { ok = false; break; }
                 tc_fence_after();
-                mma_xt<D>(tmem + C::kColDQ, tmem + C::kColS, sdesc_sw128(st, kBoxBytes, 1024), j > 0);  // dQ += dS K
-                mma_commit(bar(C::kBarEmpty + s));
+                mma_xt_half<D>(tmem + C::kColDQ, tmem + C::kColS, sdesc_sw128(st, kBoxBytes, 1024), 0, j > 0);
+                if (next) {
+                    const int s1 = (j + 1) % kStages;
+                    if (!mbar_wait(bar(C::kBarFull + s1), ((j + 1) / kStages) & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_sdp(j + 1, 0);
+                }
+                if (!mbar_wait(bar(C::kBarP + 1), j & 1)) { ok = false; break; }
+                tc_fence_after();
+                mma_xt_half<D>(tmem + C::kColDQ, tmem + C::kColS, sdesc_sw128(st, kBoxBytes, 1024), 1, j > 0);
+                mma_commit(bar(C::kBarEmpty + j % kStages));
+                if (next) issue_sdp(j + 1, 1);
             }
             if (ok) mma_commit(bar(C::kBarO));
             else raise_device_error(p.err_word, HATTN_ETIMEOUT);
@@ -509,7 +574,7 @@ __device__ __forceinline__ void query_grads_tc(const CUtensorMap& tm_q, const CU
         bool ok = true;
         for (int j = 0; j < nblk; ++j) {
             const int k0 = j * 128;
-            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarS), j & 1));
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarS + half), j & 1));
             if (!ok) continue;
             tc_fence_after();
             const bool edge = (k0 + 128 > kv_len) || (causal && k0 + 127 > q0);
@@ -555,7 +620,7 @@ __device__ __forceinline__ void query_grads_tc(const CUtensorMap& tm_q, const CU
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::kBarP));
+            if (lane == 0) mbar_arrive(bar(C::kBarP + half));
         }
         constexpr int kHalfD = D / 2;
         if (ok) {
