@@ -18,7 +18,7 @@
 //
 //   key_grads_tc:   a CTA keeps one 128-key block of K and V in shared memory
 //                   and streams 128-query blocks of Q, dO, lse2 and D through a
-//                   2-stage ring. Per block: S^T = K Q^T and dP^T = V dO^T (SS
+//                   2-stage (D = 128) / 3-stage (D = 64) ring. Per block: S^T = K Q^T and dP^T = V dO^T (SS
 //                   MMAs into TMEM); the row warps form P^T and dS^T, written back
 //                   to TMEM as bf16 over S^T and dP^T; then dV += P^T dO and
 //                   dK += dS^T Q (TS MMAs). TMEM: S^T | dP^T | dV | dK.
@@ -50,7 +50,9 @@ constexpr int kWarpMma = 1;
 constexpr int kWarpRow0 = 2;  // row warps 2-9
 constexpr int kRowWarps = 8;
 constexpr uint32_t kBoxBytes = 128 * 64 * 2;  // 128 rows x 64 bf16 columns
-constexpr int kStages = 2;
+// Ring depth: three stages where they fit (D = 64), else two.
+template <int D>
+constexpr int kStages = D == 64 ? 3 : 2;
 
 template <int D>
 struct Tile {
@@ -140,9 +142,9 @@ struct KCfg {
     static constexpr int kOffV = T::kBytes;
     static constexpr int kOffStage = 2 * T::kBytes;  // stage s: Q, dO, lse2[128], D[128]
     static constexpr int kStageBytes = 2 * T::kBytes + 1024;
-    static constexpr int kOffBar = kOffStage + kStages * kStageBytes;
+    static constexpr int kOffBar = kOffStage + kStages<D> * kStageBytes;
     // kBarS + h: S^T and dP^T of query half h ready; kBarP + h: its P^T and dS^T written.
-    static constexpr int kBarKV = 0, kBarFull = 1, kBarEmpty = 1 + kStages, kBarS = 1 + 2 * kStages,
+    static constexpr int kBarKV = 0, kBarFull = 1, kBarEmpty = 1 + kStages<D>, kBarS = 1 + 2 * kStages<D>,
                          kBarP = kBarS + 2, kBarO = kBarP + 2, kBarDrain = kBarO + 1,
                          kNumBars = kBarDrain + 1;
     static constexpr int kOffSlot = kOffBar + 8 * kNumBars;
@@ -193,7 +195,7 @@ __device__ __forceinline__ void key_grads_tc(const CUtensorMap& tm_q, const CUte
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::kBarKV), 1);
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kStages<D>; ++s) {
             mbar_init(bar(C::kBarFull + s), 1);
             mbar_init(bar(C::kBarEmpty + s), 1);
         }
@@ -225,8 +227,8 @@ __device__ __forceinline__ void key_grads_tc(const CUtensorMap& tm_q, const CUte
             const float* d_row = p.dsum + ((size_t)b * p.h + head) * p.nqp;
             int issued = 0;
             for (int i = 0; i < nblk; ++i) {
-                const int s = i % kStages;
-                if (!mbar_wait(bar(C::kBarEmpty + s), ((i / kStages) & 1) ^ 1)) {
+                const int s = i % kStages<D>;
+                if (!mbar_wait(bar(C::kBarEmpty + s), ((i / kStages<D>) & 1) ^ 1)) {
                     raise_device_error(p.err_word, HATTN_ETIMEOUT);
                     break;
                 }
@@ -243,15 +245,15 @@ __device__ __forceinline__ void key_grads_tc(const CUtensorMap& tm_q, const CUte
             }
             // Every copy this CTA started must land before the CTA may exit.
             mbar_wait(bar(C::kBarKV), 0);
-            for (int i = max(0, issued - kStages); i < issued; ++i)
-                mbar_wait(bar(C::kBarFull + i % kStages), (i / kStages) & 1);
+            for (int i = max(0, issued - kStages<D>); i < issued; ++i)
+                mbar_wait(bar(C::kBarFull + i % kStages<D>), (i / kStages<D>) & 1);
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
         if (lane == 0 && nblk > 0) {
             const uint64_t k_desc = sdesc_sw128(sbase + C::kOffK, 16, 1024);
             const uint64_t v_desc = sdesc_sw128(sbase + C::kOffV, 16, 1024);
-            auto stage = [&](int i) { return sbase + C::kOffStage + (i % kStages) * C::kStageBytes; };
+            auto stage = [&](int i) { return sbase + C::kOffStage + (i % kStages<D>) * C::kStageBytes; };
             // S^T = K Q^T and dP^T = V dO^T for the queries of half h of block i.
             auto issue_sdp = [&](int i, int h) {
                 const uint32_t st = stage(i);
@@ -281,15 +283,15 @@ __device__ __forceinline__ void key_grads_tc(const CUtensorMap& tm_q, const CUte
                 tc_fence_after();
                 issue_acc(i, 0);
                 if (next) {
-                    const int s1 = (i + 1) % kStages;
-                    if (!mbar_wait(bar(C::kBarFull + s1), ((i + 1) / kStages) & 1)) { ok = false; break; }
+                    const int s1 = (i + 1) % kStages<D>;
+                    if (!mbar_wait(bar(C::kBarFull + s1), ((i + 1) / kStages<D>) & 1)) { ok = false; break; }
                     tc_fence_after();
                     issue_sdp(i + 1, 0);
                 }
                 if (!mbar_wait(bar(C::kBarP + 1), i & 1)) { ok = false; break; }
                 tc_fence_after();
                 issue_acc(i, 1);
-                mma_commit(bar(C::kBarEmpty + i % kStages));
+                mma_commit(bar(C::kBarEmpty + i % kStages<D>));
                 if (next) issue_sdp(i + 1, 1);
             }
             if (ok) mma_commit(bar(C::kBarO));
@@ -310,10 +312,10 @@ __device__ __forceinline__ void key_grads_tc(const CUtensorMap& tm_q, const CUte
         const uint64_t c2 = f32x2(p.scale_log2, p.scale_log2);
         bool ok = true;
         for (int i = 0; i < nblk; ++i) {
-            const int s = i % kStages;
+            const int s = i % kStages<D>;
             const int q0 = (qb_first + i) * 128;
             if (ok) {
-                const bool got = mbar_wait(bar(C::kBarFull + s), (i / kStages) & 1) &&
+                const bool got = mbar_wait(bar(C::kBarFull + s), (i / kStages<D>) & 1) &&
                                  mbar_wait(bar(C::kBarS + half), i & 1);
                 ok = __all_sync(0xffffffffu, got);
             }
@@ -421,9 +423,9 @@ struct QCfg {
     static constexpr int kOffG = T::kBytes;
     static constexpr int kOffStage = 2 * T::kBytes;  // stage s: K, V
     static constexpr int kStageBytes = 2 * T::kBytes;
-    static constexpr int kOffBar = kOffStage + kStages * kStageBytes;
+    static constexpr int kOffBar = kOffStage + kStages<D> * kStageBytes;
     // kBarS + h: S and dP of key half h ready; kBarP + h: its dS written.
-    static constexpr int kBarQG = 0, kBarFull = 1, kBarEmpty = 1 + kStages, kBarS = 1 + 2 * kStages,
+    static constexpr int kBarQG = 0, kBarFull = 1, kBarEmpty = 1 + kStages<D>, kBarS = 1 + 2 * kStages<D>,
                          kBarP = kBarS + 2, kBarO = kBarP + 2, kBarDrain = kBarO + 1,
                          kNumBars = kBarDrain + 1;
     static constexpr int kOffSlot = kOffBar + 8 * kNumBars;
@@ -468,7 +470,7 @@ __device__ __forceinline__ void query_grads_tc(const CUtensorMap& tm_q, const CU
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::kBarQG), 1);
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kStages<D>; ++s) {
             mbar_init(bar(C::kBarFull + s), 1);
             mbar_init(bar(C::kBarEmpty + s), 1);
         }
@@ -498,8 +500,8 @@ __device__ __forceinline__ void query_grads_tc(const CUtensorMap& tm_q, const CU
             }
             int issued = 0;
             for (int j = 0; j < nblk; ++j) {
-                const int s = j % kStages;
-                if (!mbar_wait(bar(C::kBarEmpty + s), ((j / kStages) & 1) ^ 1)) {
+                const int s = j % kStages<D>;
+                if (!mbar_wait(bar(C::kBarEmpty + s), ((j / kStages<D>) & 1) ^ 1)) {
                     raise_device_error(p.err_word, HATTN_ETIMEOUT);
                     break;
                 }
@@ -512,15 +514,15 @@ __device__ __forceinline__ void query_grads_tc(const CUtensorMap& tm_q, const CU
                 ++issued;
             }
             mbar_wait(bar(C::kBarQG), 0);
-            for (int j = max(0, issued - kStages); j < issued; ++j)
-                mbar_wait(bar(C::kBarFull + j % kStages), (j / kStages) & 1);
+            for (int j = max(0, issued - kStages<D>); j < issued; ++j)
+                mbar_wait(bar(C::kBarFull + j % kStages<D>), (j / kStages<D>) & 1);
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
         if (lane == 0) {
             const uint64_t q_desc = sdesc_sw128(sbase + C::kOffQ, 16, 1024);
             const uint64_t g_desc = sdesc_sw128(sbase + C::kOffG, 16, 1024);
-            auto stage = [&](int j) { return sbase + C::kOffStage + (j % kStages) * C::kStageBytes; };
+            auto stage = [&](int j) { return sbase + C::kOffStage + (j % kStages<D>) * C::kStageBytes; };
             // S = Q K^T and dP = dO V^T for the keys of half h of block j.
             auto issue_sdp = [&](int j, int h) {
                 const uint32_t st = stage(j);
@@ -542,15 +544,15 @@ __device__ __forceinline__ void query_grads_tc(const CUtensorMap& tm_q, const CU
                 tc_fence_after();
                 mma_xt_half<D>(tmem + C::kColDQ, tmem + C::kColS, sdesc_sw128(st, kBoxBytes, 1024), 0, j > 0);
                 if (next) {
-                    const int s1 = (j + 1) % kStages;
-                    if (!mbar_wait(bar(C::kBarFull + s1), ((j + 1) / kStages) & 1)) { ok = false; break; }
+                    const int s1 = (j + 1) % kStages<D>;
+                    if (!mbar_wait(bar(C::kBarFull + s1), ((j + 1) / kStages<D>) & 1)) { ok = false; break; }
                     tc_fence_after();
                     issue_sdp(j + 1, 0);
                 }
                 if (!mbar_wait(bar(C::kBarP + 1), j & 1)) { ok = false; break; }
                 tc_fence_after();
                 mma_xt_half<D>(tmem + C::kColDQ, tmem + C::kColS, sdesc_sw128(st, kBoxBytes, 1024), 1, j > 0);
-                mma_commit(bar(C::kBarEmpty + j % kStages));
+                mma_commit(bar(C::kBarEmpty + j % kStages<D>));
                 if (next) issue_sdp(j + 1, 1);
             }
             if (ok) mma_commit(bar(C::kBarO));
