@@ -464,7 +464,9 @@ int pos_encoding_fwd(const void* emb, void* out, int dtype, int B, int n, int d_
     if ((long long)pos0 + n > (1LL << 24) || !std::isfinite(emb_scale)) return HATTN_EINVAL;
     if ((reinterpret_cast<uintptr_t>(out) & 7u) || (reinterpret_cast<uintptr_t>(emb) & 7u))
         return HATTN_EINVAL;
-    return from_cuda(launch_pos_encoding(emb, out, dtype, B, n, d_model, emb_scale, pos0,
+    int* err = device_error_ptr();
+    if (!err) return HATTN_ECUDA;
+    return from_cuda(launch_pos_encoding(emb, out, dtype, B, n, d_model, emb_scale, pos0, err,
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -81,7 +81,7 @@ cudaError_t launch_attn_bwd_tc(const AttnBwdArgs& a, const AttnMaps& maps, const
 
 // Sinusoidal positional encoding added to scaled embeddings (emb may be NULL).
 cudaError_t launch_pos_encoding(const void* emb, void* out, int dtype, int B, int n, int d_model,
-                                float emb_scale, int pos0, cudaStream_t stream);
+                                float emb_scale, int pos0, int* err_word, cudaStream_t stream);
 
 // Decode attention: one query per (b, h) over a per-sequence K/V prefix.
 struct DecodeLaunch {

@@ -198,6 +198,22 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
                  : "memory");
 }
 
+// Untiled bulk copy shared -> global of `bytes` (a multiple of 16; both
+// addresses 16-byte aligned), in the current bulk async-group. Thread writes of
+// the source must be made visible to the async proxy first (fence_proxy_async_smem).
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 ::"l"(reinterpret_cast<uint64_t>(dst)), "r"(src), "r"(bytes)
+                 : "memory");
+}
+
+// Waits until at most one committed bulk group is still reading shared memory.
+__device__ __forceinline__ void bulk_wait_group_read_1()
+{
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group()
 {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");

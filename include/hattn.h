@@ -174,7 +174,8 @@ int mha_fwd_noalloc(const void* x_q, const void* x_kv, const void* Wq, const voi
  *            and pos0 + n <= 2^24 (positions are exact fp32 integers in the kernel)
  * Pointers 8-byte aligned. The encoding term is within 1e-6 of the exact
  * sin/cos; the sum is rounded once to dtype. Returns HATTN_OK, HATTN_EINVAL or
- * HATTN_ECUDA.
+ * HATTN_ECUDA; large problems run a bulk-copy pipeline whose bounded waits
+ * raise HATTN_ETIMEOUT on the device error word if one ever gives up.
  */
 int pos_encoding_fwd(const void* emb, void* out, int dtype, int B, int n, int d_model,
                      float emb_scale, int pos0, hattn_stream_t stream);

@@ -17,7 +17,11 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("B,n,d_model,pos0,with_emb", [(1, 5, 4, 0, False), (2, 100, 512, 0, True),
                                                        (1, 8192, 512, 0, False), (3, 77, 128, 40000, True),
                                                        (1, 16, 64, (1 << 24) - 16, False),
-                                                       (4, 1, 2, 7, True)])
+                                                       (4, 1, 2, 7, True),
+                                                       # >= 16 MB: the bulk-copy path (ragged last
+                                                       # chunk; batch rows in two groups; no emb)
+                                                       (3, 5000, 768, 0, True), (2, 3000, 1000, 123, True),
+                                                       (10, 600, 4096, 0, True), (4, 8192, 512, 5, False)])
 def test_pos_encoding_matches_oracle(dtype, B, n, d_model, pos0, with_emb):
     t = torch()
     hattn.build()
@@ -51,6 +55,19 @@ def test_pos_encoding_in_place():
     t.cuda.synchronize()
     pe = oracle.pos_encoding(1, 33, 64)[0]
     np.testing.assert_allclose(from_device(x), from_device(ref) * 2.0 + pe[None], atol=1e-5)
+
+
+def test_pos_encoding_in_place_bulk_path():
+    # 32 MB of fp32: large enough for the bulk-copy path, which reads each chunk
+    # before it writes it back to the same addresses.
+    t = torch()
+    x = t.randn(2, 8192, 512, device="cuda")
+    ref = x.clone()
+    hattn.pos_encoding_fwd(x, emb=x, emb_scale=2.0, pos0=9)
+    t.cuda.synchronize()
+    assert hattn.check_device_error() == 0
+    want = from_device(ref) * 2.0 + oracle.pos_encoding(1, 8192, 512, None, 1.0, 9)[0][None]
+    assert np.abs(from_device(x) - want).max() <= 4e-6 * (1 + np.abs(want).max())
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
