@@ -61,14 +61,14 @@ __device__ __forceinline__ float warp_sum(float x)
 }
 
 // Copies rows [row0, row0 + rows) of a [n, *] slice (row stride src_stride
-// elements, d elements per row) into fp32 shared memory with row stride
-// dst_stride, zero for rows >= n. All 16-byte loads are issued before any store.
-template <typename T>
+// elements, d <= kMaxRowD elements per row) into fp32 shared memory with row
+// stride dst_stride, zero for rows >= n. All 16-byte loads are issued before any store.
+template <typename T, int kMaxRowD>
 __device__ __forceinline__ void stage_rows(float* dst, int dst_stride, const T* src,
                                            size_t src_stride, int row0, int rows, int n, int d)
 {
     constexpr int V = 16 / sizeof(T);           // elements per 16-byte load
-    constexpr int kMaxLoads = kKeys * kMaxD / V / kThreads;
+    constexpr int kMaxLoads = (kKeys * kMaxRowD / V + kThreads - 1) / kThreads;
     const int per_row = d / V;
     const int total = rows * per_row;
     uint4 buf[kMaxLoads];
@@ -95,7 +95,10 @@ __device__ __forceinline__ void stage_rows(float* dst, int dst_stride, const T* 
     }
 }
 
-template <typename T, int kCols>  // kCols = output columns per lane (d_v <= 32 * kCols)
+// kCols = output columns per lane (d_v <= 32 * kCols); kMaxRowD bounds d_k and d_v
+// (a tighter bound unrolls less staging code: the small fp32 problems are bound
+// by latency, instruction fetch included).
+template <typename T, int kCols, int kMaxRowD>
 __global__ void __launch_bounds__(kThreads)
     attn_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                      T* __restrict__ out, int n_q, int n_k, int h, int d_k, int d_v, float scale,
@@ -138,7 +141,7 @@ __global__ void __launch_bounds__(kThreads)
     int key_end = kv_len;
     if (causal) key_end = min(key_end, row0 + kRows);
 
-    stage_rows<T>(q_s, dkp, q_bh, qk_row_stride, row0, kRows, n_q, d_k);
+    stage_rows<T, kMaxRowD>(q_s, dkp, q_bh, qk_row_stride, row0, kRows, n_q, d_k);
 
     float m[kRowsPerWarp], l[kRowsPerWarp], acc[kRowsPerWarp][kCols];
 #pragma unroll
@@ -151,8 +154,8 @@ __global__ void __launch_bounds__(kThreads)
 
     for (int kt = 0; kt < key_end; kt += kKeys) {
         __syncthreads();  // q_s is staged and the previous tile is no longer read
-        stage_rows<T>(k_s, dkp, k_bh, qk_row_stride, kt, kKeys, n_k, d_k);
-        stage_rows<T>(v_s, d_v, v_bh, v_row_stride, kt, kKeys, n_k, d_v);
+        stage_rows<T, kMaxRowD>(k_s, dkp, k_bh, qk_row_stride, kt, kKeys, n_k, d_k);
+        stage_rows<T, kMaxRowD>(v_s, d_v, v_bh, v_row_stride, kt, kKeys, n_k, d_v);
         __syncthreads();
 
 #pragma unroll
@@ -208,16 +211,16 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-template <typename T, int kCols>
+template <typename T, int kCols, int kMaxRowD = kMaxD>
 cudaError_t launch_typed(const AttnArgs& a)
 {
     const size_t smem = sizeof(float) * ((size_t)kRows * (a.d_k + 1) + (size_t)kKeys * (a.d_k + 1) +
                                          (size_t)kKeys * a.d_v);
-    cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel<T, kCols>,
+    cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel<T, kCols, kMaxRowD>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((a.n_q + kRows - 1) / kRows, a.h, a.B);
-    attn_simt_kernel<T, kCols><<<grid, kThreads, smem, a.stream>>>(
+    attn_simt_kernel<T, kCols, kMaxRowD><<<grid, kThreads, smem, a.stream>>>(
         static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v),
         static_cast<T*>(a.out), a.n_q, a.n_k, a.h, a.d_k, a.d_v, a.scale, a.mask_kind,
         a.key_lens, a.err_word, a.lse);
@@ -227,6 +230,7 @@ cudaError_t launch_typed(const AttnArgs& a)
 template <typename T>
 cudaError_t launch_cols(const AttnArgs& a)
 {
+    if (a.d_v <= 64 && a.d_k <= 64) return launch_typed<T, 2, 64>(a);
     if (a.d_v <= 64) return launch_typed<T, 2>(a);
     if (a.d_v <= 128) return launch_typed<T, 4>(a);
     return launch_typed<T, 8>(a);
