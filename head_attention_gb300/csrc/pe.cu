@@ -6,7 +6,7 @@
 // You Need", §没有循环，模型怎样知道词序？).
 //
 // Two kernels. Problems of 16 MB or more whose rows are 16-byte multiples at
-// 16-byte aligned addresses take the bulk-copy path below (77 % of the measured
+// 16-byte aligned addresses take the bulk-copy path below (79 % of the measured
 // HBM copy bandwidth on B=16 n=8192 d_model=512 bf16, against 66 % for the
 // register path). Otherwise, the register path:
 // Layout of the work: the encoding depends on (t, i) only, so a thread owns
@@ -160,11 +160,12 @@ __global__ void __launch_bounds__(kThreads)
 // Rows of 16-byte multiples at 16-byte aligned addresses stream through shared
 // memory by bulk copies instead: a persistent CTA (one per SM) walks chunks of
 // R positions x Bc batch rows (each batch row's R rows are contiguous, one copy
-// each) through a 3-stage ring. The threads compute sin/cos once per (position,
-// frequency) of the chunk and apply them to its Bc batch rows in place; one
-// thread then stores the chunk back with bulk copies and refills the stage two
-// chunks ahead once the stores out of it have been read. Two chunks of loads
-// stay in flight per SM, without registers holding them.
+// each) through a 3-stage ring. Warp 0 moves the data: it loads a stage, and
+// once the other 31 warps report the chunk computed (an mbarrier, no block-wide
+// barrier) stores it back and refills the stage two chunks ahead after the
+// stores out of it have been read. The compute warps compute sin/cos once per
+// (position, frequency) of the chunk and apply them to its Bc batch rows in
+// place. Two chunks of loads stay in flight per SM, without registers holding them.
 constexpr int kBulkStages = 3;
 constexpr int kBulkThreads = 1024;
 constexpr uint32_t kBulkStageBytes = 64 * 1024;
@@ -188,14 +189,21 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
     float2* turns = reinterpret_cast<float2*>(smem + kBulkStages * kBulkStageBytes);
     const uint32_t bar0 = smem_u32(turns + kBulkMaxHalfD);
-    auto full = [&](int s) { return bar0 + 8u * s; };
+    // ready(s): the stage's chunk landed (or, without loads, the stage is free);
+    // computed(s): every compute warp finished the stage's chunk.
+    auto ready = [&](int st) { return bar0 + 8u * st; };
+    auto computed = [&](int st) { return bar0 + 8u * (kBulkStages + st); };
     const uint32_t stage0 = smem_u32(smem);
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    constexpr int kComputeWarps = kBulkThreads / 32 - 1;  // warp 0 moves the data
     const bool load = emb != nullptr;
 
     for (int i = tid; i < sh.half_d; i += kBulkThreads) pe_turns(log2_w_step, i, turns[i].x, turns[i].y);
     if (tid == 0) {
-        for (int st = 0; st < kBulkStages; ++st) mbar_init(full(st), 1);
+        for (int st = 0; st < kBulkStages; ++st) {
+            mbar_init(ready(st), 1);
+            mbar_init(computed(st), kComputeWarps);
+        }
         fence_barrier_init();
     }
     __syncthreads();
@@ -213,41 +221,69 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
         ch.bcnt = min(sh.Bc, sh.B - ch.b0);
         return ch;
     };
-    auto n_mine = [&]() {
-        return sh.chunks > static_cast<int>(blockIdx.x)
-                   ? (sh.chunks - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
-                   : 0;
-    };
-    const int mine = n_mine();
+    const int mine = sh.chunks > static_cast<int>(blockIdx.x)
+                         ? (sh.chunks - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                         : 0;
     const size_t batch_stride = (size_t)sh.n * 2 * sh.half_d;
     // Stage layout: batch row b of the chunk at b * R * row_bytes, its R rows contiguous.
-    auto issue_loads = [&](int k) {
-        const Chunk ch = chunk_of(k);
-        const int st = k % kBulkStages;
-        const uint32_t bytes = static_cast<uint32_t>(ch.rows) * sh.row_bytes;
-        mbar_arrive_expect_tx(full(st), bytes * static_cast<uint32_t>(ch.bcnt));
-        for (int b = 0; b < ch.bcnt; ++b)
-            bulk_load(stage0 + st * kBulkStageBytes + b * sh.R * sh.row_bytes,
-                      emb + (size_t)(ch.b0 + b) * batch_stride + (size_t)ch.t0 * 2 * sh.half_d, bytes,
-                      full(st));
-    };
-    if (tid == 0 && load)
-        for (int k = 0; k < min(mine, kBulkStages - 1); ++k) issue_loads(k);
+    auto gaddr = [&](const Chunk& ch, int b) { return (size_t)(ch.b0 + b) * batch_stride + (size_t)ch.t0 * 2 * sh.half_d; };
+    auto saddr = [&](int st, int b) { return stage0 + st * kBulkStageBytes + b * sh.R * sh.row_bytes; };
 
-    int k = 0;
-    for (; k < mine; ++k) {
+    if (warp == 0) {
+        if (lane == 0) {
+            // Marks stage k % 3 ready for chunk k: loads it, or (without loads) just
+            // releases it to the compute warps.
+            auto fill = [&](int k) {
+                const Chunk ch = chunk_of(k);
+                const int st = k % kBulkStages;
+                if (!load) {
+                    mbar_arrive(ready(st));
+                    return;
+                }
+                const uint32_t bytes = static_cast<uint32_t>(ch.rows) * sh.row_bytes;
+                mbar_arrive_expect_tx(ready(st), bytes * static_cast<uint32_t>(ch.bcnt));
+                for (int b = 0; b < ch.bcnt; ++b) bulk_load(saddr(st, b), emb + gaddr(ch, b), bytes, ready(st));
+            };
+            int filled = 0;
+            for (; filled < min(mine, kBulkStages - 1); ++filled) fill(filled);
+            int k = 0;
+            for (; k < mine; ++k) {
+                const int st = k % kBulkStages;
+                if (!mbar_wait(computed(st), (k / kBulkStages) & 1)) break;
+                const Chunk ch = chunk_of(k);
+                const uint32_t bytes = static_cast<uint32_t>(ch.rows) * sh.row_bytes;
+                for (int b = 0; b < ch.bcnt; ++b) bulk_store(out + gaddr(ch, b), saddr(st, b), bytes);
+                bulk_commit_group();
+                // The stage of chunk k + 2 held chunk k - 1, whose stores must have read it.
+                if (filled < mine) {
+                    bulk_wait_group_read_1();
+                    fill(filled++);
+                }
+            }
+            if (k < mine) raise_device_error(err_word, HATTN_ETIMEOUT);
+            bulk_wait_group_all();
+            // Loads of chunks never stored (only after a wait gave up) must land.
+            for (int j = k; load && j < filled; ++j)
+                if (!mbar_wait(ready(j % kBulkStages), (j / kBulkStages) & 1)) raise_device_error(err_word, HATTN_ETIMEOUT);
+        }
+        __syncwarp();
+        return;
+    }
+
+    // Compute warps: a thread takes one 16-byte piece of a row (kP frequency pairs)
+    // at one position and applies its sin/cos to that piece of every batch row.
+    constexpr int kP = 8 / static_cast<int>(sizeof(T));
+    const int pieces = sh.half_d / kP;
+    const int ctid = tid - 32;
+    for (int k = 0; k < mine; ++k) {
         const Chunk ch = chunk_of(k);
         const int st = k % kBulkStages;
         uint8_t* stage = smem + st * kBulkStageBytes;
-        if (load) {
-            const bool got = mbar_wait(full(st), (k / kBulkStages) & 1);
-            if (__syncthreads_or(!got)) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(ready(st), (k / kBulkStages) & 1))) {
+            if (lane == 0) raise_device_error(err_word, HATTN_ETIMEOUT);
+            break;
         }
-        // A thread takes one 16-byte piece of a row (kP frequency pairs) at one position
-        // and applies its sin/cos to that piece of every batch row of the chunk.
-        constexpr int kP = 8 / static_cast<int>(sizeof(T));
-        const int pieces = sh.half_d / kP;
-        for (int q = tid; q < ch.rows * pieces; q += kBulkThreads) {
+        for (int q = ctid; q < ch.rows * pieces; q += kComputeWarps * 32) {
             const int r = q / pieces, i0 = (q - r * pieces) * kP;
             float sn[kP], cs[kP];
 #pragma unroll
@@ -273,35 +309,17 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
                 *e = make_uint4(o[0], o[1], o[2], o[3]);
             }
         }
-        // The stage's thread writes become visible to the bulk stores.
+        // This thread's writes become visible to the bulk stores; one arrival per warp.
         fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-            const uint32_t bytes = static_cast<uint32_t>(ch.rows) * sh.row_bytes;
-            for (int b = 0; b < ch.bcnt; ++b)
-                bulk_store(out + (size_t)(ch.b0 + b) * batch_stride + (size_t)ch.t0 * 2 * sh.half_d,
-                           stage0 + st * kBulkStageBytes + b * sh.R * sh.row_bytes, bytes);
-            bulk_commit_group();
-            // The stage two chunks ahead held chunk k - 1: its stores must have read it
-            // before it is refilled (or, without loads, rewritten by the threads after
-            // the next barrier).
-            bulk_wait_group_read_1();
-            if (load && k + kBulkStages - 1 < mine) issue_loads(k + kBulkStages - 1);
-        }
-    }
-    if (k < mine && tid == 0) raise_device_error(err_word, HATTN_ETIMEOUT);
-    if (tid == 0) {
-        bulk_wait_group_all();
-        // Loads issued for chunks never consumed (only after a wait gave up) must land.
-        for (int j = k; load && j < min(mine, k + kBulkStages - 1); ++j)
-            mbar_wait(full(j % kBulkStages), (j / kBulkStages) & 1);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(computed(st));
     }
 }
 
 template <typename T>
 size_t bulk_smem_bytes()
 {
-    return kBulkStages * kBulkStageBytes + kBulkMaxHalfD * sizeof(float2) + 8 * kBulkStages + 128;
+    return kBulkStages * kBulkStageBytes + kBulkMaxHalfD * sizeof(float2) + 16 * kBulkStages + 128;
 }
 
 // The bulk path's chunk shape, or false when a row does not fit a stage, the

@@ -35,6 +35,7 @@ def test_pos_encoding_matches_oracle(dtype, B, n, d_model, pos0, with_emb):
     scale = math.sqrt(d_model)
     hattn.pos_encoding_fwd(out, emb=emb_dev, emb_scale=scale, pos0=pos0)
     t.cuda.synchronize()
+    assert hattn.check_device_error() == 0
     ref = oracle.pos_encoding(B, n, d_model, None if emb is None else synth.widen(emb, dtype),
                               float(np.float32(scale)), pos0)
     got = from_device(out)
