@@ -19,8 +19,10 @@
 // K-major) and W ([K][N] row-major, i.e. N-major, 64 x 64 boxes) through a
 // 4-stage shared-memory ring by TMA; warp 1 (one thread) issues the tcgen05
 // MMAs into one of two TMEM accumulators (256 columns each), so the epilogue
-// of one tile overlaps the MMAs of the next; warps 2-5 run the epilogue, thread
-// r of a warp quadrant owning output row r (TMEM lane r). CTAs loop over tiles
+// of one tile overlaps the MMAs of the next; warps 2-9 run the epilogue, thread
+// r of a warp quadrant owning output row r (TMEM lane r) and the two warps of a
+// quadrant taking the two halves of the tile's columns (the LayerNorm row
+// statistics combine the halves through shared memory). CTAs loop over tiles
 // (persistent grid of at most one CTA per SM). All mbarrier waits are bounded.
 //
 // Sources: the projections Q = X W^Q etc. ([hex4c59 "读懂 Attention Is All You
@@ -39,14 +41,16 @@
 namespace hattn {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int kWarpLoad = 0;
 constexpr int kWarpMma = 1;  // also owns the TMEM allocation
 constexpr int kBM = 128, kBN = 256, kBK = 64;
 constexpr uint32_t kABoxBytes = kBM * kBK * 2;  // A box: 128 rows x 64 columns
 constexpr uint32_t kWBoxBytes = 64 * kBK * 2;   // W box: 64 K-rows x 64 N-columns
 constexpr uint32_t kStageBytes = kABoxBytes + (kBN / 64) * kWBoxBytes;
-constexpr int kEpiThreads = 128;
+// Epilogue warps 2-9: warp w takes TMEM lane quadrant w % 4 (one output row per
+// thread) and half (w - 2) / 4 of the tile's 32-column chunks.
+constexpr int kEpiThreads = 256;
 
 // Shared-memory layout and barrier indices. The norm epilogue also stages the
 // tile's residual rows (up to 256 columns) by TMA, which costs one ring stage.
@@ -63,7 +67,8 @@ struct Layout {
     static constexpr int kBarXFull = 2 * kStages + 7;     // the tile's residual rows landed
     static constexpr int kBarXEmpty = 2 * kStages + 8;    // their buffer (reused for the output) is free
     static constexpr int kBarYReady = 2 * kStages + 9;    // every epilogue warp wrote its output rows
-    static constexpr int kNumBars = 2 * kStages + 10;
+    static constexpr int kBarEpi = 2 * kStages + 10;      // epilogue rendezvous (row statistics)
+    static constexpr int kNumBars = 2 * kStages + 11;
     static constexpr int kOffX = kStages * kStageBytes;  // residual: 4 boxes of 128 rows x 64 columns
     static constexpr int kXBytes = kNorm ? 4 * kABoxBytes : 0;
     static constexpr int kOffBar = kOffX + kXBytes;
@@ -72,7 +77,13 @@ struct Layout {
     // norm: gamma, beta and bias of this CTA's columns (fp32, up to 256 each)
     static constexpr int kOffVec = kOffStat + 2 * kBM * 4;
     static constexpr int kVecBytes = kNorm ? 3 * kBN * 4 : 0;
-    static constexpr int kOffSlot = kOffVec + kVecBytes;  // TMEM base address
+    // norm: the two column halves' partial row sums and squared deviations
+    // (float part[2][2][128]), the merged row mean and 1/std (float[2][128]), and
+    // a word set when any epilogue wait gave up.
+    static constexpr int kOffPart = kOffVec + kVecBytes;
+    static constexpr int kOffRow = kOffPart + (kNorm ? 4 * kBM * 4 : 0);
+    static constexpr int kOffFail = kOffRow + (kNorm ? 2 * kBM * 4 : 0);
+    static constexpr int kOffSlot = kOffFail + 16;  // TMEM base address
     static constexpr int kSmemBytes = kOffSlot + 16 + 1024;  // + slack to align the base to 1024 B
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
@@ -209,12 +220,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(Lay::kBarAccFull + b), 1);
             mbar_init(bar(Lay::kBarAccEmpty + b), kEpiThreads / 32);
         }
-        mbar_init(bar(Lay::kBarSum), kEpiThreads);
-        mbar_init(bar(Lay::kBarSq), kEpiThreads);
+        // One remote arrival per row (the column-half-0 warps exchange).
+        mbar_init(bar(Lay::kBarSum), kBM);
+        mbar_init(bar(Lay::kBarSq), kBM);
         mbar_init(bar(Lay::kBarDrain), 1);
         mbar_init(bar(Lay::kBarXFull), 1);
         mbar_init(bar(Lay::kBarXEmpty), 1);
         mbar_init(bar(Lay::kBarYReady), kEpiThreads / 32);
+        mbar_init(bar(Lay::kBarEpi), kEpiThreads / 32);
+        st_volatile_shared(sbase + Lay::kOffFail, 0u);
         fence_barrier_init();
     }
     if (warp == kWarpMma) {
@@ -323,6 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         const int q = warp % 4;  // TMEM lane quadrant this warp may access
+        const int hf = (warp - 2) / 4;  // column half of the tile
+        const int et = (warp - 2) * 32 + lane;
         const int r = q * 32 + lane;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
         const uint32_t peer = rank ^ 1u;
@@ -332,13 +348,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             // before any wait, so the named barrier cannot be left waiting.
             const TileGeom g0 = tile_geom<kNorm>(p, 0, rank);
             float* vec = reinterpret_cast<float*>(smem + Lay::kOffVec);
-            for (int c = r; c < g0.bn; c += kEpiThreads) {
+            for (int c = et; c < g0.bn; c += kEpiThreads) {
                 vec[c] = p.gamma[g0.n0 + c];
                 vec[kBN + c] = p.beta[g0.n0 + c];
                 vec[2 * kBN + c] = p.prob[0].bias ? p.prob[0].bias[g0.n0 + c] : 0.0f;
             }
             named_sync(1, kEpiThreads);
         }
+        // Rendezvous of the epilogue warps inside the tile loop: an mbarrier with one
+        // arrival per warp and a bounded wait (a named barrier could be left waiting
+        // by a warp that gave up); a failure is recorded in the shared fail word.
+        uint32_t epi_phase = 0;
+        auto epi_sync = [&]() {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(Lay::kBarEpi));
+            const bool got = mbar_wait(bar(Lay::kBarEpi), epi_phase & 1);
+            ++epi_phase;
+            if (!__all_sync(0xffffffffu, got) && lane == 0) st_volatile_shared(sbase + Lay::kOffFail, 1u);
+        };
         uint32_t i = 0;
         bool ok = true;
         for (int t = tr.first; ok && t < p.tiles; t += tr.stride, ++i) {
@@ -355,10 +382,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row = g.m0 + r;
             const bool valid = row < pr.M;
             const int nchunks = g.bn / 32;
+            // This warp's chunks: the first or the second half of the tile's columns.
+            const int c_begin = hf * ((nchunks + 1) / 2);
+            const int c_end = min(nchunks, c_begin + (nchunks + 1) / 2);
             if constexpr (!kNorm) {
                 __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(pr.c) + (size_t)row * pr.N + g.n0;
                 const bool relu = pr.relu != 0;
-                for (int c = 0; c < nchunks; ++c) {
+                for (int c = c_begin; c < c_end; ++c) {
                     uint32_t v[32];
                     tmem_ld_x32(acc + 32 * c, v);
                     if (pr.bias) {
@@ -392,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint8_t* xbase = smem + Lay::kOffX + r * 128;
                 // Pass 1: z = acc [+ bias] + x, kept in TMEM; partial row sum.
                 float sum = 0.0f;
-                for (int c = 0; c < nchunks; ++c) {
+                for (int c = c_begin; c < c_end; ++c) {
                     uint32_t z[32];
                     tmem_ld_x32(acc + 32 * c, z);
                     uint4 xv[4];
@@ -418,11 +448,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st_x32(acc + 32 * c, z);
                 }
                 tmem_st_wait();
+                // The two column halves' sums give this CTA's row sum.
+                float* part = reinterpret_cast<float*>(smem + Lay::kOffPart);
+                part[hf * kBM + r] = sum;
+                epi_sync();
+                sum = part[r] + part[kBM + r];
                 // Pass 2: squared deviations about this CTA's own mean (two passes, robust).
                 const float n_own = static_cast<float>(g.bn);
                 const float m_own = sum / n_own;
                 float sq = 0.0f;
-                for (int c = 0; c < nchunks; ++c) {
+                for (int c = c_begin; c < c_end; ++c) {
                     uint32_t z[32];
                     tmem_ld_x32(acc + 32 * c, z);
 #pragma unroll
@@ -431,25 +466,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sq = fmaf(dz, dz, sq);
                     }
                 }
-                float mean = m_own;
-                if (p.split == 2) {
-                    // One exchange of (mean, M2) with the peer's half of the row, merged by
-                    // the pairwise formula: M2 = M2_a + M2_b + (m_a - m_b)^2 n_a n_b / N.
-                    float m_peer = 0.0f, sq_peer = 0.0f;
-                    const bool got = exchange_pair<kNorm>(m_own, sq, m_peer, sq_peer, sbase, i & 1, r, peer);
-                    ok = __all_sync(0xffffffffu, got);
-                    const float n_peer = static_cast<float>(N) - n_own;
-                    const float delta = m_own - m_peer;
-                    mean = (n_own * m_own + n_peer * m_peer) / static_cast<float>(N);
-                    sq = sq + sq_peer + delta * delta * (n_own * n_peer / static_cast<float>(N));
+                part[(2 + hf) * kBM + r] = sq;
+                epi_sync();
+                sq = part[2 * kBM + r] + part[3 * kBM + r];
+                // Half 0 merges the row with the peer CTA's half-row and shares the result.
+                float* rowstat = reinterpret_cast<float*>(smem + Lay::kOffRow);
+                if (hf == 0) {
+                    float mean = m_own;
+                    if (p.split == 2) {
+                        // One exchange of (mean, M2) with the peer's half of the row, merged by
+                        // the pairwise formula: M2 = M2_a + M2_b + (m_a - m_b)^2 n_a n_b / N.
+                        float m_peer = 0.0f, sq_peer = 0.0f;
+                        const bool got = exchange_pair<kNorm>(m_own, sq, m_peer, sq_peer, sbase, i & 1, r, peer);
+                        if (!__all_sync(0xffffffffu, got) && lane == 0) st_volatile_shared(sbase + Lay::kOffFail, 1u);
+                        const float n_peer = static_cast<float>(N) - n_own;
+                        const float delta = m_own - m_peer;
+                        mean = (n_own * m_own + n_peer * m_peer) / static_cast<float>(N);
+                        sq = sq + sq_peer + delta * delta * (n_own * n_peer / static_cast<float>(N));
+                    }
+                    rowstat[r] = mean;
+                    rowstat[kBM + r] = 1.0f / sqrtf(sq / static_cast<float>(N) + p.eps);
                 }
-                const float rstd = 1.0f / sqrtf(sq / static_cast<float>(N) + p.eps);
+                epi_sync();
+                ok = ld_volatile_shared(sbase + Lay::kOffFail) == 0u;
+                const float mean = rowstat[r], rstd = rowstat[kBM + r];
                 // Pass 3: normalise, scale, shift, round once to bf16, into the residual
                 // buffer (same swizzled 128 x 64 boxes), which TMA then stores.
                 const float4* gam4 = reinterpret_cast<const float4*>(smem + Lay::kOffVec);
                 const float4* bet4 = reinterpret_cast<const float4*>(smem + Lay::kOffVec + kBN * 4);
                 uint8_t* ybase = smem + Lay::kOffX + r * 128;
-                for (int c = 0; ok && c < nchunks; ++c) {
+                for (int c = c_begin; ok && c < c_end; ++c) {
                     uint32_t z[32];
                     tmem_ld_x32(acc + 32 * c, z);
                     uint32_t w[16];
