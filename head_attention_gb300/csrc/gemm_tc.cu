@@ -17,7 +17,8 @@
 //
 // Tiles are 128 rows x up to 256 columns. Warp 0 streams A (128 x 64 boxes,
 // K-major) and W ([K][N] row-major, i.e. N-major, 64 x 64 boxes) through a
-// 4-stage shared-memory ring by TMA; warp 1 (one thread) issues the tcgen05
+// 3-stage shared-memory ring by TMA (both epilogues stage their bf16 output
+// tile in shared memory and write it with TMA stores); warp 1 (one thread) issues the tcgen05
 // MMAs into one of two TMEM accumulators (256 columns each), so the epilogue
 // of one tile overlaps the MMAs of the next; warps 2-9 run the epilogue, thread
 // r of a warp quadrant owning output row r (TMEM lane r) and the two warps of a
@@ -52,11 +53,13 @@ constexpr uint32_t kStageBytes = kABoxBytes + (kBN / 64) * kWBoxBytes;
 // thread) and half (w - 2) / 4 of the tile's 32-column chunks.
 constexpr int kEpiThreads = 256;
 
-// Shared-memory layout and barrier indices. The norm epilogue also stages the
-// tile's residual rows (up to 256 columns) by TMA, which costs one ring stage.
+// Shared-memory layout and barrier indices. Both epilogues stage the tile's
+// output (up to 128 x 256 bf16, 64 KB) in shared memory for TMA stores, and the
+// norm epilogue first loads the tile's residual rows into the same buffer; it
+// costs one ring stage (4 -> 3).
 template <bool kNorm>
 struct Layout {
-    static constexpr int kStages = kNorm ? 3 : 4;
+    static constexpr int kStages = 3;
     static constexpr int kBarFull = 0;
     static constexpr int kBarEmpty = kStages;
     static constexpr int kBarAccFull = 2 * kStages;       // 2: accumulator b holds a finished tile
@@ -64,13 +67,13 @@ struct Layout {
     static constexpr int kBarSum = 2 * kStages + 4;       // the peer's per-row partial sums arrived
     static constexpr int kBarSq = 2 * kStages + 5;        // the peer's squared deviations arrived
     static constexpr int kBarDrain = 2 * kStages + 6;
-    static constexpr int kBarXFull = 2 * kStages + 7;     // the tile's residual rows landed
-    static constexpr int kBarXEmpty = 2 * kStages + 8;    // their buffer (reused for the output) is free
+    static constexpr int kBarXFull = 2 * kStages + 7;     // norm: the tile's residual rows landed
+    static constexpr int kBarXEmpty = 2 * kStages + 8;    // the staging buffer's TMA stores have read it
     static constexpr int kBarYReady = 2 * kStages + 9;    // every epilogue warp wrote its output rows
     static constexpr int kBarEpi = 2 * kStages + 10;      // epilogue rendezvous (row statistics)
     static constexpr int kNumBars = 2 * kStages + 11;
-    static constexpr int kOffX = kStages * kStageBytes;  // residual: 4 boxes of 128 rows x 64 columns
-    static constexpr int kXBytes = kNorm ? 4 * kABoxBytes : 0;
+    static constexpr int kOffX = kStages * kStageBytes;  // staging: 4 boxes of 128 rows x 64 columns
+    static constexpr int kXBytes = 4 * kABoxBytes;
     static constexpr int kOffBar = kOffX + kXBytes;
     // float recv_sum[128], recv_sq[128] (16-byte aligned, as are the vectors after them)
     static constexpr int kOffStat = (kOffBar + 8 * kNumBars + 15) / 16 * 16;
@@ -198,7 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant__ CUtensorMap a1,
                 const __grid_constant__ CUtensorMap a2, const __grid_constant__ CUtensorMap w0,
                 const __grid_constant__ CUtensorMap w1, const __grid_constant__ CUtensorMap w2,
-                const __grid_constant__ GemmParams p)
+                const __grid_constant__ CUtensorMap c0, const __grid_constant__ CUtensorMap c1,
+                const __grid_constant__ CUtensorMap c2, const __grid_constant__ GemmParams p)
 {
     using Lay = Layout<kNorm>;
     extern __shared__ uint8_t smem_raw[];
@@ -239,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < p.nprob; ++i) {
             prefetch_tmap(pick(i, &a0, &a1, &a2));
             prefetch_tmap(pick(i, &w0, &w1, &w2));
+            if (!kNorm) prefetch_tmap(pick(i, &c0, &c1, &c2));
         }
     }
     tc_fence_before();
@@ -379,14 +384,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t acc = lane_base + 256u * b;
-            const int row = g.m0 + r;
-            const bool valid = row < pr.M;
             const int nchunks = g.bn / 32;
             // This warp's chunks: the first or the second half of the tile's columns.
             const int c_begin = hf * ((nchunks + 1) / 2);
             const int c_end = min(nchunks, c_begin + (nchunks + 1) / 2);
             if constexpr (!kNorm) {
-                __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(pr.c) + (size_t)row * pr.N + g.n0;
+                // The previous tile's TMA stores must have read the staging buffer.
+                {
+                    const bool got = mbar_wait(bar(Lay::kBarXEmpty), (i & 1) ^ 1);
+                    ok = __all_sync(0xffffffffu, got);
+                }
+                if (!ok) break;
+                // Row r of staging box j sits at kOffX + j * 16 KB + r * 128 B, its 16-byte
+                // chunks permuted by the 128-byte swizzle (chunk k at k ^ (r % 8)).
+                uint8_t* ybase = smem + Lay::kOffX + r * 128;
                 const bool relu = pr.relu != 0;
                 for (int c = c_begin; c < c_end; ++c) {
                     uint32_t v[32];
@@ -400,14 +411,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(fmaxf(__uint_as_float(v[e]), 0.0f));
                     }
-                    if (valid) {
 #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4)
-                            st_global_v4(crow + 32 * c + 8 * v4,
-                                         pack_bf16x2(__uint_as_float(v[8 * v4]), __uint_as_float(v[8 * v4 + 1])),
-                                         pack_bf16x2(__uint_as_float(v[8 * v4 + 2]), __uint_as_float(v[8 * v4 + 3])),
-                                         pack_bf16x2(__uint_as_float(v[8 * v4 + 4]), __uint_as_float(v[8 * v4 + 5])),
-                                         pack_bf16x2(__uint_as_float(v[8 * v4 + 6]), __uint_as_float(v[8 * v4 + 7])));
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        const int kc = (c % 2) * 4 + v4;
+                        *reinterpret_cast<uint4*>(ybase + (c / 2) * kABoxBytes + ((kc ^ (r & 7)) * 16)) =
+                            make_uint4(pack_bf16x2(__uint_as_float(v[8 * v4]), __uint_as_float(v[8 * v4 + 1])),
+                                       pack_bf16x2(__uint_as_float(v[8 * v4 + 2]), __uint_as_float(v[8 * v4 + 3])),
+                                       pack_bf16x2(__uint_as_float(v[8 * v4 + 4]), __uint_as_float(v[8 * v4 + 5])),
+                                       pack_bf16x2(__uint_as_float(v[8 * v4 + 6]), __uint_as_float(v[8 * v4 + 7])));
+                    }
+                }
+                // All rows written (made visible to the async proxy): one thread stores the
+                // tile (rows past M are clipped by the map) and, once the stores have read
+                // the buffer, frees it for the next tile.
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(Lay::kBarYReady));
+                if (warp == 2 && lane == 0) {
+                    if (mbar_wait(bar(Lay::kBarYReady), i & 1)) {
+                        const CUtensorMap* cm = pick(g.p, &c0, &c1, &c2);
+                        for (int j = 0; j < nchunks / 2; ++j)
+                            tma_store_2d(cm, sbase + Lay::kOffX + j * kABoxBytes, g.n0 + 64 * j, g.m0);
+                        bulk_commit_group();
+                        bulk_wait_group_read_all();
+                        mbar_arrive(bar(Lay::kBarXEmpty));
+                    } else {
+                        raise_device_error(p.err_word, HATTN_ETIMEOUT);
                     }
                 }
             } else {
@@ -541,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(bar(Lay::kBarAccEmpty + b));
         }
         if (!ok) raise_device_error(p.err_word, HATTN_ETIMEOUT);
-        if (kNorm && warp == 2 && lane == 0) bulk_wait_group_all();
+        if (warp == 2 && lane == 0) bulk_wait_group_all();
     }
 
     tc_fence_before();
@@ -564,8 +593,8 @@ int sm_count()
 }
 
 template <bool kNorm>
-cudaError_t launch(const CUtensorMap* a, const CUtensorMap* w, const GemmParams& p, int grid,
-                   int cluster, cudaStream_t stream)
+cudaError_t launch(const CUtensorMap* a, const CUtensorMap* w, const CUtensorMap* c, const GemmParams& p,
+                   int grid, int cluster, cudaStream_t stream)
 {
     constexpr int kSmemBytes = Layout<kNorm>::kSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<kNorm>,
@@ -585,7 +614,7 @@ cudaError_t launch(const CUtensorMap* a, const CUtensorMap* w, const GemmParams&
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<kNorm>, a[0], a[1], a[2], w[0], w[1], w[2], p);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<kNorm>, a[0], a[1], a[2], w[0], w[1], w[2], c[0], c[1], c[2], p);
 }
 
 }  // namespace
@@ -598,7 +627,7 @@ cudaError_t launch_proj_gemm(const ProjProblem* problems, int count, cudaStream_
     p.nprob = count;
     p.split = 1;
     p.err_word = err_word;
-    CUtensorMap a[3], w[3];
+    CUtensorMap a[3], w[3], c[3];
     int tiles = 0;
     for (int i = 0; i < 3; ++i) {
         const ProjProblem& pr = problems[i < count ? i : count - 1];
@@ -606,6 +635,7 @@ cudaError_t launch_proj_gemm(const ProjProblem* problems, int count, cudaStream_
             return cudaErrorInvalidValue;
         a[i] = pr.a;
         w[i] = pr.w;
+        c[i] = pr.cmap;
         GemmProblem& g = p.prob[i];
         g.c = pr.c;
         g.bias = pr.bias;
@@ -619,7 +649,7 @@ cudaError_t launch_proj_gemm(const ProjProblem* problems, int count, cudaStream_
     }
     p.tiles = tiles;
     const int grid = std::min(tiles, sm_count());
-    return launch<false>(a, w, p, grid, 1, stream);
+    return launch<false>(a, w, c, p, grid, 1, stream);
 }
 
 cudaError_t launch_outproj_ln(const OutProjLnArgs& args, cudaStream_t stream, int* err_word)
@@ -648,7 +678,8 @@ cudaError_t launch_outproj_ln(const OutProjLnArgs& args, cudaStream_t stream, in
     int grid;
     if (p.split == 2) grid = 2 * std::min(p.tiles, sm_count() / 2);
     else grid = std::min(p.tiles, sm_count());
-    return launch<true>(a, w, p, grid, p.split, stream);
+    const CUtensorMap c[3] = {args.ymap, args.ymap, args.ymap};  // unused by the norm epilogue
+    return launch<true>(a, w, c, p, grid, p.split, stream);
 }
 
 }  // namespace hattn
