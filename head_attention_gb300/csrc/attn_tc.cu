@@ -23,7 +23,7 @@
 // issuer that waits behind a busy softmax warp for issue slots delays the
 // tensor pipe (measured: 7% at D=64, 3% at D=128).
 //   warp 0      TMA: the unit's Q tiles, then K_j (128 keys) through a
-//               3-stage (D=128) / 6-stage (D=64) shared-memory ring.
+//               3-stage (D=128) / 7-stage (D=64) shared-memory ring.
 //   warp 2      TMA: V_j through a 2-stage (D=128) / 5-stage (D=64) ring. K
 //               runs one block ahead of V because S(j+1) precedes PV(j) (D=64)
 //               or follows it at once (D=128).
@@ -103,7 +103,7 @@ template <int D>
 struct Cfg {
     static constexpr int kBoxes = D / 64;
     static constexpr int kTileBytes = 128 * D * 2;
-    static constexpr int kKStages = (D == 128) ? 3 : 6;
+    static constexpr int kKStages = (D == 128) ? 3 : 7;
     static constexpr int kVStages = (D == 128) ? 2 : 5;
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + 2 * kTileBytes;
