@@ -6,7 +6,7 @@
 // You Need", §没有循环，模型怎样知道词序？).
 //
 // Two kernels. Problems of 16 MB or more whose rows are 16-byte multiples at
-// 16-byte aligned addresses take the bulk-copy path below (79 % of the measured
+// 16-byte aligned addresses take the bulk-copy path below (83 % of the measured
 // HBM copy bandwidth on B=16 n=8192 d_model=512 bf16, against 66 % for the
 // register path). Otherwise, the register path:
 // Layout of the work: the encoding depends on (t, i) only, so a thread owns
@@ -160,15 +160,15 @@ __global__ void __launch_bounds__(kThreads)
 // Rows of 16-byte multiples at 16-byte aligned addresses stream through shared
 // memory by bulk copies instead: a persistent CTA (one per SM) walks chunks of
 // R positions x Bc batch rows (each batch row's R rows are contiguous, one copy
-// each) through a 3-stage ring. Warp 0 moves the data: it loads a stage, and
+// each) through a 4-stage ring of 48 KB stages. Warp 0 moves the data: it loads a stage, and
 // once the other 31 warps report the chunk computed (an mbarrier, no block-wide
 // barrier) stores it back and refills the stage two chunks ahead after the
 // stores out of it have been read. The compute warps compute sin/cos once per
 // (position, frequency) of the chunk and apply them to its Bc batch rows in
 // place. Two chunks of loads stay in flight per SM, without registers holding them.
-constexpr int kBulkStages = 3;
+constexpr int kBulkStages = 4;
 constexpr int kBulkThreads = 1024;
-constexpr uint32_t kBulkStageBytes = 64 * 1024;
+constexpr uint32_t kBulkStageBytes = 48 * 1024;
 constexpr int kBulkMaxHalfD = 2048;  // turn table of half_d (hi, lo) pairs: 16 KB
 
 struct BulkShape {
