@@ -124,17 +124,11 @@ struct Cfg {
     // PV_t(j) retired for a block that is not the tile's last.
     static constexpr int kBarSFree = kBarDrain + 2;
     static constexpr int kBarPVDone = kBarSFree + 2;
-    // P over S only: the first half of P_t (keys 0-63) written (one arrival per warp).
-    static constexpr int kBarPHalf = kBarPVDone + 2;
-    static constexpr int kNumBars = kBarPHalf + 2;
+    static constexpr int kNumBars = kBarPVDone + 2;
     // TMEM columns inside a tile's 256. With D = 64 P gets columns of its own
     // (S 128 + P 64 + O 64), so S(j+1) can be computed while block j's
     // exponentials run; with D = 128 P is written over the first half of S.
     static constexpr bool kSepP = (D == 64);
-    // With P over S, S(j+1) follows PV(j) on the tensor pipe; P is handed over in
-    // two halves so that the first half of PV(j) runs during the exponentials of
-    // the second half.
-    static constexpr bool kSplitP = !kSepP;
     static constexpr uint32_t kColP = kSepP ? 128u : 0u;
     static constexpr uint32_t kColO = kSepP ? 192u : 128u;
     static_assert(kColO + D <= 256, "TMEM columns of a tile");
@@ -352,13 +346,13 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint6
     }
 }
 
-template <int D, int kKs0 = 0, int kKs1 = 8>
+template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
                                          bool accumulate)
 {
     using C = Cfg<D>;
 #pragma unroll
-    for (int ks = kKs0; ks < kKs1; ++ks) {
+    for (int ks = 0; ks < 8; ++ks) {
         // 16 keys = 16 rows of the V tile (2 swizzle atoms of 8 rows); P columns hold bf16 pairs.
         mma_ts(d_tmem, p_tmem + ks * 8, v_desc + ((ks * 2048) >> 4), C::kIdescPV,
                (accumulate || ks > 0) ? 1u : 0u);
@@ -554,14 +548,10 @@ __device__ void issue_tile_mmas(Cta c, const TcParams& p, const Sched& sch, int 
                 // K(j+1) has normally landed long before P(j) is written; waiting for it
                 // first keeps the wait off the path from P(j) to S(j+1).
                 if (has_next && !mbar_wait(c.bar(C::kBarKFull + sk1), phk1)) { ok = false; break; }
-                // Keys 0-63 of block j as soon as their half of P is written, then keys 64-127.
-                if (c.aborted() || !mbar_wait(c.bar(C::kBarPHalf + t), pc & 1)) { ok = false; break; }
-                tc_fence_after();
-                issue_pv<D, 0, 4>(tO, tS, vdesc(sv), j > 0);
                 if (c.aborted() || !mbar_wait(c.bar(C::kBarP + t), pc & 1)) { ok = false; break; }
                 ++pc;
                 tc_fence_after();
-                issue_pv<D, 4, 8>(tO, tS, vdesc(sv), true);
+                issue_pv<D>(tO, tS, vdesc(sv), j > 0);
                 // S(j+1) right behind PV(j); the commits that only release buffers follow it.
                 if (has_next && j + 1 < nb) {
                     issue_qk<D>(tS, q_desc, kdesc(sk1));
@@ -649,56 +639,6 @@ __device__ __forceinline__ float exp_block(const uint32_t (&sr)[128], uint64_t c
             }
             mx = max3f(mx, max3f(g[0], g[1], g[2]), g[3]);
         }
-    }
-    return mx;
-}
-
-// p = 2^(s * c - m) for the 32 scores of quarter q of this thread's row,
-// packed to bf16 pairs in pk; the fp32 sum goes to acc.
-__device__ __forceinline__ void exp_quarter(const uint32_t (&sr)[128], int q, uint64_t c2, uint64_t nm2,
-                                            uint64_t (&acc)[4], uint32_t (&pk)[16])
-{
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const int e = 32 * q + 2 * i;
-        const uint64_t x2 = fma_f32x2(f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nm2);
-        float t0, t1;
-        f32x2_split(x2, t0, t1);
-        const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
-        acc[i & 3] = add_f32x2(acc[i & 3], f32x2(p0, p1));
-        pk[i] = pack_bf16x2(p0, p1);
-    }
-}
-
-// Max of the 32 raw scores of quarter q.
-__device__ __forceinline__ float max_quarter(const uint32_t (&sr)[128], int q)
-{
-    float g[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const uint32_t* v8 = sr + 32 * q + 8 * k;
-        g[k] = max3f(max3f(__uint_as_float(v8[0]), __uint_as_float(v8[1]), __uint_as_float(v8[2])),
-                     max3f(__uint_as_float(v8[3]), __uint_as_float(v8[4]), __uint_as_float(v8[5])),
-                     fmaxf(__uint_as_float(v8[6]), __uint_as_float(v8[7])));
-    }
-    return max3f(g[0], g[1], fmaxf(g[2], g[3]));
-}
-
-// The first half of P (keys 0-63: quarters 0 and 1) stored into 32 TMEM columns
-// from p_taddr. With kMax, the max of all 128 raw scores is computed alongside
-// and returned, so the whole block's growth is known before this half is
-// handed to the tensor pipe.
-template <bool kMax>
-__device__ __forceinline__ float exp_first_half(const uint32_t (&sr)[128], uint64_t c2, uint64_t nm2,
-                                                uint64_t (&acc)[4], uint32_t p_taddr)
-{
-    float mx = -INFINITY;
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        uint32_t pk[16];
-        exp_quarter(sr, q, c2, nm2, acc, pk);
-        tmem_st_x16(p_taddr + 16 * q, pk);
-        if (kMax) mx = max3f(mx, max_quarter(sr, 2 * q), max_quarter(sr, 2 * q + 1));
     }
     return mx;
 }
@@ -801,52 +741,7 @@ __device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, 
                     tc_fence_after();
                 }
             }
-            if (C::kSplitP && work && ok) {
-                // As below, with P handed over in two halves: the first half's
-                // exponentials compute the whole block's max alongside, so a growing
-                // max is handled (O rescaled, the half redone) before any of P
-                // reaches the tensor pipe; the third quarter is computed before the
-                // wait for the first half's stores, which have completed by then.
-                const uint64_t c2 = f32x2(p.scale_log2, p.scale_log2);
-                uint64_t acc[4] = {0, 0, 0, 0};
-                const float mx =
-                    exp_first_half<true>(sr, c2, f32x2(-m_used, -m_used), acc, lane_base + cP) * p.scale_log2;
-                const bool grow = j > 0 && mx > m_used + kRescaleLog2;
-                if (__any_sync(0xffffffffu, grow)) {
-                    const float m_new = grow ? mx : m_used;
-                    const float alpha = ex2_approx(m_used - m_new);  // 1 where the max is kept
-#pragma unroll
-                    for (int q = 0; q < D / 16; ++q) {
-                        uint32_t o[16];
-                        tmem_ld_x16(lane_base + cO + 16 * q, o);  // PV up to block j-1 is complete
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st_x16(lane_base + cO + 16 * q, o);
-                    }
-                    l *= alpha;
-                    m_used = m_new;
-                    acc[0] = acc[1] = acc[2] = acc[3] = 0;
-                    exp_first_half<false>(sr, c2, f32x2(-m_used, -m_used), acc, lane_base + cP);
-                }
-                const uint64_t nm2 = f32x2(-m_used, -m_used);
-                uint32_t pk[16];
-                exp_quarter(sr, 2, c2, nm2, acc, pk);
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(c.bar(C::kBarPHalf + t));
-                tmem_st_x16(lane_base + cP + 32, pk);
-                exp_quarter(sr, 3, c2, nm2, acc, pk);
-                tmem_st_x16(lane_base + cP + 48, pk);
-                if (kPingPong<D> && (t == 0 || j + 1 < R)) named_arrive(other_turn, 256);
-                float a0, a1;
-                f32x2_split(add_f32x2(add_f32x2(acc[0], acc[1]), add_f32x2(acc[2], acc[3])), a0, a1);
-                l += a0 + a1;
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(c.bar(C::kBarP + t));
-            } else if (work && ok) {
+            if (work && ok) {
                 // p = 2^(s * scale * log2(e) - m) with the running max m (scale > 0, so
                 // the max of scale * s is scale * max s). After the first block the
                 // block's own max is found alongside the exponentials; a row whose max
@@ -967,7 +862,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(c.bar(C::kBarO + t), 1);
             mbar_init(c.bar(C::kBarSFree + t), 4);
             mbar_init(c.bar(C::kBarPVDone + t), 1);
-            mbar_init(c.bar(C::kBarPHalf + t), 4);
         }
         mbar_init(c.bar(C::kBarDrain), 1);
         mbar_init(c.bar(C::kBarDrain + 1), 1);
