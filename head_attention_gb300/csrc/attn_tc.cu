@@ -32,7 +32,9 @@
 //               and S_t(j+1). Completion is reported by tcgen05.commit onto
 //               mbarriers. With one issuer per tile, a tile whose P is ready
 //               never waits behind the other tile's MMA issue, and one tile's
-//               softmax overlaps the other tile's MMAs.
+//               softmax overlaps the other tile's MMAs. Nothing but the MMAs
+//               sits between P(j) and S(j+1) (D = 128): K(j+1) is waited for
+//               before P(j), and the commits that release buffers follow S(j+1).
 //   warps 4-7   softmax of tile 0, warps 8-11 softmax of tile 1; at D = 128
 //               they take turns on the exponentials (two named barriers), so
 //               that the MUFU work of one tile overlaps the MMAs of the other
