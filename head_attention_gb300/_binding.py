@@ -24,7 +24,7 @@ EXPORTED = ("attn_fwd", "attn_fwd_lse", "attn_bwd", "attn_bwd_workspace_bytes", 
             "mha_fwd_noalloc", "mha_workspace_bytes", "pos_encoding_fwd", "ffn_fwd",
             "ffn_workspace_bytes", "encoder_layer_fwd", "encoder_layer_workspace_bytes",
             "decoder_layer_fwd", "decoder_layer_workspace_bytes", "hattn_status_str",
-            "hattn_check_device_error", "hattn_version")
+            "hattn_check_device_error", "hattn_version", "hattn_selftest_wait_timeout")
 
 
 class MhaWeights(ctypes.Structure):
@@ -103,6 +103,8 @@ def load() -> ctypes.CDLL:
         lib.hattn_check_device_error.restype = i
         lib.hattn_version.argtypes = []
         lib.hattn_version.restype = i
+        lib.hattn_selftest_wait_timeout.argtypes = [vp]
+        lib.hattn_selftest_wait_timeout.restype = i
         _lib = lib
         return lib
 
@@ -263,6 +265,12 @@ def check_device_error(stream=None) -> int:
 
 def version() -> int:
     return int(load().hattn_version())
+
+
+def selftest_wait_timeout(stream=None) -> int:
+    """Enqueues the kernel whose device wait never completes and must give up on
+    its own (HATTN_ETIMEOUT in the device error word); returns the launch status."""
+    return int(load().hattn_selftest_wait_timeout(_stream(stream)))
 
 
 def ffn_workspace_bytes(dtype, M, d_model, d_ff) -> int:

@@ -11,6 +11,7 @@
 #include <unordered_map>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace hattn {
 
@@ -653,5 +654,36 @@ int hattn_check_device_error(hattn_stream_t stream)
 }
 
 int hattn_version(void) { return 100; }
+
+}  // extern "C"
+
+namespace hattn {
+namespace {
+
+// One thread waits on an mbarrier that nothing arrives on, through the same
+// bounded wait every pipeline of this library uses; when the wait gives up it
+// raises HATTN_ETIMEOUT in the device error word and the kernel returns.
+__global__ void wait_timeout_selftest_kernel(int* err_word)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    const uint32_t b = smem_u32(&bar);
+    mbar_init(b, 1);
+    fence_barrier_init();
+    if (!mbar_wait(b, 0)) raise_device_error(err_word, HATTN_ETIMEOUT);
+}
+
+}  // namespace
+}  // namespace hattn
+
+extern "C" {
+
+int hattn_selftest_wait_timeout(hattn_stream_t stream)
+{
+    int* err = hattn::device_error_ptr();
+    if (!err) return HATTN_ECUDA;
+    hattn::wait_timeout_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err);
+    return hattn::from_cuda(cudaGetLastError());
+}
 
 }  // extern "C"

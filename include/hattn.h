@@ -354,6 +354,21 @@ int hattn_check_device_error(hattn_stream_t stream);
 /* Library version, major*10000 + minor*100 + patch. */
 int hattn_version(void);
 
+/*
+ * hattn_selftest_wait_timeout — exercises the failure path of the pipelines.
+ *
+ * Not an operation of the pages: a check that a device-side wait which never
+ * completes ends by itself. It enqueues on `stream` one small kernel whose
+ * single thread waits on a shared-memory barrier that nothing arrives on,
+ * through the same bounded wait (about two seconds of SM clock cycles) that
+ * every pipeline of this library uses. When the wait gives up the kernel sets
+ * HATTN_ETIMEOUT in the device error word and returns normally: no trap, no
+ * fault, and the CUDA context stays usable. Afterwards
+ * hattn_check_device_error(stream) returns HATTN_ETIMEOUT (and clears it).
+ * Returns HATTN_OK once the kernel is enqueued, or HATTN_ECUDA.
+ */
+int hattn_selftest_wait_timeout(hattn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
