@@ -11,17 +11,23 @@ The timed steps replay a CUDA graph of one step (no per-call host overhead;
 --no-graph times eager calls instead). Default workload: long-sequence causal
 self-attention, bf16, B=4 h=16 n=8192 d=128 (Q, K, V and O are 134 MB each, so
 the 402 MB of inputs are larger than the 129 MB L2 and every step streams
-them from HBM).
+them from HBM). The same run also measures the other configurations the metric
+is quoted on (long causal d=64 h=32, encoder fp32, decoder causal, cross-attention
+with key padding, the MHA sublayer) and reports each under "configs" with the
+same fields; --configs none skips them.
 
 FLOPs per step are the defined count 4*B*h*n_q*n_k*d, halved for causal (plus
 2*M*N*K for each of the four projections of the MHA sublayer).
-Timing: W untimed warm-up steps, then exactly K steps between two CUDA events
-on the launching stream, bracketed by a barrier and a device synchronize;
-max over ranks. SM clocks and throttle reasons are sampled with nvidia-smi
-during the timed region. The e2e leg repeats the measurement with the host
-copies in the timed region: pinned host Q/K/V -> device, attn_fwd, output ->
-pinned host. The CPU baseline is the fp64 oracle on a bounded sample of the
-same workload on this host's cores.
+Timing: W untimed warm-up steps, then exactly K steps on the launching stream
+with a CUDA event at every step boundary (median, p10 and p90 of the per-step
+times are reported), bracketed by a barrier and a device synchronize; max over
+ranks. Inputs that fit in L2 are timed cold: a write larger than L2 precedes
+every step, outside its events. A sustained leg then replays a graph of many
+steps back to back for a few seconds while nvidia-smi samples the SM clock,
+throttle reasons and power, so the clock under load is on record. The e2e leg
+repeats the measurement with the host copies in the timed region: pinned host
+Q/K/V -> device, attn_fwd, output -> pinned host. The CPU baseline is the fp64
+oracle on a bounded sample of the same workload on this host's cores.
 
 --impl reference times the fp64 CPU oracle itself (the only other
 implementation of this method) on the same workload, metric and unit.
@@ -67,6 +73,12 @@ NOMINAL_HBM_GBS = 8000.0
 L2_BYTES = 129e6
 FLUSH_BYTES = 256 << 20  # > L2: written before every timed step when the inputs fit in L2
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+FP32_FMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # SMs x fp32 lanes x 2 FLOP x max SM clock
+MIN_CLOCK_SAMPLES = 5  # fewer samples inside a window say nothing about its clock
+# The other configurations the metric is quoted on, measured in the same run as the
+# default workload, each with its own roofline, per-step spread, e2e and clocks.
+COMPANION_WORKLOADS = ("long_causal_d64", "enc_self_f32", "dec_causal_bf16", "cross_bf16",
+                       "mha_bf16")
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = ("head_attention_gb300/csrc/attn_tc.cu", "head_attention_gb300/csrc/ptx.cuh")
 
@@ -89,6 +101,14 @@ def parse_args(argv=None):
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size B (smaller cases for profiler "
                          "captures; the default keeps the named workload)")
+    ap.add_argument("--configs", default="all", choices=["all", "none"],
+                    help="with the default workload, also measure the other configurations "
+                         "the metric is quoted on")
+    ap.add_argument("--sustained-s", type=float, default=3.0,
+                    help="seconds of back-to-back steps in the default workload's sustained leg")
+    ap.add_argument("--companion-sustained-s", type=float, default=1.0,
+                    help="seconds of the sustained leg of every other configuration")
+    ap.add_argument("--no-sustained", action="store_true")
     return ap.parse_args(argv)
 
 
@@ -156,24 +176,25 @@ def profiled_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons."""
+    """nvidia-smi samples (every 100 ms) of SM clock, power and throttle reasons,
+    taken for the whole run; summary(window) reduces the samples of one window."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 100
 
     def __init__(self, gpu_id: str):
         self.gpu_id = gpu_id
         self.samples = []
         self.proc = None
         self.thread = None
-        self.window = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -186,9 +207,6 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
 
-    def mark(self, t0, t1):
-        self.window = (t0, t1)
-
     def __exit__(self, *exc):
         if self.proc is not None:
             self.proc.terminate()
@@ -199,14 +217,16 @@ class ClockSampler:
         if self.thread is not None:
             self.thread.join(timeout=5)
 
-    def summary(self):
-        if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
-        rows = self.samples
-        if self.window:
-            t0, t1 = self.window
-            inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.15]
-            rows = inside or sorted(rows, key=lambda r: abs(r[0] - (t0 + t1) / 2))[:3]
+    def summary(self, window=None):
+        """Median SM clock and power, max clock and the throttle reasons seen, over the
+        samples taken inside window = (t0, t1) (wall clock; every sample if None)."""
+        rows = list(self.samples)
+        if window is not None:
+            t0, t1 = window
+            rows = [r for r in rows if t0 <= r[0] <= t1 + self.PERIOD_MS * 1e-3]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0,
+                    "reasons": ["no nvidia-smi samples inside the window"]}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = set()
         mhz, max_mhz, watts = [], [], []
@@ -222,7 +242,9 @@ class ClockSampler:
                     reasons.add(name)
         return {"sm_mhz": statistics.median(mhz) if mhz else None,
                 "sm_max_mhz": max(max_mhz) if max_mhz else None,
+                "sm_mhz_min": min(mhz) if mhz else None,
                 "power_w_median": statistics.median(watts) if watts else None,
+                "power_w_max": max(watts) if watts else None,
                 "samples": len(mhz), "reasons": sorted(reasons)}
 
 
@@ -584,8 +606,10 @@ def _setup_bwd(w, inp):
 
 
 def io_bytes(w, inp):
-    """(input bytes, algorithmic bytes moved) of one step: every input read once, the output
-    written once."""
+    """(resident input bytes, algorithmic bytes) of one step. Resident bytes are every
+    input tensor as it sits in HBM (they decide whether the step fits in L2);
+    algorithmic bytes are the inputs the method must read once plus the output written
+    once. With key padding only the first key_lens[b] rows of K and V are read."""
     esize = 4 if w.dtype == "f32" else 2
     if w.kind == "mha":
         bytes_in = (2 * w.B * w.n_q * w.d_model + 4 * w.d_model * w.h * w.d_k) * esize
@@ -601,62 +625,247 @@ def io_bytes(w, inp):
         bytes_in = (qkv + 2 * w.B * w.n_q * w.h * w.d_v) * esize + 4 * w.B * w.h * w.n_q
         bytes_alg = bytes_in + qkv * esize
     elif w.kind == "decode":
-        bytes_in = (float(inp["key_lens"].sum()) * w.h * (w.d_k + w.d_v) + w.B * w.h * w.d_k) * esize
-        bytes_alg = bytes_in + w.B * w.h * w.d_v * esize
+        bytes_in = (w.B * w.n_k * w.h * (w.d_k + w.d_v) + w.B * w.h * w.d_k) * esize
+        bytes_alg = ((float(inp["key_lens"].sum()) * w.h * (w.d_k + w.d_v) + w.B * w.h * w.d_k)
+                     * esize + w.B * w.h * w.d_v * esize)
     elif w.kind == "pe":
         bytes_in = w.B * w.n_q * w.d_model * esize
         bytes_alg = 2 * bytes_in
     else:
+        q_o = w.B * w.n_q * w.h * (w.d_k + w.d_v) * esize
         bytes_in = (w.B * w.n_q * w.h * w.d_k + w.B * w.n_k * w.h * (w.d_k + w.d_v)) * esize
-        bytes_alg = bytes_in + w.B * w.n_q * w.h * w.d_v * esize
+        kv_rows = w.B * w.n_k
+        if inp is not None and inp.get("key_lens") is not None:
+            kv_rows = int(inp["key_lens"].astype("int64").sum())
+        bytes_alg = q_o + kv_rows * w.h * (w.d_k + w.d_v) * esize
     return bytes_in, bytes_alg
 
 
-def run_gpu(args, rank, world, local):
-    import torch
+def visible_pair_flops(w, inp):
+    """4*d FLOPs per visible (query, key) pair: the count the method performs (the
+    metric's defined count differs only under key padding, where it stays dense)."""
+    if w.kind != "attn":
+        return None
+    if inp is not None and inp.get("key_lens") is not None and w.mask_kind & 2:
+        lens = inp["key_lens"].astype("float64")
+        if w.mask_kind & 1:
+            n = w.n_q
+            pairs = sum(min(L, n) * (min(L, n) + 1) / 2 for L in lens)
+        else:
+            pairs = float(lens.sum()) * w.n_q
+        return 4.0 * w.h * w.d_k * pairs
+    if w.mask_kind & 1:
+        return 4.0 * w.B * w.h * w.d_k * w.n_q * (w.n_q + 1) / 2
+    return 4.0 * w.B * w.h * w.d_k * w.n_q * w.n_k
 
-    import head_attention_gb300 as hattn
+
+def setup_workload(w):
+    """(inputs, step closure, host buffers for the e2e leg, launches per step,
+    defined FLOPs per step) of one workload, its inputs already on the device."""
     from synth import inputs as synth
-
-    torch.cuda.set_device(local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    hattn.build()
-    hattn.load()
-    w = load_workload(args)
     if w.kind == "mha":
         inp = synth.mha_inputs(w)
-        step, host, launches_per_step = _setup_mha(w, inp)
+        step, host, launches = _setup_mha(w, inp)
         flops = w.attn_flops() + w.proj_flops()
     elif w.kind == "decode":
         inp = synth.attn_inputs(w)
-        step, host, launches_per_step = _setup_decode(w, inp)
+        step, host, launches = _setup_decode(w, inp)
         flops = 4.0 * w.h * w.d_k * float(inp["key_lens"].sum())  # visible (query, key) pairs
     elif w.kind == "bwd":
         inp = synth.attn_bwd_inputs(w)
-        step, host, launches_per_step = _setup_bwd(w, inp)
+        step, host, launches = _setup_bwd(w, inp)
         flops = 2.5 * w.attn_flops()  # five n_q x n_k x d contractions against the forward's two
     elif w.kind in ("encoder", "decoder"):
         inp = synth.layer_inputs(w)
-        step, host, launches_per_step = _setup_layer(w, inp)
+        step, host, launches = _setup_layer(w, inp)
         flops = w.layer_flops()
     elif w.kind == "pe":
         inp = pe_inputs(w)
-        step, host, launches_per_step = _setup_pe(w, inp)
+        step, host, launches = _setup_pe(w, inp)
         flops = 0.0
     else:
         inp = synth.attn_inputs(w)
-        step, host, launches_per_step = _setup_attention(w, inp)
+        step, host, launches = _setup_attention(w, inp)
         flops = w.attn_flops()
-    stream = torch.cuda.current_stream()
+    return inp, step, host, launches, flops
 
+
+def percentiles(xs):
+    """(p10, median, p90) of a list of per-step times, by linear interpolation."""
+    s = sorted(xs)
+    if not s:
+        return None, None, None
+
+    def q(f):
+        pos = f * (len(s) - 1)
+        lo = int(math.floor(pos))
+        hi = min(lo + 1, len(s) - 1)
+        return s[lo] + (s[hi] - s[lo]) * (pos - lo)
+    return q(0.1), q(0.5), q(0.9)
+
+
+def time_steps(run_step, stream, steps, flush):
+    """Device time of `steps` consecutive steps with CUDA events on the launching stream.
+
+    Without a flush buffer the steps run back to back and an event is recorded at every
+    step boundary: the total is first to last event, each step the gap between two
+    neighbours. With one (inputs that fit in L2) a write larger than L2 precedes every
+    step outside its pair of events, and the total is the sum of the per-step times.
+    Returns (total ms, per-step ms list, wall-clock window)."""
+    import torch
+    torch.cuda.synchronize()
+    t0 = time.time()
+    if flush is not None:
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        for i in range(steps):
+            flush.fill_(i & 255)
+            starts[i].record(stream)
+            run_step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        total = sum(per)
+    else:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        ev[0].record(stream)
+        for i in range(steps):
+            run_step()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+        total = ev[0].elapsed_time(ev[steps])
+    return total, per, (t0, time.time())
+
+
+def sustained_leg(step, stream, flops, bytes_alg, seconds, peaks, hbm_bound, warm_l2):
+    """Back-to-back replays of a CUDA graph of many steps for about `seconds`, with the
+    SM clock and board power sampled throughout: the throughput a long run sees and the
+    clock it ran at (time x median MHz compares runs at different clocks)."""
+    import torch
+    step_ms = _probe_step_ms(step, stream)
+    per_graph = max(1, min(4096, int(math.ceil(50.0 / max(step_ms, 1e-3)))))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(per_graph):
+            step()
+    graph.replay()
+    torch.cuda.synchronize()
+    replays = max(2, int(math.ceil(seconds * 1e3 / (per_graph * step_ms))))
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(stream)
+    for _ in range(replays):
+        graph.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    del graph
+    steps = replays * per_graph
+    ms = start.elapsed_time(end) / steps
+    rec = {"seconds": round(steps * ms * 1e-3, 3), "steps": steps, "ms_per_step": round(ms, 5),
+           "_clock_window": (t0, t1),
+           "l2": "warm: steps back to back, inputs stay in L2" if warm_l2 else
+                 "inputs larger than L2, streamed from HBM every step"}
+    if hbm_bound:
+        gbs = bytes_alg / (ms * 1e-3) / 1e9
+        rec.update({"gbs_at_algorithmic_bytes": round(gbs, 1),
+                    "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4)})
+    if flops:
+        tf = flops / (ms * 1e-3) / 1e12
+        rec.update({"value": round(tf, 2), "unit": "TFLOP/s",
+                    "frac_of_sustained_bf16": round(tf / peaks["bf16_tflops_sustained"], 4),
+                    "bf16_tflops_sustained": peaks["bf16_tflops_sustained"]})
+    return rec
+
+
+def _probe_step_ms(step, stream):
+    """A rough per-step time (a few eager steps) to size the sustained graph."""
+    import torch
+    step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(5):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / 5
+
+
+def roofline_of(w, kernel, flops, alg_flops, bytes_alg, step_ms, peaks, peak_src):
+    """The roofline record of one workload's step: the bound is the larger of the two
+    roofline times (FLOPs at the tensor (bf16) or fp32 FMA peak, algorithmic bytes at
+    the measured HBM bandwidth); achieved and frac are taken against that bound."""
+    alg = alg_flops if alg_flops is not None else flops
+    gbs = bytes_alg / (step_ms * 1e-3) / 1e9
+    tf = alg / (step_ms * 1e-3) / 1e12
+    tensor_path = w.dtype == "bf16" and w.kind != "pe" and (
+        w.kind != "bwd" or (w.d_k == w.d_v and w.d_k in (64, 128)))
+    if w.kind in ("decode", "pe") or alg == 0:
+        bound = "hbm"
+    else:
+        flop_peak = peaks["bf16_tflops"] if tensor_path else FP32_FMA_TFLOPS
+        t_flop = alg / (flop_peak * 1e12)
+        t_hbm = bytes_alg / (peaks["hbm_gbs"] * 1e9)
+        bound = ("tensor" if tensor_path else "alu") if t_flop >= t_hbm else "hbm"
+    rec = {"kernel": kernel, "bound": bound}
+    if bound == "hbm":
+        rec.update({"achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(gbs / peaks["hbm_gbs"], 4),
+                    "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                    "frac_of_nominal_8000": round(gbs / NOMINAL_HBM_GBS, 4)})
+    elif bound == "tensor":
+        rec.update({"achieved": round(tf, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": round(tf / peaks["bf16_tflops"], 4),
+                    "peak_source": f"{peak_src} (burst, MEASURED_PEAKS.json bf16_tflops)",
+                    "frac_of_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
+                    "frac_of_nominal_2250": round(tf / NOMINAL_BF16_TFLOPS, 4)})
+    else:
+        rec.update({"achieved": round(tf, 3), "peak": round(FP32_FMA_TFLOPS, 1), "unit": "TFLOP/s",
+                    "frac": round(tf / FP32_FMA_TFLOPS, 4),
+                    "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2070 MHz (fp32 FMA)"})
+    rec.update({"algorithmic_flops_per_launch": alg, "defined_flops_per_launch": flops,
+                "algorithmic_bytes_per_launch": bytes_alg,
+                "hbm_gbs_at_algorithmic_bytes": round(gbs, 1),
+                "hbm_frac_at_algorithmic_bytes": round(gbs / peaks["hbm_gbs"], 4),
+                "traffic": profiled_traffic(w.name)})
+    if bound != "tensor" and tensor_path and alg:
+        rec["frac_of_bf16_tensor_peak"] = round(tf / peaks["bf16_tflops"], 4)
+    return rec
+
+
+def kernel_name(w):
+    tc_attn = w.dtype == "bf16" and w.d_k == w.d_v and w.d_k in (64, 128)
+    return {"mha": "mha sublayer: proj_gemm + attn_tc_kernel + outproj_ln (one step)",
+            "encoder": "encoder layer: MHA (proj_gemm, attn_tc_kernel, outproj_ln) + FFN "
+                       "(proj_gemm with bias+ReLU, outproj_ln with bias) (one step)",
+            "decoder": "decoder layer: two MHA sublayers + FFN (eight launches, one step)",
+            "bwd": ("attention backward on tensor cores: row_dot + grads_tc (one step)" if tc_attn
+                    else "attention backward on CUDA cores: row_dot + key_grads + query_grads"),
+            "decode": f"decode_split_kernel<{w.d_k}> + decode_combine_kernel (one step)",
+            "pe": "pos_encoding_kernel"}.get(
+                w.kind, f"attn_tc_kernel<{w.d_k}>" if tc_attn else "attn_simt_kernel")
+
+
+def measure(args, w, world, peaks, peak_src, sustained_s, with_e2e=True):
+    """Everything the bench line reports about one workload except the CPU baseline:
+    defined-FLOP throughput over exactly args.steps timed steps (CUDA-graph replays
+    of one step unless --no-graph), per-step median / p10 / p90, the roofline of the
+    step, a sustained leg with its clock record, and the e2e leg."""
+    import torch
+
+    import head_attention_gb300 as hattn
+    inp, step, host, launches_per_step, flops = setup_workload(w)
+    stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     if hattn.check_device_error(stream) != 0:
-        raise RuntimeError("device error during warm-up")
+        raise RuntimeError(f"{w.name}: device error during warm-up")
     run_step = step
+    graph = None
     if not args.no_graph:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
@@ -665,133 +874,158 @@ def run_gpu(args, rank, world, local):
         torch.cuda.synchronize()
         run_step = graph.replay
 
-    # Inputs that fit in the 129 MB L2 would be served from it after the first
-    # step: then every timed step is preceded by a 256 MB write (outside its
-    # events) and the per-step times are summed.
     bytes_in, bytes_alg = io_bytes(w, inp)
     flush_l2 = bytes_in <= L2_BYTES
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda") if flush_l2 else None
-    n_ev = args.steps if flush_l2 else 1
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    barrier(world)
+    ms_local, per_step, window = time_steps(run_step, stream, args.steps, flush)
+    barrier(world)
+    del flush
+    if hattn.check_device_error(stream) != 0:
+        raise RuntimeError(f"{w.name}: device error during the timed region")
+    ms_step = reduce_max(ms_local, world) / args.steps
+    step_ms_local = ms_local / args.steps
+    hbm_bound_kind = w.kind in ("decode", "pe")
+    alg_flops = visible_pair_flops(w, inp)
+    p10, p50, p90 = percentiles(per_step)
+    rec = {
+        "workload": w.name,
+        "description": w.description,
+        "value": round(aggregate_tflops(flops, world, ms_step), 2) if w.kind != "pe"
+        else round(bytes_alg * world / (ms_step * 1e-3) / 1e9, 1),
+        "unit": metric_of(w)[1],
+        "ms_per_step": round(ms_step, 5),
+        "step_ms": {"p10": round(p10, 5), "median": round(p50, 5), "p90": round(p90, 5),
+                    "min": round(min(per_step), 5), "max": round(max(per_step), 5)},
+        "tokens_per_s": round(w.tokens() * world / (ms_step * 1e-3), 1),
+        "dtype": w.dtype,
+        "l2": (f"inputs {bytes_in / 1e6:.0f} MB > 129 MB L2: streamed from HBM every step, no flush"
+               if not flush_l2 else
+               f"inputs {bytes_in / 1e6:.1f} MB fit in L2: a {FLUSH_BYTES >> 20} MB write "
+               "flushes L2 before every timed step (outside its events); step times summed"),
+        "roofline": roofline_of(w, kernel_name(w), flops, alg_flops, bytes_alg, step_ms_local,
+                                peaks, peak_src),
+        "_clock_window": window,
+        "gpu_launches": args.steps * launches_per_step,
+    }
+    if w.kind != "pe":
+        rec["pct_of_measured_bf16_peak"] = round(100 * flops / (ms_step * 1e-3) / 1e12
+                                                 / peaks["bf16_tflops"], 2)
+        rec["pct_of_nominal_bf16_peak"] = round(100 * flops / (ms_step * 1e-3) / 1e12
+                                                / NOMINAL_BF16_TFLOPS, 2)
+    del graph
+    if sustained_s > 0:
+        rec["sustained"] = sustained_leg(step, stream, flops if w.kind != "pe" else 0.0, bytes_alg,
+                                         sustained_s, peaks,
+                                         hbm_bound_kind or rec["roofline"]["bound"] == "hbm",
+                                         flush_l2)
+        rec["gpu_launches_sustained"] = rec["sustained"]["steps"] * launches_per_step
+    if with_e2e and w.kind != "pe":
+        rec["e2e"] = e2e_leg(args, w, host, step, flops, world)
+        rec["gpu_launches"] += rec["e2e"].pop("launches") * launches_per_step
+    rec["_inp"] = inp
+    return rec
+
+
+def finalize_clocks(rec, sampler, steps):
+    """Fills in a workload record's clock records once sampling has stopped: the
+    sustained leg's own, and the one the line reports for the timed steps. That is
+    the samples inside the timed steps when there are at least MIN_CLOCK_SAMPLES of
+    them, else (a timed region shorter than a few sampling periods) the sustained
+    leg's, which runs right after the timed steps, with the source said."""
+    timed = sampler.summary(rec.pop("_clock_window"))
+    sus = rec.get("sustained")
+    if sus is not None:
+        sus["clocks"] = sampler.summary(sus.pop("_clock_window"))
+        if sus["clocks"].get("sm_mhz"):
+            sus["ms_x_median_mhz"] = round(sus["ms_per_step"] * sus["clocks"]["sm_mhz"], 2)
+    if timed.get("samples", 0) >= MIN_CLOCK_SAMPLES or sus is None:
+        rec["clocks"] = dict(timed, source="timed steps")
+        return
+    rec["clocks"] = dict(
+        sus["clocks"],
+        source=(f"sustained leg ({sus['seconds']} s of back-to-back steps right after the "
+                f"timed steps); the {steps} timed steps ({rec['ms_per_step'] * steps:.3g} ms "
+                f"of device time) held {timed.get('samples', 0)} samples"),
+        timed_region_samples=timed.get("samples", 0),
+        timed_region_reasons=timed.get("reasons", []))
+
+
+def config_of(w, world):
+    """The workload as the bench line names it (the same for both arms)."""
+    cfg = {"workload": w.name, "description": w.description, "B": w.B, "h": w.h,
+           "n_q": w.n_q, "n_k": w.n_k, "d": w.d_k,
+           "mask": {0: "none", 1: "causal", 2: "key_padding", 3: "causal+key_padding"}[w.mask_kind],
+           "parallelism": f"replicas x{world} (independent (batch, head) work per GPU)"}
+    if w.is_mha or w.kind in ("encoder", "decoder"):
+        cfg["d_model"] = w.d_model
+    if w.kind in ("encoder", "decoder"):
+        cfg["d_ff"] = w.d_ff
+    return cfg
+
+
+def run_gpu(args, rank, world, local):
+    import torch
+
+    import head_attention_gb300 as hattn
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    hattn.build()
+    hattn.load()
+    peaks, peak_src = load_peaks()
+    w = load_workload(args)
+    companions = []
+    if args.configs == "all" and w.name == DEFAULT_WORKLOAD and args.batch == 0:
+        from synth import inputs as synth
+        companions = [synth.workload(n) for n in COMPANION_WORKLOADS]
+
     sampler = ClockSampler(gpu_uuid(local))
     with sampler:
-        time.sleep(0.25)  # let the sampler start
-        barrier(world)
-        torch.cuda.synchronize()
-        t_wall0 = time.time()
-        if flush_l2:
-            for i in range(args.steps):
-                flush.fill_(i & 255)
-                starts[i].record(stream)
-                run_step()
-                ends[i].record(stream)
-        else:
-            starts[0].record(stream)
-            for _ in range(args.steps):
-                run_step()
-            ends[0].record(stream)
-        torch.cuda.synchronize()
-        t_wall1 = time.time()
-        barrier(world)
-        sampler.mark(t_wall0, t_wall1)
-        time.sleep(0.15)
-    ms_local = sum(s_.elapsed_time(e_) for s_, e_ in zip(starts, ends))
-    if hattn.check_device_error(stream) != 0:
-        raise RuntimeError("device error during the timed region")
-    ms_total = reduce_max(ms_local, world)
-    ms_step = ms_total / args.steps
-    tflops = aggregate_tflops(flops, world, ms_step)
-    tokens_s = w.tokens() * world / (ms_step * 1e-3)
-
-    peaks, peak_src = load_peaks()
-    step_ms = ms_local / args.steps
-    achieved = flops / (step_ms * 1e-3) / 1e12
-    tc_attn = w.dtype == "bf16" and w.d_k == w.d_v and w.d_k in (64, 128)
-    kernel = {"mha": "mha sublayer: proj_gemm + attn_tc_kernel + outproj_ln (one step)",
-              "encoder": "encoder layer: MHA (proj_gemm, attn_tc_kernel, outproj_ln) + FFN "
-                         "(proj_gemm with bias+ReLU, outproj_ln with bias) (one step)",
-              "decoder": "decoder layer: two MHA sublayers + FFN (eight launches, one step)",
-              "bwd": "attention backward on tensor cores: row_dot + key_grads_tc + query_grads_tc (one step)",
-              "decode": f"decode_split_kernel<{w.d_k}> + decode_combine_kernel (one step)",
-              "pe": "pos_encoding_kernel"}.get(
-                  w.kind, f"attn_tc_kernel<{w.d_k}>" if tc_attn else "attn_simt_kernel")
-    hbm_bound = w.kind in ("decode", "pe")
-    gbs = bytes_alg / (step_ms * 1e-3) / 1e9
-    if w.kind == "bwd" and not (w.dtype == "bf16" and w.d_k == w.d_v and w.d_k in (64, 128)):
-        # CUDA-core kernels: fp32 FMA peak = SMs x 128 lanes x 2 FLOP x max SM clock.
-        alu_peak = 152 * 128 * 2 * 2.07e9 / 1e12
-        roofline = {
-            "kernel": "attention backward on CUDA cores (row_dot, key_grads, query_grads)",
-            "bound": "alu",
-            "achieved": round(achieved, 2),
-            "peak": round(alu_peak, 1),
-            "unit": "TFLOP/s",
-            "frac": round(achieved / alu_peak, 4),
-            "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2070 MHz (fp32 FMA)",
-            "frac_of_bf16_tensor_peak": round(achieved / peaks["bf16_tflops"], 4),
-            "algorithmic_flops_per_launch": flops,
-            "algorithmic_bytes_per_launch": bytes_alg,
-            "hbm_gbs_at_algorithmic_bytes": round(gbs, 1),
-            "traffic": None,
-        }
-    else:
-        roofline = {
-            "kernel": kernel,
-            "bound": "hbm" if hbm_bound else "tensor",
-            "achieved": round(gbs if hbm_bound else achieved, 2),
-            "peak": peaks["hbm_gbs"] if hbm_bound else peaks["bf16_tflops"],
-            "unit": "GB/s" if hbm_bound else "TFLOP/s",
-            "frac": round(gbs / peaks["hbm_gbs"] if hbm_bound else achieved / peaks["bf16_tflops"], 4),
-            "peak_source": (f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if hbm_bound else
-                            f"{peak_src} (burst, MEASURED_PEAKS.json bf16_tflops)"),
-            "frac_of_sustained": None if hbm_bound else round(achieved / peaks["bf16_tflops_sustained"], 4),
-            "frac_of_nominal_2250": None if hbm_bound else round(achieved / NOMINAL_BF16_TFLOPS, 4),
-            "algorithmic_flops_per_launch": flops,
-            "algorithmic_bytes_per_launch": bytes_alg,
-            "hbm_gbs_at_algorithmic_bytes": round(bytes_alg / (step_ms * 1e-3) / 1e9, 1),
-            "hbm_frac_at_algorithmic_bytes": round(bytes_alg / (step_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-            "traffic": profiled_traffic(w.name),
-        }
+        time.sleep(0.3)  # let the sampler start
+        head = measure(args, w, world, peaks, peak_src,
+                       0.0 if args.no_sustained else args.sustained_s, with_e2e=not args.no_e2e)
+        others = {}
+        for cw in companions:
+            rec = measure(args, cw, world, peaks, peak_src,
+                          0.0 if args.no_sustained else args.companion_sustained_s,
+                          with_e2e=not args.no_e2e)
+            rec.pop("_inp")
+            others[cw.name] = rec
+        time.sleep(0.25)  # the last samples of the last window
+    inp = head.pop("_inp")
+    for rec in [head, *others.values()]:
+        finalize_clocks(rec, sampler, args.steps)
 
     result = {
         "metric": metric_of(w)[0],
-        "value": round(tflops, 2) if w.kind != "pe" else round(gbs * world, 1),
+        "value": head["value"],
         "unit": metric_of(w)[1],
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(ms_step, 5),
+        "ms_per_step": head["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": w.dtype,
         "data": "synthetic: seeded Philox N(0,1) inputs rounded to the kernel dtype (no dataset)",
-        "config": {"workload": w.name, "description": w.description, "B": w.B, "h": w.h,
-                   "n_q": w.n_q, "n_k": w.n_k, "d": w.d_k,
-                   "mask": {0: "none", 1: "causal", 2: "key_padding", 3: "causal+key_padding"}[
-                       w.mask_kind],
-                   "timing": "CUDA-graph replay of one step" if not args.no_graph else "eager calls",
-                   "parallelism": f"replicas x{world} (independent (batch, head) work per GPU)",
-                   "l2": (f"inputs {bytes_in / 1e6:.0f} MB > 129 MB L2: streamed from HBM every step, no flush"
-                          if not flush_l2 else
-                          f"inputs {bytes_in / 1e6:.1f} MB fit in L2: a {FLUSH_BYTES >> 20} MB write "
-                          "flushes L2 before every timed step (outside its events); step times summed")},
-        "tokens_per_s": round(tokens_s, 1),
-        "pct_of_measured_bf16_peak": round(100 * tflops / world / peaks["bf16_tflops"], 2),
-        "pct_of_nominal_bf16_peak": round(100 * tflops / world / NOMINAL_BF16_TFLOPS, 2),
-        "roofline": roofline,
-        "gpu_launches": args.steps * launches_per_step,
-        "clocks": sampler.summary(),
+        "config": config_of(w, world),
+        "timing": {"steps": "CUDA-graph replay of one step" if not args.no_graph else "eager calls",
+                   "l2": head["l2"]},
+        "tokens_per_s": head["tokens_per_s"],
+        "step_ms": head["step_ms"],
+        "roofline": head["roofline"],
+        "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"],
     }
-    if w.is_mha or w.kind in ("encoder", "decoder"):
-        result["config"]["d_model"] = w.d_model
-    if w.kind in ("encoder", "decoder"):
-        result["config"]["d_ff"] = w.d_ff
-
-    if not args.no_e2e and w.kind != "pe":
-        result["e2e"] = e2e_leg(args, w, host, step, flops, world)
-        result["gpu_launches"] += result["e2e"].pop("launches") * launches_per_step
+    for key in ("pct_of_measured_bf16_peak", "pct_of_nominal_bf16_peak", "sustained", "e2e"):
+        if key in head:
+            result[key] = head[key]
+    if others:
+        result["configs"] = others
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, threads, desc = sample_rate(w, inp, args.cpu_budget_s)
         result["cpu_baseline"] = {"value": round(rate, 6), "unit": metric_of(w)[1], "cores": threads,
@@ -953,8 +1187,7 @@ def run_reference(args, rank, world):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic: seeded Philox N(0,1) inputs rounded to bf16 (no dataset)",
-        "config": {"workload": w.name, "description": w.description, "B": w.B, "h": w.h,
-                   "n_q": w.n_q, "n_k": w.n_k, "d": w.d_k},
+        "config": config_of(w, world),
         "cpu_baseline": {"value": round(value, 6), "unit": metric_of(w)[1], "cores": threads,
                          "kind": "oracle",
                          "sample": f"each step: {descs[0] if descs else ''} (median over steps)"},

@@ -3,6 +3,7 @@
 // for the contract of every entry point.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cmath>
@@ -104,6 +105,30 @@ bool cached_map(CUtensorMap* out, const MapKey& key, bool (*make)(CUtensorMap*, 
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// One NVTX range (domain "hattn", named after the entry point) around an entry
+// point's host work and launches, so a timeline shows which call enqueued which
+// kernels. Without a tool attached a range costs a few nanoseconds.
+class Range {
+public:
+    explicit Range(const char* name)
+    {
+        static const nvtxDomainHandle_t dom = nvtxDomainCreateA("hattn");
+        dom_ = dom;
+        nvtxEventAttributes_t a = {};
+        a.version = NVTX_VERSION;
+        a.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+        a.messageType = NVTX_MESSAGE_TYPE_ASCII;
+        a.message.ascii = name;
+        nvtxDomainRangePushEx(dom_, &a);
+    }
+    ~Range() { nvtxDomainRangePop(dom_); }
+    Range(const Range&) = delete;
+    Range& operator=(const Range&) = delete;
+
+private:
+    nvtxDomainHandle_t dom_;
+};
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? HATTN_OK : HATTN_ECUDA; }
 
@@ -228,6 +253,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, int dtype, 
              int n_q, int n_k, int d_k, int d_v, float scale, int mask_kind,
              const int32_t* key_lens, hattn_stream_t stream)
 {
+    const Range range("attn_fwd");
     int rc = validate_attn(q, k, v, out, dtype, B, h, n_q, n_k, d_k, d_v, scale, mask_kind,
                            key_lens);
     if (rc != HATTN_OK) return rc;
@@ -251,6 +277,7 @@ int mha_fwd(const void* x_q, const void* x_kv, const void* Wq, const void* Wk, c
             int B, int n_q, int n_k, int d_model, int h, int d_k, int d_v, int mask_kind,
             const int32_t* key_lens, void* workspace, size_t ws_bytes, hattn_stream_t stream)
 {
+    const Range range("mha_fwd");
     if (!x_q || !x_kv || !Wq || !Wk || !Wv || !Wo || !gamma || !beta || !y) return HATTN_EINVAL;
     if (dtype != HATTN_BF16) return dtype == HATTN_F32 ? HATTN_EUNSUPPORTED : HATTN_EINVAL;
     if (B <= 0 || n_q <= 0 || n_k <= 0 || d_model <= 0 || h <= 0 || d_k <= 0 || d_v <= 0)
@@ -355,7 +382,13 @@ int mha_fwd_noalloc(const void* x_q, const void* x_kv, const void* Wq, const voi
                     int d_k, int d_v, int mask_kind, const int32_t* key_lens,
                     hattn_stream_t stream)
 {
-    // Sizes first: an oversized request is rejected before any CUDA call.
+    const Range range("mha_fwd_noalloc");
+    // Missing or misaligned buffers and a wrong dtype are reported as such whatever
+    // the problem size; then an oversized request is rejected before any CUDA call.
+    const void* bufs[] = {x_q, x_kv, Wq, Wk, Wv, Wo, gamma, beta, y};
+    for (const void* p : bufs)
+        if (!p || !aligned16(p)) return HATTN_EINVAL;
+    if (dtype != HATTN_BF16) return dtype == HATTN_F32 ? HATTN_EUNSUPPORTED : HATTN_EINVAL;
     const size_t need = mha_workspace_bytes(dtype, B, n_q, n_k, d_model, h, d_k, d_v);
     if (need > HATTN_NOALLOC_SCRATCH_BYTES) return HATTN_ESCRATCH;
     if (need == 0) {
@@ -373,6 +406,7 @@ int attn_fwd_lse(const void* q, const void* k, const void* v, void* out, float* 
                  int B, int h, int n_q, int n_k, int d_k, int d_v, float scale, int mask_kind,
                  const int32_t* key_lens, hattn_stream_t stream)
 {
+    const Range range("attn_fwd_lse");
     if (!lse || !aligned16(lse)) return HATTN_EINVAL;
     int rc = validate_attn(q, k, v, out, dtype, B, h, n_q, n_k, d_k, d_v, scale, mask_kind,
                            key_lens);
@@ -396,6 +430,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* out, const
              int n_k, int d_k, int d_v, float scale, int mask_kind, const int32_t* key_lens,
              void* workspace, size_t ws_bytes, hattn_stream_t stream)
 {
+    const Range range("attn_bwd");
     if (!dout || !lse || !dq || !dk || !dv) return HATTN_EINVAL;
     const void* ptrs[] = {dout, lse, dq, dk, dv};
     for (const void* ptr : ptrs)
@@ -441,6 +476,7 @@ int attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, voi
                     int B, int h, int n_max, int d, float scale, const int32_t* kv_lens,
                     void* workspace, size_t ws_bytes, hattn_stream_t stream)
 {
+    const Range range("attn_decode_fwd");
     if (!q || !k_cache || !v_cache || !out || !kv_lens) return HATTN_EINVAL;
     if (dtype != HATTN_BF16) return dtype == HATTN_F32 ? HATTN_EUNSUPPORTED : HATTN_EINVAL;
     if (B <= 0 || h <= 0 || n_max <= 0 || d <= 0 || !std::isfinite(scale)) return HATTN_EINVAL;
@@ -461,6 +497,7 @@ int attn_decode_fwd(const void* q, const void* k_cache, const void* v_cache, voi
 int pos_encoding_fwd(const void* emb, void* out, int dtype, int B, int n, int d_model,
                      float emb_scale, int pos0, hattn_stream_t stream)
 {
+    const Range range("pos_encoding_fwd");
     if (!out || (dtype != HATTN_F32 && dtype != HATTN_BF16)) return HATTN_EINVAL;
     if (B <= 0 || n <= 0 || d_model <= 0 || (d_model & 1) || pos0 < 0) return HATTN_EINVAL;
     if ((long long)pos0 + n > (1LL << 24) || !std::isfinite(emb_scale)) return HATTN_EINVAL;
@@ -502,6 +539,7 @@ int ffn_fwd(const void* x, const void* W1, const float* b1, const void* W2, cons
             const float* gamma, const float* beta, float eps, void* y, int dtype, int M,
             int d_model, int d_ff, void* workspace, size_t ws_bytes, hattn_stream_t stream)
 {
+    const Range range("ffn_fwd");
     if (!x || !W1 || !W2 || !gamma || !beta || !y) return HATTN_EINVAL;
     if (dtype != HATTN_BF16) return dtype == HATTN_F32 ? HATTN_EUNSUPPORTED : HATTN_EINVAL;
     if (!ffn_shapes_ok(M, d_model, d_ff)) return HATTN_EINVAL;
@@ -564,6 +602,7 @@ int encoder_layer_fwd(const void* x, const hattn_mha_weights* attn, const hattn_
                       int d_ff, const int32_t* key_lens, void* workspace, size_t ws_bytes,
                       hattn_stream_t stream)
 {
+    const Range range("encoder_layer_fwd");
     if (!x || !attn || !ffn || !y) return HATTN_EINVAL;
     if (B <= 0 || n <= 0 || (long long)B * n > 0x7fffffffLL) return HATTN_EINVAL;
     const size_t need = encoder_layer_workspace_bytes(dtype, B, n, d_model, h, d_k, d_ff);
@@ -598,6 +637,7 @@ int decoder_layer_fwd(const void* x, const void* memory, const hattn_mha_weights
                       int d_k, int d_ff, const int32_t* src_lens, void* workspace,
                       size_t ws_bytes, hattn_stream_t stream)
 {
+    const Range range("decoder_layer_fwd");
     if (!x || !memory || !self_attn || !cross_attn || !ffn || !y) return HATTN_EINVAL;
     if (B <= 0 || n_tgt <= 0 || n_src <= 0 || (long long)B * n_tgt > 0x7fffffffLL)
         return HATTN_EINVAL;
@@ -680,6 +720,7 @@ extern "C" {
 
 int hattn_selftest_wait_timeout(hattn_stream_t stream)
 {
+    const hattn::Range range("hattn_selftest_wait_timeout");
     int* err = hattn::device_error_ptr();
     if (!err) return HATTN_ECUDA;
     hattn::wait_timeout_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err);

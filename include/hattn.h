@@ -141,9 +141,11 @@ int mha_fwd(const void* x_q, const void* x_kv, const void* Wq, const void* Wk, c
  *
  *   - The first call on a device looks up the buffer's device address (with
  *     that device current); make that first call before any stream capture.
- *   - Sizes whose mha_workspace_bytes() exceeds the buffer are rejected with
- *     HATTN_ESCRATCH before anything is enqueued (the B=16, n=512,
- *     d_model=512, h=8, d=64 sublayer needs exactly 32 MiB).
+ *   - Null or misaligned buffers and a dtype other than HATTN_BF16 are
+ *     reported first (HATTN_EINVAL / HATTN_EUNSUPPORTED, as mha_fwd reports
+ *     them); then sizes whose mha_workspace_bytes() exceeds the buffer are
+ *     rejected with HATTN_ESCRATCH before anything is enqueued (the B=16,
+ *     n=512, d_model=512, h=8, d=64 sublayer needs exactly 32 MiB).
  *   - Every call shares the one buffer and overwrites it completely before
  *     reading it (nothing in it has to start at zero); calls whose work overlaps
  *     on the GPU (different streams, or different host threads) race on it and

@@ -128,6 +128,18 @@ def test_noalloc_rejects_problems_beyond_its_static_scratch(lib):
     assert hattn.mha_fwd_noalloc_raw(**args) == hattn._binding.ESCRATCH
 
 
+def test_noalloc_reports_bad_buffers_before_the_size(lib):
+    # An oversized call with a missing or misaligned buffer, or a wrong dtype, is
+    # reported as that argument error, not as a scratch shortage.
+    args = dict(MHA)
+    del args["workspace"], args["ws_bytes"]
+    args.update(B=17)
+    assert hattn.mha_fwd_noalloc_raw(**dict(args, y=None)) == hattn._binding.EINVAL
+    assert hattn.mha_fwd_noalloc_raw(**dict(args, x_q=args["x_q"] + 8)) == hattn._binding.EINVAL
+    assert hattn.mha_fwd_noalloc_raw(**dict(args, dtype=0)) == hattn._binding.EUNSUPPORTED
+    assert hattn.mha_fwd_noalloc_raw(**dict(args, dtype=7)) == hattn._binding.EINVAL
+
+
 @pytest.mark.parametrize("kw,code", [
     (dict(out=None), hattn._binding.EINVAL),
     (dict(dtype=5), hattn._binding.EINVAL),

@@ -8,8 +8,7 @@ import pytest
 import head_attention_gb300 as hattn
 import oracle
 from synth import inputs as synth
-from tests.gpu_util import (assert_close, from_device, keylens_device, sample_rows, to_device,
-                            torch)
+from tests.gpu_util import assert_close, from_device, keylens_device, to_device, torch
 
 pytestmark = pytest.mark.gpu
 
@@ -43,14 +42,20 @@ def test_decode_matches_oracle(B, h, n_max, d, lens):
     assert_close(got, ref, "bf16", f"decode {B} {h} {n_max} {d}")
 
 
-def test_decode_named_workload_sampled():
+def test_decode_named_workload_full():
+    """The bench's decode workload at full size, every output against the oracle
+    over the first kv_lens[b] cached rows of each batch element."""
     w = synth.workload("decode_bf16")
     inp = synth.attn_inputs(w)
     got = _run(w, inp)
-    sel = sample_rows(w.B, 1, w.h, 128, seed=6)
-    ref = oracle.attn_rows(*(synth.widen(inp[n], "bf16") for n in ("q", "k", "v")), w.scale, sel,
-                           synth.MASK_KEY_PADDING, inp["key_lens"])
-    assert_close(got[sel[:, 0], sel[:, 1], sel[:, 2]], ref, "bf16", "decode_bf16")
+    assert hattn.check_device_error() == 0
+    ref = np.empty_like(got)
+    for b in range(w.B):
+        L = int(inp["key_lens"][b])
+        q = synth.widen(inp["q"][b:b + 1], "bf16")
+        k, v = (synth.widen(inp[n][b:b + 1, :L], "bf16") for n in ("k", "v"))
+        ref[b:b + 1] = oracle.attn(q, k, v, w.scale, synth.MASK_NONE, None)
+    assert_close(got, ref, "bf16", "decode_bf16")
 
 
 def test_decode_matches_attn_fwd_and_ignores_rows_past_length():

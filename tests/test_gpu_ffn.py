@@ -1,10 +1,13 @@
 """GPU parity of the feed-forward sublayer and of the encoder / decoder layers
 (through the C ABI) against the fp64 oracle.
 
-The layers are compositions of bf16-in / bf16-out sublayers, so the oracle
-side composes oracle.mha / oracle.ffn with each sublayer's output rounded to
-bf16, exactly as the API hands it to the next sublayer; everything inside a
-sublayer stays fp64 on the oracle side."""
+The layers are compositions of bf16-in / bf16-out sublayers. Each sublayer is
+checked at the single bf16 tolerance against the oracle run on the GPU's own
+input to that sublayer, and the layer entry points are checked to be bit for
+bit the composition of the sublayer entry points. The composed checks compare
+the layer output with the oracle's own composition (oracle.mha / oracle.ffn
+with each sublayer's output rounded to bf16, as the API hands it on), at the
+chained tolerance; everything inside a sublayer stays fp64 on the oracle side."""
 
 import numpy as np
 import pytest
@@ -110,34 +113,101 @@ def test_decoder_layer_matches_oracle():
     assert_close(from_device(y), ref, "bf16", "decoder layer", tol=chained_tol(3))
 
 
-def _sample_bt(B, n, count, seed):
-    rng = np.random.default_rng(seed)
-    edges = [(0, 0), (B - 1, n - 1), (0, 127), (0, 128), (B - 1, n // 2)]
-    rand = [(int(b), int(t)) for b, t in zip(rng.integers(0, B, count), rng.integers(0, n, count))]
-    return np.array(sorted(set(edges + rand)), dtype=np.int32)
+def _gpu_mha(xq_dev, xkv_dev, m_dev, eps, h, mask, kl_dev):
+    return hattn.mha_fwd(xq_dev, xkv_dev, m_dev["wq"], m_dev["wk"], m_dev["wv"], m_dev["wo"],
+                         m_dev["gamma"], m_dev["beta"], eps, h, mask_kind=mask, key_lens=kl_dev)
 
 
-def test_encoder_layer_full_size_sampled():
-    """The bench's encoder-layer workload at full size, checked on sampled rows (the
-    FFN is position-wise, so a row of y needs only that row of y1)."""
+def _gpu_ffn(x_dev, f_dev, eps):
+    return hattn.ffn_fwd(x_dev, f_dev["w1"], f_dev["b1"], f_dev["w2"], f_dev["b2"],
+                         f_dev["gamma"], f_dev["beta"], eps)
+
+
+ENCODER_CASES = [
+    synth.Workload("enc_case", "bf16", B=2, h=2, n_q=200, n_k=200, d_k=64, d_v=64,
+                   mask_kind=synth.MASK_KEY_PADDING, seed=51, key_len_range=(60, 200),
+                   d_model=128, d_ff=256, kind="encoder"),
+    synth.workload("encoder_layer_bf16"),
+]
+DECODER_CASES = [
+    synth.Workload("dec_case", "bf16", B=2, h=2, n_q=150, n_k=260, d_k=64, d_v=64,
+                   mask_kind=synth.MASK_KEY_PADDING, seed=52, key_len_range=(50, 260),
+                   d_model=128, d_ff=256, kind="decoder"),
+    synth.workload("decoder_layer_bf16"),
+]
+
+
+@pytest.mark.parametrize("w", ENCODER_CASES, ids=lambda w: w.name)
+def test_encoder_layer_each_sublayer_at_the_single_tolerance(w):
+    """Each sublayer of the encoder layer against the oracle run on the GPU's own
+    input to that sublayer, at the single bf16 tolerance (not the chained one):
+    y1 = MHA(x) against oracle.mha(x); y = FFN(y1) against oracle.ffn(y1 as the
+    GPU produced it); and the layer entry point's output is bit for bit the
+    composition of the two sublayer entry points."""
+    inp = synth.layer_inputs(w)
+    kl = inp["key_lens"]
+    mask = synth.MASK_KEY_PADDING if kl is not None else 0
+    x = to_device(inp["x"], "bf16")
+    m, f = _dev_mha(inp["self_attn"]), _dev_ffn(inp["ffn"])
+    kl_dev = keylens_device(kl)
+    y1 = _gpu_mha(x, x, m, inp["eps"], w.h, mask, kl_dev)
+    y = _gpu_ffn(y1, f, inp["eps"])
+    layer = hattn.encoder_layer_fwd(x, m, f, inp["eps"], w.h, key_lens=kl_dev)
+    torch().cuda.synchronize()
+    assert hattn.check_device_error() == 0
+    assert torch().equal(layer, y), "layer != FFN(MHA(x))"
+    x64 = _w(inp["x"])
+    y1_host = from_device(y1)
+    assert_close(y1_host, _oracle_mha(x64, x64, inp["self_attn"], inp["eps"], w.h, mask, kl),
+                 "bf16", f"{w.name}: MHA sublayer")
+    assert_close(from_device(y), _oracle_ffn(y1_host, inp["ffn"]), "bf16",
+                 f"{w.name}: FFN sublayer on the GPU's y1")
+
+
+@pytest.mark.parametrize("w", DECODER_CASES, ids=lambda w: w.name)
+def test_decoder_layer_each_sublayer_at_the_single_tolerance(w):
+    """The decoder layer's three sublayers, each against the oracle on the GPU's
+    own input at the single bf16 tolerance, and the layer entry point bit for bit
+    equal to their composition."""
+    inp = synth.layer_inputs(w)
+    kl = inp["key_lens"]
+    x, mem = to_device(inp["x"], "bf16"), to_device(inp["memory"], "bf16")
+    ms, mc, f = _dev_mha(inp["self_attn"]), _dev_mha(inp["cross_attn"]), _dev_ffn(inp["ffn"])
+    kl_dev = keylens_device(kl)
+    y1 = _gpu_mha(x, x, ms, inp["eps"], w.h, synth.MASK_CAUSAL, None)
+    y2 = _gpu_mha(y1, mem, mc, inp["eps"], w.h, synth.MASK_KEY_PADDING, kl_dev)
+    y = _gpu_ffn(y2, f, inp["eps"])
+    layer = hattn.decoder_layer_fwd(x, mem, ms, mc, f, inp["eps"], w.h, src_lens=kl_dev)
+    torch().cuda.synchronize()
+    assert hattn.check_device_error() == 0
+    assert torch().equal(layer, y), "layer != FFN(cross(self(x)))"
+    x64, mem64 = _w(inp["x"]), _w(inp["memory"])
+    y1_host, y2_host = from_device(y1), from_device(y2)
+    assert_close(y1_host, _oracle_mha(x64, x64, inp["self_attn"], inp["eps"], w.h,
+                                      synth.MASK_CAUSAL, None),
+                 "bf16", f"{w.name}: causal self-attention sublayer")
+    assert_close(y2_host, _oracle_mha(y1_host, mem64, inp["cross_attn"], inp["eps"], w.h,
+                                      synth.MASK_KEY_PADDING, kl),
+                 "bf16", f"{w.name}: cross-attention sublayer on the GPU's y1")
+    assert_close(from_device(y), _oracle_ffn(y2_host, inp["ffn"]), "bf16",
+                 f"{w.name}: FFN sublayer on the GPU's y2")
+
+
+def test_encoder_layer_full_size_composed():
+    """The bench's encoder-layer workload at full size, every element against the
+    oracle's composition of its sublayers (chained tolerance)."""
     w = synth.workload("encoder_layer_bf16")
     inp = synth.layer_inputs(w)
     y = hattn.encoder_layer_fwd(to_device(inp["x"], "bf16"), _dev_mha(inp["self_attn"]),
                                 _dev_ffn(inp["ffn"]), inp["eps"], w.h)
     torch().cuda.synchronize()
-    got = from_device(y)
-    sel = _sample_bt(w.B, w.n_q, 24, seed=8)
-    m = inp["self_attn"]
     x64 = _w(inp["x"])
-    y1 = oracle.mha_rows(x64, x64, _w(m["wq"]), _w(m["wk"]), _w(m["wv"]), _w(m["wo"]),
-                         m["gamma"].astype(np.float64), m["beta"].astype(np.float64), inp["eps"],
-                         w.h, sel)
+    y1 = _oracle_mha(x64, x64, inp["self_attn"], inp["eps"], w.h, 0, None)
     ref = _oracle_ffn(_rb(y1), inp["ffn"])
-    assert_close(got[sel[:, 0], sel[:, 1]], ref, "bf16", "encoder_layer_bf16 sampled",
-                 tol=chained_tol(2))
+    assert_close(from_device(y), ref, "bf16", "encoder_layer_bf16", tol=chained_tol(2))
 
 
-def test_decoder_layer_full_size_sampled():
+def test_decoder_layer_full_size_composed():
     w = synth.workload("decoder_layer_bf16")
     inp = synth.layer_inputs(w)
     kl = inp["key_lens"]
@@ -145,19 +215,9 @@ def test_decoder_layer_full_size_sampled():
                                 _dev_mha(inp["self_attn"]), _dev_mha(inp["cross_attn"]),
                                 _dev_ffn(inp["ffn"]), inp["eps"], w.h, src_lens=keylens_device(kl))
     torch().cuda.synchronize()
-    got = from_device(y)
-    sel = _sample_bt(w.B, w.n_q, 16, seed=9)
     x64 = _w(inp["x"])
-    ms, mc = inp["self_attn"], inp["cross_attn"]
-    g = lambda m: (m["gamma"].astype(np.float64), m["beta"].astype(np.float64))
-    y1 = _rb(oracle.mha_rows(x64, x64, _w(ms["wq"]), _w(ms["wk"]), _w(ms["wv"]), _w(ms["wo"]),
-                             *g(ms), inp["eps"], w.h, sel, synth.MASK_CAUSAL))
-    # Row t of the cross-attention output reads only row t of its query input.
-    xq = np.zeros((w.B, w.n_q, w.d_model))
-    xq[sel[:, 0], sel[:, 1]] = y1
-    y2 = _rb(oracle.mha_rows(xq, _w(inp["memory"]), _w(mc["wq"]), _w(mc["wk"]), _w(mc["wv"]),
-                             _w(mc["wo"]), *g(mc), inp["eps"], w.h, sel, synth.MASK_KEY_PADDING,
-                             kl))
+    y1 = _rb(_oracle_mha(x64, x64, inp["self_attn"], inp["eps"], w.h, synth.MASK_CAUSAL, None))
+    y2 = _rb(_oracle_mha(y1, _w(inp["memory"]), inp["cross_attn"], inp["eps"], w.h,
+                         synth.MASK_KEY_PADDING, kl))
     ref = _oracle_ffn(y2, inp["ffn"])
-    assert_close(got[sel[:, 0], sel[:, 1]], ref, "bf16", "decoder_layer_bf16 sampled",
-                 tol=chained_tol(3))
+    assert_close(from_device(y), ref, "bf16", "decoder_layer_bf16", tol=chained_tol(3))
