@@ -211,6 +211,15 @@ int validate_attn(const void* q, const void* k, const void* v, void* out, int dt
 
 int run_attn(const AttnArgs& a)
 {
+    if (attn_short_supported(a)) {
+        AttnMaps m;
+        if (!make_bnhd_map(&m.q, a.q, a.B, a.n_q, a.h, a.d_k, 128) ||
+            !make_bnhd_map(&m.k, a.k, a.B, a.n_k, a.h, a.d_k, 128) ||
+            !make_bnhd_map(&m.v, a.v, a.B, a.n_k, a.h, a.d_v, 128) ||
+            !make_bnhd_map(&m.o, a.out, a.B, a.n_q, a.h, a.d_v, 128))
+            return HATTN_ECUDA;
+        return from_cuda(launch_attn_short(a, m));
+    }
     if (attn_tc_supported(a)) {
         AttnMaps m;
         if (!make_bnhd_map(&m.q, a.q, a.B, a.n_q, a.h, a.d_k, 128) ||

@@ -583,15 +583,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-int sm_count()
-{
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-        return 152;
-    return n;
-}
-
 template <bool kNorm>
 cudaError_t launch(const CUtensorMap* a, const CUtensorMap* w, const CUtensorMap* c, const GemmParams& p,
                    int grid, int cluster, cudaStream_t stream)

@@ -32,14 +32,24 @@ struct AttnArgs {
 // 4-D [B][n][h][d] bf16 tensors, loaded as 128-row x 64-column boxes.
 struct AttnMaps {
     CUtensorMap q, k, v;
+    CUtensorMap o;  // the output, [B][n_q][h][d] (short-sequence kernel only)
 };
 
 // CUDA-core kernel: fp32 (d <= 128) and bf16 (d <= 256), any d_k / d_v.
 cudaError_t launch_attn_simt(const AttnArgs& a);
 
 // Tensor-core (tcgen05) kernel: bf16, d_k == d_v in {64, 128}.
+// Streaming multiprocessors of the current device (152 on GB300 if the query fails).
+int sm_count();
+
 bool attn_tc_supported(const AttnArgs& a);
 cudaError_t launch_attn_tc(const AttnArgs& a, const AttnMaps& maps);
+
+// Tensor-core kernel for short sequences (one CTA per head, no work loop): bf16,
+// n_q <= 128, d_k == d_v == 64 with n_k <= 256 or d_k == d_v == 128 with n_k <= 128.
+// Needs maps.o as well.
+bool attn_short_supported(const AttnArgs& a);
+cudaError_t launch_attn_short(const AttnArgs& a, const AttnMaps& maps);
 
 // Encodes a tensor map through the driver entry point. Returns false on failure.
 bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,

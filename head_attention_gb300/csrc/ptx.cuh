@@ -198,6 +198,18 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
                  : "memory");
 }
 
+// 4-D tiled tensor store shared -> global (a bulk async-group; elements past
+// the tensor's extent are not written). Make the shared-memory writes it reads
+// visible to the async proxy first (fence_proxy_async_smem).
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                             int c2, int c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];"
+        ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
 // Untiled bulk copy shared -> global of `bytes` (a multiple of 16; both
 // addresses 16-byte aligned), in the current bulk async-group. Thread writes of
 // the source must be made visible to the async proxy first (fence_proxy_async_smem).

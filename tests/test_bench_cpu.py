@@ -17,13 +17,13 @@ def test_io_bytes_attention_counts_each_tensor_once():
 
 
 def test_default_workload_exceeds_l2_and_small_ones_do_not():
-    # The default workload streams from HBM without a flush; the small configs
-    # fit in L2 and are timed with a flush that is itself larger than L2.
+    # The default workload streams from HBM as it is; the small configs fit in L2 and
+    # rotate over input copies whose total is more than twice the L2.
     big, _ = bench.io_bytes(synth.workload("long_causal_d128"), None)
     small, _ = bench.io_bytes(synth.workload("dec_causal_bf16"), None)
     assert big > bench.L2_BYTES
     assert small <= bench.L2_BYTES
-    assert bench.FLUSH_BYTES > bench.L2_BYTES
+    assert bench.ROTATE_BYTES > 2 * bench.L2_BYTES
 
 
 def test_profiled_traffic_needs_the_current_source_hash(tmp_path, monkeypatch):
@@ -34,6 +34,15 @@ def test_profiled_traffic_needs_the_current_source_hash(tmp_path, monkeypatch):
     (tmp_path / "attn_tc_wl.md").write_text("kernel_source_sha: 0000000000000000\ndram_bytes_per_launch: 1234\n")
     assert bench.profiled_traffic("wl") is None
     assert bench.profiled_traffic("missing") is None
+    # A summary that names its kernel's own sources is checked against those.
+    srcs = ("head_attention_gb300/csrc/attn_short.cu", "head_attention_gb300/csrc/ptx.cuh")
+    (tmp_path / "attn_short_wl2.md").write_text(
+        f"kernel_sources: {' '.join(srcs)}\nkernel_source_sha: {bench.kernel_source_sha(srcs)}\n"
+        "dram_bytes_per_launch: 99\n")
+    assert bench.profiled_traffic("wl2") == 99.0
+    (tmp_path / "attn_short_wl2.md").write_text(
+        f"kernel_sources: {' '.join(srcs)}\nkernel_source_sha: {sha}\ndram_bytes_per_launch: 99\n")
+    assert bench.profiled_traffic("wl2") is None
 
 
 def test_percentiles_interpolate_linearly():

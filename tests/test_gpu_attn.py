@@ -109,7 +109,7 @@ def test_bf16_tensor_core_shapes(d, mask_kind, shape):
                                            ("bf16", 128, 64), ("bf16", 8, 8)])
 @pytest.mark.parametrize("mask_kind", [0, 1, 2, 3])
 @pytest.mark.parametrize("shape", [(1, 1, 1, 1), (2, 3, 100, 100), (1, 2, 129, 129),
-                                   (3, 2, 77, 300)])
+                                   (3, 2, 77, 300), (2, 3, 64, 64), (3, 2, 33, 33), (2, 2, 50, 40)])
 def test_cuda_core_shapes(dtype, d_k, d_v, mask_kind, shape):
     B, h, n_q, n_k = shape
     if mask_kind & 1 and n_q != n_k:
@@ -129,6 +129,35 @@ def test_large_grids(shape, d):
     wq, wk, wv = (synth.widen(inp[n], w.dtype) for n in ("q", "k", "v"))
     ref = oracle.attn_rows(wq, wk, wv, w.scale, sel, 0, None)
     assert_close(got[sel[:, 0], sel[:, 1], sel[:, 2]], ref, "bf16", str(shape))
+
+
+# n_q <= 128 with n_k <= 256 at d = 64 (n_k <= 128 at d = 128) runs the short-sequence
+# kernel (one CTA per head): key lengths on both sides of the 128-key block edge, a single
+# query row, full tiles.
+@pytest.mark.parametrize("d,n_q,n_k", [(64, 128, 256), (64, 1, 129), (64, 100, 256),
+                                       (64, 77, 130), (128, 128, 128), (128, 1, 1),
+                                       (128, 100, 127)])
+def test_short_kernel_key_lengths_around_the_block_edge(d, n_q, n_k):
+    lens = sorted({1, min(127, n_k), min(128, n_k), min(129, n_k), max(1, n_k - 1), n_k})
+    w = _sweep_workload("bf16", len(lens), 3, n_q, n_k, d, d, synth.MASK_KEY_PADDING)
+    inp = synth.attn_inputs(w)
+    inp["key_lens"] = np.array(lens, dtype=np.int32)
+    assert_close(run_kernel(w, inp), oracle_full(w, inp), "bf16", f"short d={d} {n_q}x{n_k}")
+
+
+@pytest.mark.parametrize("d,n", [(64, 128), (64, 37), (128, 128), (128, 65)])
+def test_short_kernel_log_sum_exp(d, n):
+    # attn_fwd_lse on the short-sequence kernel: the row log-sum-exp of the scaled scores.
+    w = _sweep_workload("bf16", 2, 3, n, n, d, d, synth.MASK_CAUSAL)
+    inp = synth.attn_inputs(w)
+    q, k, v = (to_device(inp[x], "bf16") for x in ("q", "k", "v"))
+    out, lse = hattn.attn_fwd_lse(q, k, v, scale=w.scale, mask_kind=1)
+    torch().cuda.synchronize()
+    assert hattn.check_device_error() == 0
+    wq, wk, wv = (synth.widen(inp[x], "bf16") for x in ("q", "k", "v"))
+    assert_close(from_device(out), oracle.attn(wq, wk, wv, w.scale, 1, None), "bf16", "lse out")
+    rlse = oracle.attn_bwd(wq, wk, wv, np.zeros_like(wv), w.scale, 1, None)[3]
+    np.testing.assert_allclose(lse.cpu().numpy(), rlse, rtol=0, atol=1e-4 * (1 + np.abs(rlse).max()))
 
 
 # ---------------------------------------------------------------- invariants
@@ -153,12 +182,15 @@ def test_causal_future_perturbation_is_bitwise_invisible(dtype, d):
     assert not torch().equal(out1[:, t0 + 1:], out2[:, t0 + 1:])
 
 
-@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("bf16", 128), ("f32", 64)])
-def test_padding_contents_are_bitwise_invisible(dtype, d):
-    w = _sweep_workload(dtype, 4, 2, 100, 300, d, d, synth.MASK_KEY_PADDING)
+@pytest.mark.parametrize("dtype,d,n_k", [("bf16", 64, 300), ("bf16", 128, 300), ("f32", 64, 300),
+                                         ("bf16", 64, 200), ("f32", 64, 60)])
+def test_padding_contents_are_bitwise_invisible(dtype, d, n_k):
+    # n_k = 200 runs the short-sequence tensor-core kernel, n_k = 60 in fp32 the CUDA-core
+    # kernel with the head's keys resident in shared memory.
+    w = _sweep_workload(dtype, 4, 2, 100, n_k, d, d, synth.MASK_KEY_PADDING)
     inp = synth.attn_inputs(w)
     q, k, v = _device_inputs(w, inp)
-    kl_host = np.array([1, 129, 255, 300], dtype=np.int32)
+    kl_host = np.array([1, min(129, n_k - 3), min(255, n_k - 1), n_k], dtype=np.int32)
     kl = keylens_device(kl_host)
     out1 = hattn.attn_fwd(q, k, v, scale=w.scale, mask_kind=2, key_lens=kl)
     k2, v2 = k.clone(), v.clone()

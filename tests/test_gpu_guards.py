@@ -55,7 +55,10 @@ def _built():
 
 @pytest.mark.parametrize("dtype,B,h,n_q,n_k,d,mask", [
     ("bf16", 2, 3, 300, 300, 128, 3),   # tensor cores, causal + ragged key lengths
-    ("bf16", 3, 5, 100, 200, 64, 2),    # tensor cores, paired heads, key padding
+    ("bf16", 3, 5, 100, 200, 64, 2),    # short-sequence kernel, two key blocks, key padding
+    ("bf16", 2, 3, 77, 120, 128, 2),    # short-sequence kernel at d = 128, rows past n_q clipped
+    ("bf16", 2, 4, 128, 256, 64, 0),    # short-sequence kernel, full 128-row tile
+    ("bf16", 3, 5, 130, 200, 64, 2),    # persistent tensor-core kernel, key padding
     ("f32", 2, 2, 70, 70, 64, 1),       # CUDA cores, fp32
     ("bf16", 1, 3, 50, 50, 32, 0),      # CUDA cores, bf16 head size the tensor cores do not take
 ])
