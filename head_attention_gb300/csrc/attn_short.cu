@@ -12,9 +12,9 @@
 //
 // How. One CTA of four warps per (b, i) head, a straight-line chain without a
 // work loop or a ring: thread r owns query row r (TMEM lane r).
-//   1. Thread 0 issues every TMA load the head needs at once (Q, K_0 and V_0,
-//      then K_1 and V_1 once the key length says block 1 holds valid keys), so
-//      one DRAM round trip covers them all.
+//   1. Thread 0 issues every TMA load the head may need at once (Q and both key
+//      blocks' K and V, before the key length is read), so one DRAM round trip
+//      covers them all.
 //   2. Thread 0 issues S_j = Q K_j^T (tcgen05, M = 128, N = 128) for every
 //      block into TMEM columns [128 j, 128 j + 128).
 //   3. The whole row is visible at once, so the softmax takes two passes over
@@ -135,16 +135,31 @@ __global__ void __launch_bounds__(kShortThreads, (D == 64 && NKB == 1) ? 3 : 2)
     griddep_wait();
     griddep_launch_dependents();
 
-    // 1. Loads of block 0 go out before the key length is known.
+    // 1. Every load goes out before the key length is known: waiting for it would
+    // put a DRAM round trip in front of block 1's loads, and the bandwidth a block
+    // past the key length wastes is cheaper than that latency.
+    const bool two_blocks = NKB == 2 && p.n_k > 128;
     if (leader) {
         mbar_arrive_expect_tx(bar(C::kBarQK0), 2 * C::kTileBytes);
         for (int x = 0; x < C::kBoxes; ++x) {
             tma_load_4d(sbase + C::kOffQ + x * kBoxBytes, &tm_q, bar(C::kBarQK0), 64 * x, head, 0, b);
             tma_load_4d(sbase + C::kOffK + x * kBoxBytes, &tm_k, bar(C::kBarQK0), 64 * x, head, 0, b);
         }
+        if (two_blocks) {
+            mbar_arrive_expect_tx(bar(C::kBarK1), C::kTileBytes);
+            for (int x = 0; x < C::kBoxes; ++x)
+                tma_load_4d(sbase + C::kOffK + C::kTileBytes + x * kBoxBytes, &tm_k, bar(C::kBarK1),
+                            64 * x, head, 128, b);
+        }
         mbar_arrive_expect_tx(bar(C::kBarV0), C::kTileBytes);
         for (int x = 0; x < C::kBoxes; ++x)
             tma_load_4d(sbase + C::kOffV + x * kBoxBytes, &tm_v, bar(C::kBarV0), 64 * x, head, 0, b);
+        if (two_blocks) {
+            mbar_arrive_expect_tx(bar(C::kBarV1), C::kTileBytes);
+            for (int x = 0; x < C::kBoxes; ++x)
+                tma_load_4d(sbase + C::kOffV + C::kTileBytes + x * kBoxBytes, &tm_v, bar(C::kBarV1),
+                            64 * x, head, 128, b);
+        }
     }
     const bool causal = (p.mask_kind & HATTN_MASK_CAUSAL) != 0;
     const int kv_len = (p.mask_kind & HATTN_MASK_KEY_PADDING) ? p.key_lens[b] : p.n_k;
@@ -152,19 +167,9 @@ __global__ void __launch_bounds__(kShortThreads, (D == 64 && NKB == 1) ? 3 : 2)
     const int nblk = valid ? (NKB == 2 && kv_len > 128 ? 2 : 1) : 0;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
 
-    // 2. Block 1's loads (only when it holds valid keys), then every S MMA.
+    // 2. S_j for every block that holds valid keys.
     bool ctl_ok = true;
     if (leader) {
-        if (NKB == 2 && nblk == 2) {
-            mbar_arrive_expect_tx(bar(C::kBarK1), C::kTileBytes);
-            for (int x = 0; x < C::kBoxes; ++x)
-                tma_load_4d(sbase + C::kOffK + C::kTileBytes + x * kBoxBytes, &tm_k, bar(C::kBarK1),
-                            64 * x, head, 128, b);
-            mbar_arrive_expect_tx(bar(C::kBarV1), C::kTileBytes);
-            for (int x = 0; x < C::kBoxes; ++x)
-                tma_load_4d(sbase + C::kOffV + C::kTileBytes + x * kBoxBytes, &tm_v, bar(C::kBarV1),
-                            64 * x, head, 128, b);
-        }
         if (nblk > 0) {
             const uint64_t q_desc = sdesc_sw128(sbase + C::kOffQ, 16, 1024);
             for (int j = 0; j < nblk && ctl_ok; ++j) {
@@ -258,7 +263,7 @@ __global__ void __launch_bounds__(kShortThreads, (D == 64 && NKB == 1) ? 3 : 2)
         // tile is overwritten or the CTA exits; every MMA it issued has completed.
         mbar_wait(bar(C::kBarQK0), 0);
         mbar_wait(bar(C::kBarV0), 0);
-        if (NKB == 2 && nblk == 2) {
+        if (two_blocks) {
             mbar_wait(bar(C::kBarK1), 0);
             mbar_wait(bar(C::kBarV1), 0);
         }
@@ -307,7 +312,7 @@ __global__ void __launch_bounds__(kShortThreads, (D == 64 && NKB == 1) ? 3 : 2)
         for (int x = 0; x < C::kBoxes; ++x)
             tma_store_4d(&tm_o, sbase + C::kOffQ + x * kBoxBytes, 64 * x, head, 0, b);
         bulk_commit_group();
-        bulk_wait_group_all();
+        bulk_wait_group_read_all();  // the tile is read out before shared memory is released
     }
     __syncwarp();
     if (warp == 0) {
@@ -351,16 +356,16 @@ cudaError_t launch_short(const AttnArgs& a, const AttnMaps& m)
 
 // The short kernel runs every head from scratch; the persistent kernel overlaps one
 // head's loads with another's compute, which pays once each SM has many heads to
-// run. Measured on GB300 (back-to-back steps, inputs from HBM): one CTA per head was
-// 12-20 % faster at 256 and 1024 heads with one key block, even at 512 heads with
-// two, and 25 % slower at 8192 heads with two.
+// run. Measured on GB300 (back-to-back steps, inputs from HBM): with one key block
+// one CTA per head was 12-20 % faster at 256, 1024 and 2048 heads (13.5 per SM);
+// with two it was even at 512 heads and 19 % slower at 1024 (6.7 per SM).
 bool attn_short_supported(const AttnArgs& a)
 {
     if (!attn_tc_supported(a) || a.n_q > 128) return false;
     const bool one_block = a.n_k <= 128;
     if (!(one_block || (a.d_k == 64 && a.n_k <= 256))) return false;
     const long long heads = (long long)a.B * a.h;
-    return heads <= (long long)sm_count() * (one_block ? 8 : 4);
+    return heads <= (long long)sm_count() * (one_block ? 16 : 3);
 }
 
 cudaError_t launch_attn_short(const AttnArgs& a, const AttnMaps& maps)
