@@ -4,9 +4,7 @@
 //
 // Each CTA owns 8 query rows of one (batch, head); each warp owns 2 of them.
 // K/V stream through shared memory 32 keys at a time, staged with batched
-// 16-byte loads (every load of a tile is in flight before the first store);
-// when a head has at most 64 keys (d <= 64) they are staged once, in the same
-// batch of loads as Q, and stay resident. For
+// 16-byte loads (every load of a tile is in flight before the first store). For
 // a row, lane j scores key j of the tile (four independent partial dot
 // products), the row max and row sum are warp-shuffle reductions, and the
 // output columns are spread over the lanes (column c on lane c % 32). The
@@ -97,71 +95,10 @@ __device__ __forceinline__ void stage_rows(float* dst, int dst_stride, const T* 
     }
 }
 
-// Keys a CTA keeps resident when the whole key range is short (d_k, d_v <= 64).
-constexpr int kResidentKeys = 64;
-
-// Stages rows [row0, row0 + kRows) of Q and rows [0, keys) of K and V into fp32
-// shared memory (rows past n_q are zero) in one batch: every 16-byte load of the
-// three is in flight before the first store, so the whole head costs one DRAM
-// round trip. V rows [keys, keys rounded up to a tile of 32) are zero: their
-// weights are 0 and 0 * V must stay 0 (K rows there are masked by selection).
-// d_k, d_v <= 64 and keys <= kResidentKeys.
-template <typename T>
-__device__ __forceinline__ void stage_resident(float* q_s, float* k_s, float* v_s, int dkp,
-                                               const T* q_bh, const T* k_bh, const T* v_bh,
-                                               size_t qk_stride, size_t v_stride, int row0,
-                                               int n_q, int keys, int d_k, int d_v)
-{
-    constexpr int V = 16 / sizeof(T);
-    constexpr int kMaxLoads = (kRows * (64 / V) + 2 * kResidentKeys * (64 / V) + kThreads - 1) / kThreads;
-    const int pq = d_k / V, pv = d_v / V;
-    const int v_rows = (keys + kKeys - 1) / kKeys * kKeys;
-    const int nq = kRows * pq, nk = keys * pq, total = nq + nk + v_rows * pv;
-    uint4 buf[kMaxLoads];
-#pragma unroll
-    for (int u = 0; u < kMaxLoads; ++u) {
-        const int idx = threadIdx.x + u * kThreads;
-        buf[u] = make_uint4(0u, 0u, 0u, 0u);
-        if (idx < nq) {
-            const int r = idx / pq;
-            if (row0 + r < n_q)
-                buf[u] = *reinterpret_cast<const uint4*>(q_bh + (size_t)(row0 + r) * qk_stride + (idx % pq) * V);
-        } else if (idx < nq + nk) {
-            const int i = idx - nq;
-            buf[u] = *reinterpret_cast<const uint4*>(k_bh + (size_t)(i / pq) * qk_stride + (i % pq) * V);
-        } else if (idx < total) {
-            const int i = idx - nq - nk;
-            if (i / pv < keys)
-                buf[u] = *reinterpret_cast<const uint4*>(v_bh + (size_t)(i / pv) * v_stride + (i % pv) * V);
-        }
-    }
-#pragma unroll
-    for (int u = 0; u < kMaxLoads; ++u) {
-        const int idx = threadIdx.x + u * kThreads;
-        if (idx >= total) continue;
-        float w[V];
-        widen4(buf[u], static_cast<const T*>(nullptr), w);
-        float* o;
-        if (idx < nq) {
-            o = q_s + (idx / pq) * dkp + (idx % pq) * V;
-        } else if (idx < nq + nk) {
-            const int i = idx - nq;
-            o = k_s + (i / pq) * dkp + (i % pq) * V;
-        } else {
-            const int i = idx - nq - nk;
-            o = v_s + (i / pv) * d_v + (i % pv) * V;
-        }
-#pragma unroll
-        for (int e = 0; e < V; ++e) o[e] = w[e];
-    }
-}
-
 // kCols = output columns per lane (d_v <= 32 * kCols); kMaxRowD bounds d_k and d_v
 // (a tighter bound unrolls less staging code: the small fp32 problems are bound
-// by latency, instruction fetch included). kResident: the head's keys (at most
-// kResidentKeys, d_k, d_v <= 64) are staged once, together with Q, and the key
-// tiles are then read from shared memory without further loads or barriers.
-template <typename T, int kCols, int kMaxRowD, bool kResident>
+// by latency, instruction fetch included).
+template <typename T, int kCols, int kMaxRowD>
 __global__ void __launch_bounds__(kThreads)
     attn_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                      T* __restrict__ out, int n_q, int n_k, int h, int d_k, int d_v, float scale,
@@ -170,10 +107,9 @@ __global__ void __launch_bounds__(kThreads)
 {
     extern __shared__ float smem[];
     const int dkp = d_k + 1;  // padded stride: lane j reads row j without bank conflicts
-    constexpr int kTileRows = kResident ? kResidentKeys : kKeys;
-    float* q_s = smem;                      // [kRows][dkp]
-    float* k_s = q_s + kRows * dkp;         // [kTileRows][dkp]
-    float* v_s = k_s + kTileRows * dkp;     // [kTileRows][d_v]
+    float* q_s = smem;                    // [kRows][dkp]
+    float* k_s = q_s + kRows * dkp;       // [kKeys][dkp]
+    float* v_s = k_s + kKeys * dkp;       // [kKeys][d_v]
 
     const int row0 = blockIdx.x * kRows;
     const int head = blockIdx.y;
@@ -205,13 +141,7 @@ __global__ void __launch_bounds__(kThreads)
     int key_end = kv_len;
     if (causal) key_end = min(key_end, row0 + kRows);
 
-    if constexpr (kResident) {
-        stage_resident<T>(q_s, k_s, v_s, dkp, q_bh, k_bh, v_bh, qk_row_stride, v_row_stride, row0,
-                          n_q, key_end, d_k, d_v);
-        __syncthreads();
-    } else {
-        stage_rows<T, kMaxRowD>(q_s, dkp, q_bh, qk_row_stride, row0, kRows, n_q, d_k);
-    }
+    stage_rows<T, kMaxRowD>(q_s, dkp, q_bh, qk_row_stride, row0, kRows, n_q, d_k);
 
     float m[kRowsPerWarp], l[kRowsPerWarp], acc[kRowsPerWarp][kCols];
 #pragma unroll
@@ -223,19 +153,10 @@ __global__ void __launch_bounds__(kThreads)
     }
 
     for (int kt = 0; kt < key_end; kt += kKeys) {
-        // Resident keys: tile kt sits at row kt of k_s / v_s (rows past key_end are
-        // never visible, so their contents do not matter).
-        const float* kt_s = k_s;
-        const float* vt_s = v_s;
-        if constexpr (kResident) {
-            kt_s += kt * dkp;
-            vt_s += kt * d_v;
-        } else {
-            __syncthreads();  // q_s is staged and the previous tile is no longer read
-            stage_rows<T, kMaxRowD>(k_s, dkp, k_bh, qk_row_stride, kt, kKeys, n_k, d_k);
-            stage_rows<T, kMaxRowD>(v_s, d_v, v_bh, v_row_stride, kt, kKeys, n_k, d_v);
-            __syncthreads();
-        }
+        __syncthreads();  // q_s is staged and the previous tile is no longer read
+        stage_rows<T, kMaxRowD>(k_s, dkp, k_bh, qk_row_stride, kt, kKeys, n_k, d_k);
+        stage_rows<T, kMaxRowD>(v_s, d_v, v_bh, v_row_stride, kt, kKeys, n_k, d_v);
+        __syncthreads();
 
 #pragma unroll
         for (int rr = 0; rr < kRowsPerWarp; ++rr) {
@@ -243,7 +164,7 @@ __global__ void __launch_bounds__(kThreads)
             const int t = row0 + r;
             const int j = kt + lane;
             const float* qr = q_s + r * dkp;
-            const float* kr = kt_s + lane * dkp;
+            const float* kr = k_s + lane * dkp;
             float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
             int c = 0;
             for (; c + 4 <= d_k; c += 4) {
@@ -269,7 +190,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
                 for (int i = 0; i < kCols; ++i) {
                     const int cc = lane + 32 * i;
-                    if (cc < d_v) acc[rr][i] = fmaf(pj, vt_s[jj * d_v + cc], acc[rr][i]);
+                    if (cc < d_v) acc[rr][i] = fmaf(pj, v_s[jj * d_v + cc], acc[rr][i]);
                 }
             }
             m[rr] = m_new;
@@ -290,17 +211,16 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-template <typename T, int kCols, int kMaxRowD = kMaxD, bool kResident = false>
+template <typename T, int kCols, int kMaxRowD = kMaxD>
 cudaError_t launch_typed(const AttnArgs& a)
 {
-    const size_t tile_rows = kResident ? kResidentKeys : kKeys;
-    const size_t smem = sizeof(float) * ((size_t)kRows * (a.d_k + 1) + tile_rows * (a.d_k + 1) +
-                                         tile_rows * a.d_v);
-    cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel<T, kCols, kMaxRowD, kResident>,
+    const size_t smem = sizeof(float) * ((size_t)kRows * (a.d_k + 1) + (size_t)kKeys * (a.d_k + 1) +
+                                         (size_t)kKeys * a.d_v);
+    cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel<T, kCols, kMaxRowD>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((a.n_q + kRows - 1) / kRows, a.h, a.B);
-    attn_simt_kernel<T, kCols, kMaxRowD, kResident><<<grid, kThreads, smem, a.stream>>>(
+    attn_simt_kernel<T, kCols, kMaxRowD><<<grid, kThreads, smem, a.stream>>>(
         static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v),
         static_cast<T*>(a.out), a.n_q, a.n_k, a.h, a.d_k, a.d_v, a.scale, a.mask_kind,
         a.key_lens, a.err_word, a.lse);
@@ -310,7 +230,6 @@ cudaError_t launch_typed(const AttnArgs& a)
 template <typename T>
 cudaError_t launch_cols(const AttnArgs& a)
 {
-    if (a.d_v <= 64 && a.d_k <= 64 && a.n_k <= kResidentKeys) return launch_typed<T, 2, 64, true>(a);
     if (a.d_v <= 64 && a.d_k <= 64) return launch_typed<T, 2, 64>(a);
     if (a.d_v <= 64) return launch_typed<T, 2>(a);
     if (a.d_v <= 128) return launch_typed<T, 4>(a);
