@@ -117,28 +117,16 @@ __global__ void __launch_bounds__(kShortThreads, (D == 64 && NKB == 1) ? 3 : 2)
         mbar_init(bar(C::kBarO), 1);
         mbar_init(bar(C::kBarDrain), 1);
         fence_barrier_init();
-        prefetch_tmap(&tm_q);
-        prefetch_tmap(&tm_k);
-        prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_o);
     }
-    __syncwarp();
-    if (warp == 0) {
-        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    // The set-up above overlaps the previous kernel's tail; its outputs are read below.
-    griddep_wait();
-    griddep_launch_dependents();
-
-    // 1. Every load goes out before the key length is known: waiting for it would
-    // put a DRAM round trip in front of block 1's loads, and the bandwidth a block
-    // past the key length wastes is cheaper than that latency.
+    // 1. Every load goes out first, before the TMEM allocation and the CTA-wide
+    // barrier (only this thread uses the barriers it just initialised), and before
+    // the key length is known: waiting for it would put a DRAM round trip in front
+    // of block 1's loads, and the bandwidth a block past the key length wastes is
+    // cheaper than that latency. The inputs may come from the previous kernel
+    // (programmatic dependent launch), so the grid dependency is waited for first.
     const bool two_blocks = NKB == 2 && p.n_k > 128;
+    griddep_wait();
     if (leader) {
         mbar_arrive_expect_tx(bar(C::kBarQK0), 2 * C::kTileBytes);
         for (int x = 0; x < C::kBoxes; ++x) {
@@ -161,6 +149,16 @@ __global__ void __launch_bounds__(kShortThreads, (D == 64 && NKB == 1) ? 3 : 2)
                             64 * x, head, 128, b);
         }
     }
+    __syncwarp();
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    griddep_launch_dependents();
     const bool causal = (p.mask_kind & HATTN_MASK_CAUSAL) != 0;
     const int kv_len = (p.mask_kind & HATTN_MASK_KEY_PADDING) ? p.key_lens[b] : p.n_k;
     const bool valid = kv_len >= 1 && kv_len <= p.n_k;

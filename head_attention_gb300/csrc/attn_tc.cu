@@ -91,12 +91,7 @@ static_assert(256 * kRegsSoftmax + 128 * kRegsControl <= kThreads * 168, "regist
 
 // Named barriers that make the two softmax warpgroups take turns on the
 // exponentials (barrier 0 is __syncthreads): tile 0 waits on kTurn0, tile 1 on kTurn1.
-// Measured on the long causal problems: at D = 128 the turns are worth 16 %; at
-// D = 64 (P in columns of its own, MMAs half as long) running both tiles'
-// exponentials freely is 1 % faster.
 constexpr uint32_t kTurn0 = 1, kTurn1 = 2;
-template <int D>
-constexpr bool kPingPong = (D == 128);
 
 constexpr int kRowsPerCta = 256;
 constexpr float kRescaleLog2 = 8.0f;
@@ -173,6 +168,15 @@ struct SchedSnake {};
 struct SchedPaired {};
 template <class Sched>
 constexpr bool kPaired = std::is_same<Sched, SchedPaired>::value;
+
+// Whether the two tiles' softmax warpgroups take turns on the exponentials, so
+// that one tile's exponentials overlap the other tile's MMAs. Measured on GB300:
+// at D = 128 the turns are worth 16 % on the long causal workload. At D = 64 (P in
+// columns of its own, MMAs half as long) they cost 5.5 % on the long causal
+// workload (table schedule) and gain 2 % on the MHA sublayer (n = 512, snake
+// order) and on cross-attention (paired heads).
+template <int D, class Sched>
+constexpr bool kPingPong = D == 128 || !std::is_same<Sched, SchedTable>::value;
 
 // Per-CTA state shared by the role functions; the unit fields are rewritten
 // by unit_setup for every unit.
@@ -643,11 +647,13 @@ __device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, 
         // of times): tile 0 waits for its turn, works, hands the turn over; tile 1
         // hands tile 0 the first turn, then waits, works, and hands it back
         // (except after the last round).
-        if (kPingPong<D> && t == 1 && R > 0) named_arrive(kTurn0, 256);
+        if (kPingPong<D, Sched> && t == 1 && R > 0) named_arrive(kTurn0, 256);
         for (int j = 0; j < R; ++j) {
             ok = __all_sync(0xffffffffu, ok && !c.aborted());
             const bool work = ok && j < nb;
             uint32_t sr[128];  // raw scores q.k of this row for keys kbase .. kbase + 127
+            const int kbase = j * 128;
+            const bool need_mask = (kbase + 128 > kv_len) || (c.causal && kbase + 127 > my_row0);
             if (work) {
                 const bool got = mbar_wait(c.bar(C::kBarS + t), sc & 1);
                 ++sc;
@@ -664,8 +670,6 @@ __device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, 
                         if (lane == 0) mbar_arrive(c.bar(C::kBarSFree + t));
                     }
                 }
-                const int kbase = j * 128;
-                const bool need_mask = (kbase + 128 > kv_len) || (c.causal && kbase + 127 > my_row0);
                 if (need_mask) {
                     // Key kbase + i is visible iff i < lim (inside the key length and,
                     // when causal, not after this row): one compare per score.
@@ -677,7 +681,7 @@ __device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, 
                 // The first block sets the running max before its exponentials.
                 if (j == 0) m_used = row_max(sr) * p.scale_log2;
             }
-            if (kPingPong<D>) named_sync(my_turn, 256);
+            if (kPingPong<D, Sched>) named_sync(my_turn, 256);
             if constexpr (C::kSepP) {
                 // PV(j-1) must have read P before it is overwritten (and O must be
                 // complete before a rescale).
@@ -714,7 +718,7 @@ __device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, 
                     acc[0] = acc[1] = acc[2] = acc[3] = 0;
                     exp_block<false>(sr, c2, f32x2(-m_used, -m_used), acc, lane_base + cP);
                 }
-                if (kPingPong<D> && (t == 0 || j + 1 < R)) named_arrive(other_turn, 256);
+                if (kPingPong<D, Sched> && (t == 0 || j + 1 < R)) named_arrive(other_turn, 256);
                 float a0, a1;
                 f32x2_split(add_f32x2(add_f32x2(acc[0], acc[1]), add_f32x2(acc[2], acc[3])), a0, a1);
                 l += a0 + a1;
@@ -725,7 +729,7 @@ __device__ void softmax_tile(Cta c, const TcParams& p, const Sched& sch, int t, 
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(c.bar(C::kBarP + t));
-            } else if (kPingPong<D> && (t == 0 || j + 1 < R)) {
+            } else if (kPingPong<D, Sched> && (t == 0 || j + 1 < R)) {
                 named_arrive(other_turn, 256);
             }
         }
