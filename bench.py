@@ -296,13 +296,17 @@ def _rows_flops(w, rows, kv_len):
     return float(4 * w.d_k * kv_len * len(rows))
 
 
-def oracle_sample_rate(w, inp, budget_s: float, sample_index: int = 0):
+def oracle_sample_rate(w, inp, budget_s: float, sample_index: int = 0, threads: int = 0,
+                       gpu_head=None, errs=None):
     """Times the oracle on whole (batch, head) units of the workload, one after
     another from unit `sample_index` on, until about budget_s seconds of work;
     returns (TFLOP/s, threads, description) counting the exact FLOPs of the
-    visible (query, key) pairs the oracle computed."""
+    visible (query, key) pairs the oracle computed. threads = 0: every host core.
+    With gpu_head(b, i) (the GPU's output of that unit, fp64 [n_q, d_v]) and a dict
+    errs, the largest and the summed absolute difference of the oracle's outputs
+    from the GPU's are accumulated there (after the timing of each unit)."""
     import oracle
-    threads = os.cpu_count() or 1
+    threads = threads or os.cpu_count() or 1
     n_units = w.B * w.h
     done, flops, elapsed = [], 0.0, 0.0
     while elapsed < budget_s and len(done) < n_units:
@@ -312,10 +316,16 @@ def oracle_sample_rate(w, inp, budget_s: float, sample_index: int = 0):
         kv_len = int(inp["key_lens"][b]) if inp.get("key_lens") is not None else w.n_k
         kl = None if inp.get("key_lens") is None else inp["key_lens"][b:b + 1]
         t0 = time.perf_counter()
-        oracle.attn(q, k, v, w.scale, w.mask_kind, kl, nthreads=threads)
+        ref = oracle.attn(q, k, v, w.scale, w.mask_kind, kl, nthreads=threads)
         elapsed += time.perf_counter() - t0
         flops += _rows_flops(w, range(w.n_q), kv_len)
         done.append((b, i))
+        if gpu_head is not None and errs is not None:
+            import numpy as np
+            d = np.abs(gpu_head(b, i) - ref[0, :, 0, :])
+            errs["max"] = max(errs.get("max", 0.0), float(d.max()))
+            errs["sum"] = errs.get("sum", 0.0) + float(d.sum())
+            errs["n"] = errs.get("n", 0) + d.size
     desc = (f"{len(done)} of {n_units} (batch, head) units, all {w.n_q} query rows each; "
             f"{flops / 1e9:.2f} GFLOP of visible (query, key) pairs in {elapsed:.2f} s")
     return flops / elapsed / 1e12, threads, desc
@@ -971,6 +981,12 @@ def measure(args, w, world, peaks, peak_src, sustained_s, with_e2e=True):
         raise RuntimeError(f"{w.name}: device error during the timed region")
     ms_step = reduce_max(ms_local, world) / args.steps
     step_ms_local = ms_local / args.steps
+    warm_ms = None
+    if copies > 1:
+        # The same steps on one copy of the inputs, which then stay in L2: the hot-L2
+        # time next to the cold one.
+        warm_total, _ = time_steps([graphs[0].replay] if graphs else fns[:1], stream, args.steps)
+        warm_ms = warm_total / args.steps
     hbm_bound_kind = w.kind in ("decode", "pe")
     alg_flops = visible_pair_flops(w, inp)
     p10, p50, p90 = percentiles(per_step)
@@ -989,6 +1005,7 @@ def measure(args, w, world, peaks, peak_src, sustained_s, with_e2e=True):
         "dtype": w.dtype,
         "l2": l2_note,
         "input_copies": copies,
+        "warm_l2_ms_per_step": None if warm_ms is None else round(warm_ms, 5),
         "roofline": roofline_of(w, kernel_name(w), flops, alg_flops, bytes_alg, step_ms_local,
                                 peaks, peak_src),
         "_clock_window": window,
@@ -1010,6 +1027,7 @@ def measure(args, w, world, peaks, peak_src, sustained_s, with_e2e=True):
         rec["e2e"] = e2e_leg(args, w, host, step, flops, world)
         rec["gpu_launches"] += rec["e2e"].pop("launches") * launches_per_step
     rec["_inp"] = inp
+    rec["_out"] = host["output"]
     return rec
 
 
@@ -1035,6 +1053,11 @@ def finalize_clocks(rec, sampler, steps):
                 f"of device time) held {timed.get('samples', 0)} samples"),
         timed_region_samples=timed.get("samples", 0),
         timed_region_reasons=timed.get("reasons", []))
+
+
+def torch_int16():
+    import torch
+    return torch.int16
 
 
 def config_of(w, world):
@@ -1079,9 +1102,11 @@ def run_gpu(args, rank, world, local):
                           0.0 if args.no_sustained else args.companion_sustained_s,
                           with_e2e=not args.no_e2e)
             rec.pop("_inp")
+            rec.pop("_out")
             others[cw.name] = rec
         time.sleep(0.25)  # the last samples of the last window
     inp = head.pop("_inp")
+    out = head.pop("_out")
     for rec in [head, *others.values()]:
         finalize_clocks(rec, sampler, args.steps)
 
@@ -1114,9 +1139,35 @@ def run_gpu(args, rank, world, local):
     if others:
         result["configs"] = others
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, threads, desc = sample_rate(w, inp, args.cpu_budget_s)
+        if w.kind == "attn":
+            # The sampled units' oracle outputs are also compared with the GPU's output of
+            # the timed workload (the parity of the bench's own run, on those units).
+            import numpy as np
+            from synth import inputs as synth
+
+            def gpu_head(b, i):
+                t = out[b, :, i, :].contiguous().cpu()
+                if w.dtype == "f32":
+                    return t.numpy().astype(np.float64)
+                return synth.bf16_bits_to_f64(t.view(torch_int16()).numpy().view(np.uint16))
+            errs = {}
+            rate, threads, desc = oracle_sample_rate(w, inp, args.cpu_budget_s, gpu_head=gpu_head,
+                                                     errs=errs)
+            rate1, _, desc1 = oracle_sample_rate(w, inp, args.cpu_budget_s / 5, sample_index=7,
+                                                 threads=1)
+        else:
+            errs = {}
+            rate, threads, desc = sample_rate(w, inp, args.cpu_budget_s)
+            rate1 = desc1 = None
         result["cpu_baseline"] = {"value": round(rate, 6), "unit": metric_of(w)[1], "cores": threads,
                                   "kind": "oracle", "sample": desc}
+        if rate1 is not None:
+            result["cpu_baseline"]["single_thread"] = {"value": round(rate1, 6), "sample": desc1}
+        if errs.get("n"):
+            result["cpu_baseline"]["gpu_vs_oracle"] = {
+                "max_abs_err": errs["max"], "mean_abs_err": errs["sum"] / errs["n"],
+                "elements": errs["n"],
+                "tolerance": {"max": 1e-5} if w.dtype == "f32" else {"max": 2e-2, "mean": 2e-3}}
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

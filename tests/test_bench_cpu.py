@@ -121,3 +121,25 @@ def test_both_arms_name_the_same_config():
     w = synth.workload("long_causal_d128")
     assert bench.config_of(w, 1) == bench.config_of(w, 1)
     assert set(bench.config_of(w, 1)) >= {"workload", "B", "h", "n_q", "n_k", "d", "mask"}
+
+
+def test_cpu_baseline_compares_the_sampled_units_with_the_gpu_output():
+    # A stand-in for the GPU output that differs from the oracle by exactly 0.25 in one
+    # element of every unit: the accumulated max is 0.25 and the mean is 0.25 / elements.
+    import numpy as np
+    import oracle
+    w = synth.Workload("tiny", "bf16", B=2, h=2, n_q=16, n_k=16, d_k=8, d_v=8, mask_kind=1, seed=3)
+    inp = synth.attn_inputs(w)
+
+    def gpu_head(b, i):
+        q, k, v = bench._head_arrays(inp, w, b, i)
+        ref = oracle.attn(q, k, v, w.scale, w.mask_kind, None)[0, :, 0, :].copy()
+        ref[3, 2] += 0.25
+        return ref
+
+    errs = {}
+    rate, threads, desc = bench.oracle_sample_rate(w, inp, 10.0, gpu_head=gpu_head, errs=errs)
+    assert errs["n"] == w.B * w.h * w.n_q * w.d_v
+    assert abs(errs["max"] - 0.25) < 1e-12
+    assert abs(errs["sum"] - 0.25 * w.B * w.h) < 1e-9
+    assert rate > 0 and threads >= 1
