@@ -1133,7 +1133,8 @@ def run_gpu(args, rank, world, local):
         "gpu_launches": head["gpu_launches"],
         "clocks": head["clocks"],
     }
-    for key in ("pct_of_measured_bf16_peak", "pct_of_nominal_bf16_peak", "sustained", "e2e"):
+    for key in ("pct_of_measured_bf16_peak", "pct_of_nominal_bf16_peak", "input_copies",
+                "warm_l2_ms_per_step", "sustained", "e2e"):
         if key in head:
             result[key] = head[key]
     if others:
