@@ -323,7 +323,7 @@ int mha_fwd(const void* x_q, const void* x_kv, const void* Wq, const void* Wk, c
     for (int i = 0; i < 3; ++i) {
         if (!make_2d_map(&pr[i].a, xs[i], Ms[i], d_model, 128) ||
             !make_2d_map(&pr[i].w, ws3[i], d_model, Ns[i], 64) ||
-            !make_2d_map(&pr[i].cmap, outs[i], Ms[i], Ns[i], 128))
+            !make_2d_map(&pr[i].cmap, outs[i], Ms[i], Ns[i], 32))
             return HATTN_ECUDA;
         pr[i].c = outs[i];
         pr[i].M = Ms[i];
@@ -570,7 +570,7 @@ int ffn_fwd(const void* x, const void* W1, const float* b1, const void* W2, cons
     // H = max(0, x W1 + b1)
     ProjProblem pr;
     if (!make_2d_map(&pr.a, x, M, d_model, 128) || !make_2d_map(&pr.w, W1, d_model, d_ff, 64) ||
-        !make_2d_map(&pr.cmap, H, M, d_ff, 128))
+        !make_2d_map(&pr.cmap, H, M, d_ff, 32))
         return HATTN_ECUDA;
     pr.c = H;
     pr.M = M;

@@ -17,8 +17,9 @@
 //
 // Tiles are 128 rows x up to 256 columns. Warp 0 streams A (128 x 64 boxes,
 // K-major) and W ([K][N] row-major, i.e. N-major, 64 x 64 boxes) through a
-// 3-stage shared-memory ring by TMA (both epilogues stage their bf16 output
-// tile in shared memory and write it with TMA stores); warp 1 (one thread) issues the tcgen05
+// shared-memory ring by TMA (four stages for the store epilogue, three for the
+// norm one; both epilogues stage their bf16 output in shared memory and write
+// it with TMA stores); warp 1 (one thread) issues the tcgen05
 // MMAs into one of two TMEM accumulators (256 columns each), so the epilogue
 // of one tile overlaps the MMAs of the next; warps 2-9 run the epilogue, thread
 // r of a warp quadrant owning output row r (TMEM lane r) and the two warps of a
@@ -49,17 +50,21 @@ constexpr int kBM = 128, kBN = 256, kBK = 64;
 constexpr uint32_t kABoxBytes = kBM * kBK * 2;  // A box: 128 rows x 64 columns
 constexpr uint32_t kWBoxBytes = 64 * kBK * 2;   // W box: 64 K-rows x 64 N-columns
 constexpr uint32_t kStageBytes = kABoxBytes + (kBN / 64) * kWBoxBytes;
+constexpr uint32_t kWarpBoxBytes = 32 * 64 * 2;  // store epilogue: 32 rows x 64 columns
 // Epilogue warps 2-9: warp w takes TMEM lane quadrant w % 4 (one output row per
 // thread) and half (w - 2) / 4 of the tile's 32-column chunks.
 constexpr int kEpiThreads = 256;
 
-// Shared-memory layout and barrier indices. Both epilogues stage the tile's
-// output (up to 128 x 256 bf16, 64 KB) in shared memory for TMA stores, and the
-// norm epilogue first loads the tile's residual rows into the same buffer; it
-// costs one ring stage (4 -> 3).
+// Shared-memory layout and barrier indices. The norm epilogue loads the tile's
+// residual rows (up to 128 x 256 bf16, 64 KB) into a staging buffer and writes
+// its output over them for TMA stores, which leaves room for three ring stages.
+// The store epilogue gives each epilogue warp a 4 KB buffer of its own (32 rows
+// x 64 columns, one TMA store box), 32 KB in all: each warp stores its rows as
+// soon as it has written them, without waiting for the other warps, and the
+// ring keeps a fourth stage.
 template <bool kNorm>
 struct Layout {
-    static constexpr int kStages = 3;
+    static constexpr int kStages = kNorm ? 3 : 4;
     static constexpr int kBarFull = 0;
     static constexpr int kBarEmpty = kStages;
     static constexpr int kBarAccFull = 2 * kStages;       // 2: accumulator b holds a finished tile
@@ -68,17 +73,18 @@ struct Layout {
     static constexpr int kBarSq = 2 * kStages + 5;        // the peer's squared deviations arrived
     static constexpr int kBarDrain = 2 * kStages + 6;
     static constexpr int kBarXFull = 2 * kStages + 7;     // norm: the tile's residual rows landed
-    static constexpr int kBarXEmpty = 2 * kStages + 8;    // the staging buffer's TMA stores have read it
-    static constexpr int kBarYReady = 2 * kStages + 9;    // every epilogue warp wrote its output rows
+    static constexpr int kBarXEmpty = 2 * kStages + 8;    // norm: the staging buffer's TMA stores have read it
+    static constexpr int kBarYReady = 2 * kStages + 9;    // norm: every epilogue warp wrote its output rows
     static constexpr int kBarEpi = 2 * kStages + 10;      // epilogue rendezvous (row statistics)
     static constexpr int kNumBars = 2 * kStages + 11;
-    static constexpr int kOffX = kStages * kStageBytes;  // staging: 4 boxes of 128 rows x 64 columns
-    static constexpr int kXBytes = 4 * kABoxBytes;
+    static constexpr int kOffX = kStages * kStageBytes;  // staging (1024-byte aligned)
+    // norm: 4 boxes of 128 rows x 64 columns; store: 8 per-warp boxes of 32 x 64
+    static constexpr int kXBytes = kNorm ? 4 * kABoxBytes : 8 * kWarpBoxBytes;
     static constexpr int kOffBar = kOffX + kXBytes;
-    // float recv_sum[128], recv_sq[128] (16-byte aligned, as are the vectors after them)
+    // norm: float recv_sum[128], recv_sq[128] (16-byte aligned, as are the vectors after them)
     static constexpr int kOffStat = (kOffBar + 8 * kNumBars + 15) / 16 * 16;
     // norm: gamma, beta and bias of this CTA's columns (fp32, up to 256 each)
-    static constexpr int kOffVec = kOffStat + 2 * kBM * 4;
+    static constexpr int kOffVec = kOffStat + (kNorm ? 2 * kBM * 4 : 0);
     static constexpr int kVecBytes = kNorm ? 3 * kBN * 4 : 0;
     // norm: the two column halves' partial row sums and squared deviations
     // (float part[2][2][128]), the merged row mean and 1/std (float[2][128]), and
@@ -389,54 +395,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int c_begin = hf * ((nchunks + 1) / 2);
             const int c_end = min(nchunks, c_begin + (nchunks + 1) / 2);
             if constexpr (!kNorm) {
-                // The previous tile's TMA stores must have read the staging buffer.
-                {
-                    const bool got = mbar_wait(bar(Lay::kBarXEmpty), (i & 1) ^ 1);
-                    ok = __all_sync(0xffffffffu, got);
-                }
-                if (!ok) break;
-                // Row r of staging box j sits at kOffX + j * 16 KB + r * 128 B, its 16-byte
-                // chunks permuted by the 128-byte swizzle (chunk k at k ^ (r % 8)).
-                uint8_t* ybase = smem + Lay::kOffX + r * 128;
+                // Whole 64-column boxes per warp: half hf takes boxes [jb_begin, jb_end).
+                // Each box goes through the warp's own 32-row staging buffer (row `lane`
+                // at lane * 128 B, 16-byte chunk k at k ^ (lane % 8) by the 128-byte
+                // swizzle) and one TMA store of the warp's 32 rows (rows past M are
+                // clipped by the map); the buffer is rewritten once that store has read it.
+                const int nbox = g.bn / 64;
+                const int jb_begin = hf * ((nbox + 1) / 2);
+                const int jb_end = min(nbox, jb_begin + (nbox + 1) / 2);
+                uint8_t* wbuf = smem + Lay::kOffX + (warp - 2) * kWarpBoxBytes;
+                const uint32_t wbuf_s = sbase + Lay::kOffX + (warp - 2) * kWarpBoxBytes;
                 const bool relu = pr.relu != 0;
-                for (int c = c_begin; c < c_end; ++c) {
-                    uint32_t v[32];
-                    tmem_ld_x32(acc + 32 * c, v);
-                    if (pr.bias) {
+                const CUtensorMap* cm = pick(g.p, &c0, &c1, &c2);
+                for (int jb = jb_begin; jb < jb_end; ++jb) {
+                    if (lane == 0) bulk_wait_group_read_all();
+                    __syncwarp();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            v[e] = __float_as_uint(__uint_as_float(v[e]) + __ldg(pr.bias + g.n0 + 32 * c + e));
-                    }
-                    if (relu) {
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int c = 2 * jb + h2;
+                        uint32_t v[32];
+                        tmem_ld_x32(acc + 32 * c, v);
+                        if (pr.bias) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(fmaxf(__uint_as_float(v[e]), 0.0f));
-                    }
+                            for (int e = 0; e < 32; ++e)
+                                v[e] = __float_as_uint(__uint_as_float(v[e]) + __ldg(pr.bias + g.n0 + 32 * c + e));
+                        }
+                        if (relu) {
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        const int kc = (c % 2) * 4 + v4;
-                        *reinterpret_cast<uint4*>(ybase + (c / 2) * kABoxBytes + ((kc ^ (r & 7)) * 16)) =
-                            make_uint4(pack_bf16x2(__uint_as_float(v[8 * v4]), __uint_as_float(v[8 * v4 + 1])),
-                                       pack_bf16x2(__uint_as_float(v[8 * v4 + 2]), __uint_as_float(v[8 * v4 + 3])),
-                                       pack_bf16x2(__uint_as_float(v[8 * v4 + 4]), __uint_as_float(v[8 * v4 + 5])),
-                                       pack_bf16x2(__uint_as_float(v[8 * v4 + 6]), __uint_as_float(v[8 * v4 + 7])));
+                            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(fmaxf(__uint_as_float(v[e]), 0.0f));
+                        }
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            const int kc = h2 * 4 + v4;
+                            *reinterpret_cast<uint4*>(wbuf + lane * 128 + ((kc ^ (lane & 7)) * 16)) =
+                                make_uint4(pack_bf16x2(__uint_as_float(v[8 * v4]), __uint_as_float(v[8 * v4 + 1])),
+                                           pack_bf16x2(__uint_as_float(v[8 * v4 + 2]), __uint_as_float(v[8 * v4 + 3])),
+                                           pack_bf16x2(__uint_as_float(v[8 * v4 + 4]), __uint_as_float(v[8 * v4 + 5])),
+                                           pack_bf16x2(__uint_as_float(v[8 * v4 + 6]), __uint_as_float(v[8 * v4 + 7])));
+                        }
                     }
-                }
-                // All rows written (made visible to the async proxy): one thread stores the
-                // tile (rows past M are clipped by the map) and, once the stores have read
-                // the buffer, frees it for the next tile.
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(Lay::kBarYReady));
-                if (warp == 2 && lane == 0) {
-                    if (mbar_wait(bar(Lay::kBarYReady), i & 1)) {
-                        const CUtensorMap* cm = pick(g.p, &c0, &c1, &c2);
-                        for (int j = 0; j < nchunks / 2; ++j)
-                            tma_store_2d(cm, sbase + Lay::kOffX + j * kABoxBytes, g.n0 + 64 * j, g.m0);
+                    // The warp's rows are written (and visible to the async proxy): one lane
+                    // stores the box.
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(cm, wbuf_s, g.n0 + 64 * jb, g.m0 + 32 * q);
                         bulk_commit_group();
-                        bulk_wait_group_read_all();
-                        mbar_arrive(bar(Lay::kBarXEmpty));
-                    } else {
-                        raise_device_error(p.err_word, HATTN_ETIMEOUT);
                     }
                 }
             } else {
@@ -449,8 +453,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Row r of residual box j sits at kOffX + j * 16 KB + r * 128 B, its 16-byte
                 // chunks permuted by the 128-byte swizzle (chunk k at k ^ (r % 8)).
                 const uint8_t* xbase = smem + Lay::kOffX + r * 128;
-                // Pass 1: z = acc [+ bias] + x, kept in TMEM; partial row sum.
-                float sum = 0.0f;
+                // Pass 1: z = acc [+ bias] + x, written back to TMEM, and the sums of
+                // (z - s) and (z - s)^2 over this thread's columns about a shift s near the
+                // row's values (its first residual value plus bias): the shifted-data form
+                // of the mean and squared deviations, one pass without the cancellation of
+                // a plain sum of squares. Paired fp32 instructions take two columns each.
+                const float* biasv = reinterpret_cast<const float*>(smem + Lay::kOffVec + 2 * kBN * 4);
+                const float shift = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                                        xbase + (c_begin / 2) * kABoxBytes + ((((c_begin % 2) * 4) ^ (r & 7)) * 16))) +
+                                    biasv[32 * c_begin];
+                const uint64_t nshift2 = f32x2(-shift, -shift);
+                uint64_t s1[2] = {0, 0}, s2[2] = {0, 0};
                 for (int c = c_begin; c < c_end; ++c) {
                     uint32_t z[32];
                     tmem_ld_x32(acc + 32 * c, z);
@@ -460,44 +473,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int kc = (c % 2) * 4 + v4;
                         xv[v4] = *reinterpret_cast<const uint4*>(xbase + (c / 2) * kABoxBytes + ((kc ^ (r & 7)) * 16));
                     }
-                    const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(xv);
-                    const float4* bias4 = reinterpret_cast<const float4*>(smem + Lay::kOffVec + 2 * kBN * 4) + 8 * c;
+                    const uint32_t* xw = reinterpret_cast<const uint32_t*>(xv);
+                    const float2* bias2 = reinterpret_cast<const float2*>(biasv + 32 * c);
 #pragma unroll
-                    for (int e4 = 0; e4 < 8; ++e4) {
-                        const float4 bv = bias4[e4];
-                        const float bb[4] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int e = 4 * e4 + u;
-                            const float zi = __uint_as_float(z[e]) + __bfloat162float(xb[e]) + bb[u];
-                            sum += zi;
-                            z[e] = __float_as_uint(zi);
-                        }
+                    for (int e2 = 0; e2 < 16; ++e2) {
+                        // A bf16 pair widens exactly: each half is the top of an fp32.
+                        const uint64_t x2 = f32x2(__uint_as_float(xw[e2] << 16), __uint_as_float(xw[e2] & 0xffff0000u));
+                        const float2 bv = bias2[e2];
+                        uint64_t z2 = add_f32x2(f32x2(__uint_as_float(z[2 * e2]), __uint_as_float(z[2 * e2 + 1])), x2);
+                        z2 = add_f32x2(z2, f32x2(bv.x, bv.y));
+                        const uint64_t d2 = add_f32x2(z2, nshift2);
+                        s1[e2 & 1] = add_f32x2(s1[e2 & 1], d2);
+                        s2[e2 & 1] = fma_f32x2(d2, d2, s2[e2 & 1]);
+                        float z0, z1;
+                        f32x2_split(z2, z0, z1);
+                        z[2 * e2] = __float_as_uint(z0);
+                        z[2 * e2 + 1] = __float_as_uint(z1);
                     }
                     tmem_st_x32(acc + 32 * c, z);
                 }
                 tmem_st_wait();
-                // The two column halves' sums give this CTA's row sum.
+                float t0, t1, u0, u1;
+                f32x2_split(add_f32x2(s1[0], s1[1]), t0, t1);
+                f32x2_split(add_f32x2(s2[0], s2[1]), u0, u1);
+                const float n_t = static_cast<float>(32 * (c_end - c_begin));
+                const float d1 = t0 + t1;
+                const float m_t = shift + d1 / n_t;
+                const float q_t = fmaxf((u0 + u1) - d1 * (d1 / n_t), 0.0f);
+                // The two column halves' (mean, squared deviations) merge pairwise into this
+                // CTA's: M2 = M2_a + M2_b + (m_a - m_b)^2 n_a n_b / (n_a + n_b).
                 float* part = reinterpret_cast<float*>(smem + Lay::kOffPart);
-                part[hf * kBM + r] = sum;
+                part[(2 * hf) * kBM + r] = m_t;
+                part[(2 * hf + 1) * kBM + r] = q_t;
                 epi_sync();
-                sum = part[r] + part[kBM + r];
-                // Pass 2: squared deviations about this CTA's own mean (two passes, robust).
-                const float n_own = static_cast<float>(g.bn);
-                const float m_own = sum / n_own;
-                float sq = 0.0f;
-                for (int c = c_begin; c < c_end; ++c) {
-                    uint32_t z[32];
-                    tmem_ld_x32(acc + 32 * c, z);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float dz = __uint_as_float(z[e]) - m_own;
-                        sq = fmaf(dz, dz, sq);
-                    }
-                }
-                part[(2 + hf) * kBM + r] = sq;
-                epi_sync();
-                sq = part[2 * kBM + r] + part[3 * kBM + r];
+                const int hc = (nchunks + 1) / 2;
+                const float n_a = static_cast<float>(32 * hc), n_b = static_cast<float>(32 * (nchunks - hc));
+                const float m_a = part[r], q_a = part[kBM + r], m_b = part[2 * kBM + r], q_b = part[3 * kBM + r];
+                const float n_own = n_a + n_b;
+                const float m_own = (n_a * m_a + n_b * m_b) / n_own;
+                float sq = q_a + q_b + (m_a - m_b) * (m_a - m_b) * (n_a * n_b / n_own);
                 // Half 0 merges the row with the peer CTA's half-row and shares the result.
                 float* rowstat = reinterpret_cast<float*>(smem + Lay::kOffRow);
                 if (hf == 0) {
@@ -519,24 +533,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 epi_sync();
                 ok = ld_volatile_shared(sbase + Lay::kOffFail) == 0u;
                 const float mean = rowstat[r], rstd = rowstat[kBM + r];
-                // Pass 3: normalise, scale, shift, round once to bf16, into the residual
+                // Pass 2: normalise, scale, shift, round once to bf16, into the residual
                 // buffer (same swizzled 128 x 64 boxes), which TMA then stores.
                 const float4* gam4 = reinterpret_cast<const float4*>(smem + Lay::kOffVec);
                 const float4* bet4 = reinterpret_cast<const float4*>(smem + Lay::kOffVec + kBN * 4);
                 uint8_t* ybase = smem + Lay::kOffX + r * 128;
+                // y = (z - mean) rstd gamma + beta = z g + (beta - mean g), g = rstd gamma.
+                const uint64_t rstd2 = f32x2(rstd, rstd), nmean2 = f32x2(-mean, -mean);
                 for (int c = c_begin; ok && c < c_end; ++c) {
                     uint32_t z[32];
                     tmem_ld_x32(acc + 32 * c, z);
+                    const float2* gam2 = reinterpret_cast<const float2*>(gam4) + 16 * c;
+                    const float2* bet2 = reinterpret_cast<const float2*>(bet4) + 16 * c;
                     uint32_t w[16];
 #pragma unroll
-                    for (int e4 = 0; e4 < 8; ++e4) {
-                        const float4 gv = gam4[8 * c + e4], bv = bet4[8 * c + e4];
-                        const float y0 = (__uint_as_float(z[4 * e4]) - mean) * rstd * gv.x + bv.x;
-                        const float y1 = (__uint_as_float(z[4 * e4 + 1]) - mean) * rstd * gv.y + bv.y;
-                        const float y2 = (__uint_as_float(z[4 * e4 + 2]) - mean) * rstd * gv.z + bv.z;
-                        const float y3 = (__uint_as_float(z[4 * e4 + 3]) - mean) * rstd * gv.w + bv.w;
-                        w[2 * e4] = pack_bf16x2(y0, y1);
-                        w[2 * e4 + 1] = pack_bf16x2(y2, y3);
+                    for (int e2 = 0; e2 < 16; ++e2) {
+                        const float2 gv = gam2[e2], bv = bet2[e2];
+                        const uint64_t sc2 = mul_f32x2(rstd2, f32x2(gv.x, gv.y));
+                        const uint64_t of2 = fma_f32x2(nmean2, sc2, f32x2(bv.x, bv.y));
+                        const uint64_t y2 =
+                            fma_f32x2(f32x2(__uint_as_float(z[2 * e2]), __uint_as_float(z[2 * e2 + 1])), sc2, of2);
+                        float y0, y1;
+                        f32x2_split(y2, y0, y1);
+                        w[e2] = pack_bf16x2(y0, y1);
                     }
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4) {
@@ -570,7 +589,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(bar(Lay::kBarAccEmpty + b));
         }
         if (!ok) raise_device_error(p.err_word, HATTN_ETIMEOUT);
-        if (warp == 2 && lane == 0) bulk_wait_group_all();
+        // Every TMA store this warp issued has completed before the CTA exits.
+        if (lane == 0) bulk_wait_group_all();
     }
 
     tc_fence_before();

@@ -115,7 +115,7 @@ cudaError_t launch_attn_decode(const DecodeLaunch& a);
 struct ProjProblem {
     CUtensorMap a;  // A [M][K], 64 x 128 boxes, K-major
     CUtensorMap w;  // W [K][N], 64 x 64 boxes, N-major
-    CUtensorMap cmap;  // C [M][N], 64 x 128 boxes: the output, stored by TMA
+    CUtensorMap cmap;  // C [M][N], 64 x 32 boxes: the output, stored by TMA (one box per epilogue warp)
     void* c;        // bf16 [M][N]
     int M, N, K;
     const float* bias = nullptr;  // optional fp32 [N], added to every row
