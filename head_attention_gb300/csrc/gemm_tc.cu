@@ -69,8 +69,7 @@ struct Layout {
     static constexpr int kBarEmpty = kStages;
     static constexpr int kBarAccFull = 2 * kStages;       // 2: accumulator b holds a finished tile
     static constexpr int kBarAccEmpty = 2 * kStages + 2;  // 2: the epilogue has read accumulator b
-    static constexpr int kBarSum = 2 * kStages + 4;       // the peer's per-row partial sums arrived
-    static constexpr int kBarSq = 2 * kStages + 5;        // the peer's squared deviations arrived
+    static constexpr int kBarXchg = 2 * kStages + 4;      // 2: the peer's row statistics arrived (tile parity)
     static constexpr int kBarDrain = 2 * kStages + 6;
     static constexpr int kBarXFull = 2 * kStages + 7;     // norm: the tile's residual rows landed
     static constexpr int kBarXEmpty = 2 * kStages + 8;    // norm: the staging buffer's TMA stores have read it
@@ -81,10 +80,12 @@ struct Layout {
     // norm: 4 boxes of 128 rows x 64 columns; store: 8 per-warp boxes of 32 x 64
     static constexpr int kXBytes = kNorm ? 4 * kABoxBytes : 8 * kWarpBoxBytes;
     static constexpr int kOffBar = kOffX + kXBytes;
-    // norm: float recv_sum[128], recv_sq[128] (16-byte aligned, as are the vectors after them)
+    // norm: float2 recv[2][128], the peer's (mean, M2) per row by tile parity (16-byte
+    // aligned, as are the vectors after them)
     static constexpr int kOffStat = (kOffBar + 8 * kNumBars + 15) / 16 * 16;
+    static constexpr uint32_t kXchgBytes = 8 * kBM;  // one (mean, M2) pair per row
     // norm: gamma, beta and bias of this CTA's columns (fp32, up to 256 each)
-    static constexpr int kOffVec = kOffStat + (kNorm ? 2 * kBM * 4 : 0);
+    static constexpr int kOffVec = kOffStat + (kNorm ? 2 * kXchgBytes : 0);
     static constexpr int kVecBytes = kNorm ? 3 * kBN * 4 : 0;
     // norm: the two column halves' partial row sums and squared deviations
     // (float part[2][2][128]), the merged row mean and 1/std (float[2][128]), and
@@ -178,27 +179,26 @@ __device__ __forceinline__ float ld_volatile_shared_f32(uint32_t addr)
     return __uint_as_float(ld_volatile_shared(addr));
 }
 
-// Sends this row's partial `v` to the peer CTA of the pair and returns the
-// peer's partial for the same row. Each exchange barrier completes once per
-// tile: the peer's next arrival on it needs this CTA's next exchange, which
-// happens only after this one has been read.
-// Sends this row's (a, b) to the peer CTA of the pair and returns the peer's
-// pair for the same row; the exchange barrier completes once per tile (the
-// peer's next arrival needs this CTA's next exchange, after this one was read).
+// Sends this row's (a, b) to the peer CTA of the pair and returns the peer's pair
+// for the same row. The pair travels by st.async, which completes its 8 bytes on the
+// peer's exchange barrier; each CTA's barrier expects all 128 rows' bytes (armed
+// once per phase by one thread, for the tile two ahead once it has been read). Even
+// and odd tiles use their own barrier and slots, so the peer's next exchange (which
+// needs all of this CTA's rows of the next tile, hence all of them past this one)
+// never meets a phase or a slot still in use.
 template <bool kNorm>
 __device__ __forceinline__ bool exchange_pair(float a, float b, float& peer_a, float& peer_b,
-                                              uint32_t sbase, uint32_t parity, int r, uint32_t peer)
+                                              uint32_t sbase, uint32_t tile, int r, uint32_t peer)
 {
     using Lay = Layout<kNorm>;
-    const uint32_t slot_a = sbase + Lay::kOffStat + 4u * r;
-    const uint32_t slot_b = slot_a + 4u * kBM;
-    const uint32_t bar = sbase + Lay::kOffBar + 8u * Lay::kBarSum;
-    st_cluster_f32(mapa_shared(slot_a, peer), a);
-    st_cluster_f32(mapa_shared(slot_b, peer), b);
-    mbar_arrive_cluster(mapa_shared(bar, peer));
-    if (!mbar_wait_cluster(bar, parity)) return false;
-    peer_a = ld_volatile_shared_f32(slot_a);
-    peer_b = ld_volatile_shared_f32(slot_b);
+    const uint32_t k = tile & 1u;
+    const uint32_t slot = sbase + Lay::kOffStat + k * Lay::kXchgBytes + 8u * r;
+    const uint32_t bar = sbase + Lay::kOffBar + 8u * (Lay::kBarXchg + k);
+    st_async_f32x2(mapa_shared(slot, peer), a, b, mapa_shared(bar, peer));
+    if (!mbar_wait_cluster(bar, (tile >> 1) & 1u)) return false;
+    peer_a = ld_volatile_shared_f32(slot);
+    peer_b = ld_volatile_shared_f32(slot + 4u);
+    if (r == 0) mbar_arrive_expect_tx(bar, Lay::kXchgBytes);
     return true;
 }
 
@@ -231,14 +231,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(Lay::kBarAccEmpty + b), kEpiThreads / 32);
         }
         // One remote arrival per row (the column-half-0 warps exchange).
-        mbar_init(bar(Lay::kBarSum), kBM);
-        mbar_init(bar(Lay::kBarSq), kBM);
+        // Each exchange barrier: one arrival with the 128 rows' bytes expected, armed
+        // here for tiles 0 and 1 (the peer's stores need the cluster barrier below).
+        for (int k = 0; k < 2; ++k) mbar_init(bar(Lay::kBarXchg + k), 1);
         mbar_init(bar(Lay::kBarDrain), 1);
         mbar_init(bar(Lay::kBarXFull), 1);
         mbar_init(bar(Lay::kBarXEmpty), 1);
         mbar_init(bar(Lay::kBarYReady), kEpiThreads / 32);
         mbar_init(bar(Lay::kBarEpi), kEpiThreads / 32);
         st_volatile_shared(sbase + Lay::kOffFail, 0u);
+        if (kNorm)
+            for (int k = 0; k < 2; ++k) mbar_arrive_expect_tx(bar(Lay::kBarXchg + k), Lay::kXchgBytes);
         fence_barrier_init();
     }
     if (warp == kWarpMma) {
@@ -520,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // One exchange of (mean, M2) with the peer's half of the row, merged by
                         // the pairwise formula: M2 = M2_a + M2_b + (m_a - m_b)^2 n_a n_b / N.
                         float m_peer = 0.0f, sq_peer = 0.0f;
-                        const bool got = exchange_pair<kNorm>(m_own, sq, m_peer, sq_peer, sbase, i & 1, r, peer);
+                        const bool got = exchange_pair<kNorm>(m_own, sq, m_peer, sq_peer, sbase, i, r, peer);
                         if (!__all_sync(0xffffffffu, got) && lane == 0) st_volatile_shared(sbase + Lay::kOffFail, 1u);
                         const float n_peer = static_cast<float>(N) - n_own;
                         const float delta = m_own - m_peer;

@@ -110,6 +110,17 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t cluster_addr, float v)
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
 }
 
+// Writes the pair (a, b) to shared memory of a CTA of the cluster (8-byte
+// aligned address from mapa_shared) and completes 8 transaction bytes on that
+// CTA's mbarrier at cluster_bar; the data is visible to whoever observes the
+// barrier's phase complete.
+__device__ __forceinline__ void st_async_f32x2(uint32_t cluster_addr, float a, float b, uint32_t cluster_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+                 ::"r"(cluster_addr), "f"(a), "f"(b), "r"(cluster_bar)
+                 : "memory");
+}
+
 // Arrive on an mbarrier of another CTA of the cluster; release at cluster
 // scope orders this thread's earlier writes (e.g. st_cluster_f32) before it.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)

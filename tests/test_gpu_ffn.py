@@ -76,6 +76,25 @@ def test_ffn_matches_oracle(M, dm, dff, biases):
     assert_close(from_device(y), ref, "bf16", f"ffn {M} {dm} {dff}")
 
 
+@pytest.mark.parametrize("offset", [8.0, -60.0])
+def test_ffn_layernorm_rows_far_from_zero(offset):
+    # Rows whose values sit far from zero (x = offset + N(0, 1)): the LayerNorm's mean and
+    # variance must come out without cancellation (a plain sum of squares in fp32 would
+    # lose the variance against offset^2).
+    hattn.build()
+    M, dm, dff = 640, 512, 512
+    w = synth.Workload("ffn_offset", "bf16", B=1, h=1, n_q=M, n_k=M, d_k=64, d_v=64, mask_kind=0,
+                       seed=77, d_model=dm, d_ff=dff, kind="encoder")
+    f = synth.ffn_inputs(w)
+    x = synth.round_to_bf16_bits(offset + synth.draw_normal(w.seed, synth.STREAM_XQ, (M, dm)))
+    d = _dev_ffn(f)
+    y = hattn.ffn_fwd(to_device(x, "bf16"), d["w1"], d["b1"], d["w2"], d["b2"], d["gamma"],
+                      d["beta"], f["eps"])
+    torch().cuda.synchronize()
+    assert hattn.check_device_error() == 0
+    assert_close(from_device(y), _oracle_ffn(_w(x), f), "bf16", f"ffn offset {offset}")
+
+
 @pytest.mark.parametrize("padding", [False, True])
 def test_encoder_layer_matches_oracle(padding):
     w = synth.Workload("enc_case", "bf16", B=2, h=2, n_q=200, n_k=200, d_k=64, d_v=64,

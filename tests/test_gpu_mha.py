@@ -60,3 +60,25 @@ def test_mha_shapes(B, n_q, n_k, d_model, h, d, mask_kind, cross):
     inp["gamma"] = rng.uniform(0.5, 1.5, d_model).astype(np.float32)
     inp["beta"] = rng.uniform(-0.5, 0.5, d_model).astype(np.float32)
     assert_close(run_mha(w, inp), oracle_mha(w, inp), "bf16", f"mha {B} {n_q} {n_k} {d_model}")
+
+
+def test_mha_several_row_tiles_per_cta():
+    # 24 x 1024 rows: 192 row tiles of 128, so every CTA pair of the LayerNorm GEMM takes
+    # two or three tiles (both exchange barriers, several phases each) and the projection
+    # GEMM's CTAs take up to ten. No row depends on which CTA or tile computed it, so the
+    # result must equal, bit for bit, three launches of 8 x 1024 rows (one row tile per
+    # CTA pair); one of those is held to the oracle.
+    w = synth.Workload("mha_many_tiles", "bf16", B=24, h=8, n_q=1024, n_k=1024, d_k=64, d_v=64,
+                       mask_kind=synth.MASK_NONE, seed=612, d_model=512, kind="mha")
+    inp = synth.mha_inputs(w)
+    y_all = run_mha(w, inp)
+    for k in range(3):
+        wk = synth.Workload("mha_many_tiles", "bf16", B=8, h=8, n_q=1024, n_k=1024, d_k=64, d_v=64,
+                            mask_kind=synth.MASK_NONE, seed=612, d_model=512, kind="mha")
+        part = dict(inp)
+        part["x_q"] = part["x_kv"] = inp["x_q"][8 * k:8 * k + 8]
+        y_k = run_mha(wk, part)
+        # (bf16 results widened exactly to fp64: equal arrays are equal bits)
+        assert np.array_equal(y_all[8 * k:8 * k + 8], y_k), f"rows of batch slice {k} differ"
+        if k == 0:
+            assert_close(y_k, oracle_mha(wk, part), "bf16", "mha 8 x 1024")
