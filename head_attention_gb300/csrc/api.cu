@@ -341,7 +341,7 @@ int mha_fwd(const void* x_q, const void* x_kv, const void* Wq, const void* Wk, c
 
     OutProjLnArgs o;
     if (!make_2d_map(&o.a, A, Mq, hdv, 128) || !make_2d_map(&o.wo, Wo, hdv, d_model, 64) ||
-        !make_2d_map(&o.xmap, x_q, Mq, d_model, 128) || !make_2d_map(&o.ymap, y, Mq, d_model, 128))
+        !make_2d_map(&o.xmap, x_q, Mq, d_model, 128) || !make_2d_map(&o.ymap, y, Mq, d_model, 32))
         return HATTN_ECUDA;
     o.x = x_q;
     o.gamma = gamma;
@@ -583,7 +583,7 @@ int ffn_fwd(const void* x, const void* W1, const float* b1, const void* W2, cons
     // y = LN(x + H W2 + b2)
     OutProjLnArgs o;
     if (!make_2d_map(&o.a, H, M, d_ff, 128) || !make_2d_map(&o.wo, W2, d_ff, d_model, 64) ||
-        !make_2d_map(&o.xmap, x, M, d_model, 128) || !make_2d_map(&o.ymap, y, M, d_model, 128))
+        !make_2d_map(&o.xmap, x, M, d_model, 128) || !make_2d_map(&o.ymap, y, M, d_model, 32))
         return HATTN_ECUDA;
     o.x = x;
     o.gamma = gamma;

@@ -72,10 +72,9 @@ struct Layout {
     static constexpr int kBarXchg = 2 * kStages + 4;      // 2: the peer's row statistics arrived (tile parity)
     static constexpr int kBarDrain = 2 * kStages + 6;
     static constexpr int kBarXFull = 2 * kStages + 7;     // norm: the tile's residual rows landed
-    static constexpr int kBarXEmpty = 2 * kStages + 8;    // norm: the staging buffer's TMA stores have read it
-    static constexpr int kBarYReady = 2 * kStages + 9;    // norm: every epilogue warp wrote its output rows
-    static constexpr int kBarEpi = 2 * kStages + 10;      // epilogue rendezvous (row statistics)
-    static constexpr int kNumBars = 2 * kStages + 11;
+    static constexpr int kBarXEmpty = 2 * kStages + 8;    // norm: every warp's TMA stores have read the staging buffer
+    static constexpr int kBarEpi = 2 * kStages + 9;       // epilogue rendezvous (row statistics)
+    static constexpr int kNumBars = 2 * kStages + 10;
     static constexpr int kOffX = kStages * kStageBytes;  // staging (1024-byte aligned)
     // norm: 4 boxes of 128 rows x 64 columns; store: 8 per-warp boxes of 32 x 64
     static constexpr int kXBytes = kNorm ? 4 * kABoxBytes : 8 * kWarpBoxBytes;
@@ -236,8 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 2; ++k) mbar_init(bar(Lay::kBarXchg + k), 1);
         mbar_init(bar(Lay::kBarDrain), 1);
         mbar_init(bar(Lay::kBarXFull), 1);
-        mbar_init(bar(Lay::kBarXEmpty), 1);
-        mbar_init(bar(Lay::kBarYReady), kEpiThreads / 32);
+        mbar_init(bar(Lay::kBarXEmpty), kEpiThreads / 32);
         mbar_init(bar(Lay::kBarEpi), kEpiThreads / 32);
         st_volatile_shared(sbase + Lay::kOffFail, 0u);
         if (kNorm)
@@ -393,19 +391,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t acc = lane_base + 256u * b;
-            const int nchunks = g.bn / 32;
             // This warp's chunks: the first or the second half of the tile's columns.
-            const int c_begin = hf * ((nchunks + 1) / 2);
-            const int c_end = min(nchunks, c_begin + (nchunks + 1) / 2);
+            // Whole 64-column boxes per warp: half hf takes boxes [jb_begin, jb_end), i.e.
+            // chunks [c_begin, c_end) (the second half may be empty for a one-box tile).
+            const int nbox = g.bn / 64;
+            const int hb = (nbox + 1) / 2;
+            const int jb_begin = min(nbox, hf * hb);
+            const int jb_end = min(nbox, jb_begin + hb);
+            const int c_begin = 2 * jb_begin, c_end = 2 * jb_end;
             if constexpr (!kNorm) {
-                // Whole 64-column boxes per warp: half hf takes boxes [jb_begin, jb_end).
                 // Each box goes through the warp's own 32-row staging buffer (row `lane`
                 // at lane * 128 B, 16-byte chunk k at k ^ (lane % 8) by the 128-byte
                 // swizzle) and one TMA store of the warp's 32 rows (rows past M are
                 // clipped by the map); the buffer is rewritten once that store has read it.
-                const int nbox = g.bn / 64;
-                const int jb_begin = hf * ((nbox + 1) / 2);
-                const int jb_end = min(nbox, jb_begin + (nbox + 1) / 2);
                 uint8_t* wbuf = smem + Lay::kOffX + (warp - 2) * kWarpBoxBytes;
                 const uint32_t wbuf_s = sbase + Lay::kOffX + (warp - 2) * kWarpBoxBytes;
                 const bool relu = pr.relu != 0;
@@ -499,18 +497,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float t0, t1, u0, u1;
                 f32x2_split(add_f32x2(s1[0], s1[1]), t0, t1);
                 f32x2_split(add_f32x2(s2[0], s2[1]), u0, u1);
+                // (A half without columns contributes nothing: weight 0 in the merge.)
                 const float n_t = static_cast<float>(32 * (c_end - c_begin));
                 const float d1 = t0 + t1;
-                const float m_t = shift + d1 / n_t;
-                const float q_t = fmaxf((u0 + u1) - d1 * (d1 / n_t), 0.0f);
+                const float m_t = n_t > 0.0f ? shift + d1 / n_t : 0.0f;
+                const float q_t = n_t > 0.0f ? fmaxf((u0 + u1) - d1 * (d1 / n_t), 0.0f) : 0.0f;
                 // The two column halves' (mean, squared deviations) merge pairwise into this
                 // CTA's: M2 = M2_a + M2_b + (m_a - m_b)^2 n_a n_b / (n_a + n_b).
                 float* part = reinterpret_cast<float*>(smem + Lay::kOffPart);
                 part[(2 * hf) * kBM + r] = m_t;
                 part[(2 * hf + 1) * kBM + r] = q_t;
                 epi_sync();
-                const int hc = (nchunks + 1) / 2;
-                const float n_a = static_cast<float>(32 * hc), n_b = static_cast<float>(32 * (nchunks - hc));
+                const float n_a = static_cast<float>(64 * min(nbox, hb)), n_b = static_cast<float>(64 * (nbox - min(nbox, hb)));
                 const float m_a = part[r], q_a = part[kBM + r], m_b = part[2 * kBM + r], q_b = part[3 * kBM + r];
                 const float n_own = n_a + n_b;
                 const float m_own = (n_a * m_a + n_b * m_b) / n_own;
@@ -567,22 +565,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                             make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
                     }
                 }
-                // All rows written (each warp's writes made visible to the async proxy):
-                // one thread stores the tile (map a2) and, once the stores have read the
-                // buffer, frees it for the next tile's residual.
+                // The warp's rows are written (and visible to the async proxy): one lane
+                // stores the warp's 32 rows of each of its boxes (map a2, 32-row boxes)
+                // and, once those stores have read shared memory, counts the warp out of
+                // the residual buffer, which the next tile's residual may then overwrite.
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(Lay::kBarYReady));
-                if (warp == 2 && lane == 0) {
-                    if (mbar_wait(bar(Lay::kBarYReady), i & 1)) {
-                        for (int j = 0; j < nchunks / 2; ++j)
-                            tma_store_2d(&a2, sbase + Lay::kOffX + j * kABoxBytes, g.n0 + 64 * j, g.m0);
-                        bulk_commit_group();
-                        bulk_wait_group_read_all();
-                        mbar_arrive(bar(Lay::kBarXEmpty));
-                    } else {
-                        raise_device_error(p.err_word, HATTN_ETIMEOUT);
-                    }
+                if (lane == 0) {
+                    for (int jb = jb_begin; jb < jb_end; ++jb)
+                        tma_store_2d(&a2, sbase + Lay::kOffX + jb * kABoxBytes + q * 32 * 128, g.n0 + 64 * jb,
+                                     g.m0 + 32 * q);
+                    bulk_commit_group();
+                    bulk_wait_group_read_all();
+                    mbar_arrive(bar(Lay::kBarXEmpty));
                 }
                 if (!ok) break;
             }

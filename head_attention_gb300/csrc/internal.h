@@ -132,7 +132,7 @@ struct OutProjLnArgs {
     CUtensorMap wo;  // Wo [K][N] bf16, N-major boxes 64 x 64
     const void* x;   // residual, bf16 [M][N]
     CUtensorMap xmap;  // the residual as 64 x 128 boxes (loaded into shared memory by TMA)
-    CUtensorMap ymap;  // the output as 64 x 128 boxes (stored from shared memory by TMA)
+    CUtensorMap ymap;  // the output as 64 x 32 boxes (each epilogue warp stores its rows by TMA)
     const float* gamma;
     const float* beta;
     float eps;
