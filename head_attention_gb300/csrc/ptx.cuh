@@ -105,11 +105,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
     return r;
 }
 
-__device__ __forceinline__ void st_cluster_f32(uint32_t cluster_addr, float v)
-{
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
-}
-
 // Writes the pair (a, b) to shared memory of a CTA of the cluster (8-byte
 // aligned address from mapa_shared) and completes 8 transaction bytes on that
 // CTA's mbarrier at cluster_bar; the data is visible to whoever observes the
@@ -121,16 +116,8 @@ __device__ __forceinline__ void st_async_f32x2(uint32_t cluster_addr, float a, f
                  : "memory");
 }
 
-// Arrive on an mbarrier of another CTA of the cluster; release at cluster
-// scope orders this thread's earlier writes (e.g. st_cluster_f32) before it.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
-{
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-                 : "memory");
-}
-
-// Bounded wait with acquire at cluster scope (sees the writes that the remote
-// arrivals released).
+// Bounded wait with acquire at cluster scope (sees what the remote operations
+// that completed the phase wrote, e.g. st_async_f32x2).
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity)
 {
     const long long t0 = clock64();
