@@ -126,6 +126,21 @@ __global__ void __launch_bounds__(kShortThreads, (D == 64 && NKB == 1) ? 3 : 2)
     // cheaper than that latency. The inputs may come from the previous kernel
     // (programmatic dependent launch), so the grid dependency is waited for first.
     const bool two_blocks = NKB == 2 && p.n_k > 128;
+    // While the previous kernel may still run (programmatic dependent launch), this
+    // head's tiles are only prefetched into L2: inputs that are already in memory
+    // then arrive from L2 once the dependency is met, and inputs the previous kernel
+    // is still writing are simply read again (L2 holds the latest values).
+    if (leader) {
+        for (int x = 0; x < C::kBoxes; ++x) {
+            tma_prefetch_4d(&tm_q, 64 * x, head, 0, b);
+            tma_prefetch_4d(&tm_k, 64 * x, head, 0, b);
+            tma_prefetch_4d(&tm_v, 64 * x, head, 0, b);
+            if (two_blocks) {
+                tma_prefetch_4d(&tm_k, 64 * x, head, 128, b);
+                tma_prefetch_4d(&tm_v, 64 * x, head, 128, b);
+            }
+        }
+    }
     griddep_wait();
     if (leader) {
         mbar_arrive_expect_tx(bar(C::kBarQK0), 2 * C::kTileBytes);

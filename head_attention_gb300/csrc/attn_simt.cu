@@ -122,6 +122,25 @@ __global__ void __launch_bounds__(kThreads)
     const T* v_bh = v + (size_t)b * n_k * v_row_stride + (size_t)head * d_v;
     T* o_bh = out + (size_t)b * n_q * v_row_stride + (size_t)head * d_v;
 
+    // While the previous kernel may still run (programmatic dependent launch): the
+    // rows this CTA will read, into L2 only (Q rows, and the K and V rows its causal
+    // bound allows; the key length may be the previous kernel's output, so n_k).
+    {
+        const int q_end = min(n_q, row0 + kRows);
+        const int k_end = causal ? min(n_k, row0 + kRows) : n_k;
+        const int qk_lines = (d_k * (int)sizeof(T) + 127) / 128, v_lines = (d_v * (int)sizeof(T) + 127) / 128;
+        const int nq = max(0, q_end - row0) * qk_lines, nk = k_end * qk_lines, nv = k_end * v_lines;
+        for (int i = threadIdx.x; i < nq + nk + nv; i += kThreads) {
+            const T* a;
+            if (i < nq) a = q_bh + (size_t)(row0 + i / qk_lines) * qk_row_stride + (i % qk_lines) * (128 / sizeof(T));
+            else if (i < nq + nk) a = k_bh + (size_t)((i - nq) / qk_lines) * qk_row_stride + ((i - nq) % qk_lines) * (128 / sizeof(T));
+            else a = v_bh + (size_t)((i - nq - nk) / v_lines) * v_row_stride + ((i - nq - nk) % v_lines) * (128 / sizeof(T));
+            prefetch_l2(a);
+        }
+    }
+    griddep_wait();
+    griddep_launch_dependents();
+
     int kv_len = n_k;
     if (mask_kind & HATTN_MASK_KEY_PADDING) {
         kv_len = key_lens[b];
@@ -219,12 +238,20 @@ cudaError_t launch_rows(const AttnArgs& a)
     cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel<T, kCols, kMaxRowD, kRows>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((a.n_q + kRows - 1) / kRows, a.h, a.B);
-    attn_simt_kernel<T, kCols, kMaxRowD, kRows><<<grid, kThreads, smem, a.stream>>>(
-        static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v),
-        static_cast<T*>(a.out), a.n_q, a.n_k, a.h, a.d_k, a.d_v, a.scale, a.mask_kind,
-        a.key_lens, a.err_word, a.lse);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((a.n_q + kRows - 1) / kRows, a.h, a.B);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_simt_kernel<T, kCols, kMaxRowD, kRows>, static_cast<const T*>(a.q),
+                              static_cast<const T*>(a.k), static_cast<const T*>(a.v), static_cast<T*>(a.out),
+                              a.n_q, a.n_k, a.h, a.d_k, a.d_v, a.scale, a.mask_kind, a.key_lens, a.err_word,
+                              a.lse);
 }
 
 // 8 query rows per CTA share each staged K/V tile; when that leaves fewer than

@@ -175,6 +175,16 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
+// Prefetch of a 4-D tile into L2 (no shared memory, no completion to wait for).
+// L2 is the point of coherence for device memory, so a prefetch issued before a
+// grid dependency cannot make a later load see stale data: it only warms L2.
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int c0, int c1, int c2, int c3)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
 // 2-D tiled tensor load.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int c0, int c1)
@@ -255,6 +265,13 @@ __device__ __forceinline__ void fence_proxy_async_smem()
 __device__ __forceinline__ void griddep_wait()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Prefetch of the cache line holding addr into L2 (see tma_prefetch_4d on why this
+// is safe ahead of a grid dependency).
+__device__ __forceinline__ void prefetch_l2(const void* addr)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
 }
 
 // Lets the next grid on the stream start launching (its CTAs then run their
