@@ -417,9 +417,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint32_t v[32];
                         tmem_ld_x32(acc + 32 * c, v);
                         if (pr.bias) {
+                            // (16-byte aligned: the entry points check the bias pointers.)
+                            const float4* b4 = reinterpret_cast<const float4*>(pr.bias + g.n0 + 32 * c);
 #pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                v[e] = __float_as_uint(__uint_as_float(v[e]) + __ldg(pr.bias + g.n0 + 32 * c + e));
+                            for (int e4 = 0; e4 < 8; ++e4) {
+                                const float4 bv = __ldg(b4 + e4);
+                                v[4 * e4] = __float_as_uint(__uint_as_float(v[4 * e4]) + bv.x);
+                                v[4 * e4 + 1] = __float_as_uint(__uint_as_float(v[4 * e4 + 1]) + bv.y);
+                                v[4 * e4 + 2] = __float_as_uint(__uint_as_float(v[4 * e4 + 2]) + bv.z);
+                                v[4 * e4 + 3] = __float_as_uint(__uint_as_float(v[4 * e4 + 3]) + bv.w);
+                            }
                         }
                         if (relu) {
 #pragma unroll
@@ -475,12 +482,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         xv[v4] = *reinterpret_cast<const uint4*>(xbase + (c / 2) * kABoxBytes + ((kc ^ (r & 7)) * 16));
                     }
                     const uint32_t* xw = reinterpret_cast<const uint32_t*>(xv);
-                    const float2* bias2 = reinterpret_cast<const float2*>(biasv + 32 * c);
+                    const float4* bias4 = reinterpret_cast<const float4*>(biasv + 32 * c);
 #pragma unroll
                     for (int e2 = 0; e2 < 16; ++e2) {
                         // A bf16 pair widens exactly: each half is the top of an fp32.
                         const uint64_t x2 = f32x2(__uint_as_float(xw[e2] << 16), __uint_as_float(xw[e2] & 0xffff0000u));
-                        const float2 bv = bias2[e2];
+                        const float4 b4 = bias4[e2 / 2];  // one 16-byte load per two pairs
+                        const float2 bv = (e2 & 1) ? make_float2(b4.z, b4.w) : make_float2(b4.x, b4.y);
                         uint64_t z2 = add_f32x2(f32x2(__uint_as_float(z[2 * e2]), __uint_as_float(z[2 * e2 + 1])), x2);
                         z2 = add_f32x2(z2, f32x2(bv.x, bv.y));
                         const uint64_t d2 = add_f32x2(z2, nshift2);
@@ -544,12 +552,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = c_begin; ok && c < c_end; ++c) {
                     uint32_t z[32];
                     tmem_ld_x32(acc + 32 * c, z);
-                    const float2* gam2 = reinterpret_cast<const float2*>(gam4) + 16 * c;
-                    const float2* bet2 = reinterpret_cast<const float2*>(bet4) + 16 * c;
                     uint32_t w[16];
 #pragma unroll
                     for (int e2 = 0; e2 < 16; ++e2) {
-                        const float2 gv = gam2[e2], bv = bet2[e2];
+                        const float4 g4 = gam4[8 * c + e2 / 2], b4 = bet4[8 * c + e2 / 2];
+                        const float2 gv = (e2 & 1) ? make_float2(g4.z, g4.w) : make_float2(g4.x, g4.y);
+                        const float2 bv = (e2 & 1) ? make_float2(b4.z, b4.w) : make_float2(b4.x, b4.y);
                         const uint64_t sc2 = mul_f32x2(rstd2, f32x2(gv.x, gv.y));
                         const uint64_t of2 = fma_f32x2(nmean2, sc2, f32x2(bv.x, bv.y));
                         const uint64_t y2 =
