@@ -12,9 +12,10 @@
 //
 // How. One CTA of four warps per (b, i) head, a straight-line chain without a
 // work loop or a ring: thread r owns query row r (TMEM lane r).
-//   1. Thread 0 issues every TMA load the head may need at once (Q and both key
-//      blocks' K and V, before the key length is read), so one DRAM round trip
-//      covers them all.
+//   1. Thread 0 prefetches the head's tiles into L2 while the previous kernel
+//      may still run, then (past the grid dependency) issues every TMA load the
+//      head may need at once (Q and both key blocks' K and V, before the key
+//      length is read), so one DRAM round trip covers them all.
 //   2. Thread 0 issues S_j = Q K_j^T (tcgen05, M = 128, N = 128) for every
 //      block into TMEM columns [128 j, 128 j + 128).
 //   3. The whole row is visible at once, so the softmax takes two passes over
@@ -25,10 +26,11 @@
 //   4. Thread 0 issues O = sum_j P_j V_j (TS MMAs, P from TMEM, V from shared
 //      memory) into columns [64, 64 + d), i.e. over S_0's second half, which
 //      no thread reads any more.
-//   5. O / l is packed to bf16 into the (no longer needed) Q tile in shared
-//      memory, in the 128-byte swizzled layout of the output tensor map, and
-//      leaves as one TMA store per 64-column box; rows past n_q are clipped by
-//      the map.
+//   5. O / l is packed to bf16. At d = 64 each thread stores its 128-byte row
+//      directly; at d = 128 the tile goes into the (no longer needed) Q tile in
+//      shared memory, in the 128-byte swizzled layout of the output tensor map,
+//      and leaves as one TMA store per 64-column box (rows past n_q clipped by
+//      the map).
 // TMEM: 128 columns at d = 64 with one key block (up to four CTAs per SM),
 // 256 otherwise. Every mbarrier wait is bounded (HATTN_ETIMEOUT on give-up).
 // A key length outside [1, n_k] zeroes the head's output and raises
